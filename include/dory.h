@@ -1,0 +1,210 @@
+/*
+ * dory.h - C ABI of the looped normalized-GPT forward pass on one B300 GPU.
+ *
+ * The operation is the inference forward pass of the looped nGPT described in
+ * "Dory1.0-4B: A Looped Normalized-GPT":
+ *   - Architecture: every hidden state lives on the unit sphere and each
+ *     sublayer moves it with the nGPT residual step
+ *         h <- N(h + alpha * (N(y) - h)),   N(v) = v / ||v||_2 per token;
+ *     grouped-query attention with an input-dependent sigmoid output gate,
+ *     per-head L2-normalised queries and keys, the gated concatenated output
+ *     normalised before the output projection, a SwiGLU MLP whose activation
+ *     is normalised before the down projection, and a 3:1 interleave of
+ *     sliding-window and full causal attention layers.
+ *   - Training with Loops: an input block runs once, a shared recurrent
+ *     block runs k times, an output block runs once.  With x the input
+ *     block's output, s_0 = x and s_i = N(F(N(s_{i-1} + x))); the output
+ *     block receives s_k.  No adapter weights, no outer residual.
+ *   - Long-Context Extension: rotary positions, base 1e4 on sliding-window
+ *     layers and 1e7 on full layers.
+ *   - Last-Loop KV Caching: a per-loop cache keeps one K/V slice per loop for
+ *     each recurrent layer (a loop-i query sees loop-i keys of earlier
+ *     tokens); a last-loop cache keeps one slice whose entries are those of
+ *     the final loop.  Tokens of the current call are always seen with their
+ *     current-loop keys and values.  Input and output layers keep one slice.
+ *
+ * Readings fixed where the paper is silent: layer i uses full attention iff
+ * i % full_every == full_offset; the window W counts the query itself (key j
+ * visible from query t iff j <= t and t - j < W); RoPE is rotate-half over the
+ * whole head, applied before the q/k normalisation, then q and k are scaled
+ * by s_qk; softmax scale sqrt(head_dim) unless set; the gate is elementwise
+ * over the n_q * head_dim attention output; m = (W_up h) * SiLU(W_sl h);
+ * logits = s_z * (E_out h); greedy decoding picks the lowest index among
+ * equal maxima.
+ *
+ * Conventions
+ *   - All pointers named "device" are CUDA device pointers on the current
+ *     device.  The library never allocates device memory and never owns the
+ *     weights, the KV cache or the workspace: the caller allocates them (sizes
+ *     from dory_kv_bytes / dory_workspace_bytes) and keeps them alive while
+ *     the handle uses them.
+ *   - Every compute call is asynchronous on the caller's stream (a
+ *     cudaStream_t passed as void*; NULL = legacy default stream) and makes no
+ *     host/device synchronisation, so calls may be captured in a CUDA graph.
+ *   - Argument, capacity and state errors are detected on the host before any
+ *     launch and returned as a negative dory_status; the handle is unchanged.
+ *     Device-side failures (a bounded wait that expired) set a status word
+ *     that dory_device_status reads.  No call aborts or throws.
+ *   - All sequences of one call share the same current length (they are
+ *     prefilled and decoded together).
+ */
+#ifndef DORY_H
+#define DORY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DORY_OK = 0,
+    DORY_EINVAL = -1,       /* bad argument (null pointer, bad size, bad config) */
+    DORY_ENOMEM = -2,       /* a caller buffer is smaller than required */
+    DORY_ECUDA = -3,        /* a CUDA runtime/driver call failed */
+    DORY_ECAPACITY = -4,    /* batch > max_batch, or length would exceed max_ctx */
+    DORY_EKMISMATCH = -5,   /* per-loop cache used with a k other than the bound one,
+                               or a cache mode other than the bound one */
+    DORY_EUNBOUND = -6,     /* compute call before dory_bind */
+    DORY_EDEVICE = -7,      /* device status word set (bounded wait expired) */
+    DORY_EUNSUPPORTED = -8  /* config outside what the kernels implement */
+} dory_status;
+
+typedef enum { DORY_CACHE_LAST_LOOP = 0, DORY_CACHE_PER_LOOP = 1 } dory_cache_mode;
+
+/* Model dimensions.  Supported: head_dim in {32, 64, 128}; d, ffn multiples
+ * of 128; n_q a multiple of n_kv; vocab a multiple of 16. */
+typedef struct {
+    int d, n_in, n_rec, n_out;   /* model width; layers in input/recurrent/output blocks */
+    int n_q, n_kv, head_dim;     /* query heads, kv heads, head width */
+    int ffn, vocab, window;      /* SwiGLU width, vocabulary, sliding window W */
+    int full_every, full_offset; /* layer i full-attention iff i % full_every == full_offset */
+    int rope;                    /* 1 = rotary positions on, 0 = off */
+    float rope_base_swa, rope_base_full;
+    float softmax_scale;         /* <= 0 selects sqrt(head_dim) */
+} dory_config;
+
+/* One layer.  Matrices are bf16, row-major [out, in], device. */
+typedef struct {
+    const void* w_qkvg;       /* [(2 n_q + 2 n_kv) head_dim, d]: rows W_q | W_k | W_v | W_g */
+    const void* w_o;          /* [d, n_q head_dim] */
+    const void* w_upgate;     /* [2 ffn, d]: rows W_up | W_sl (W_sl feeds the SiLU) */
+    const void* w_down;       /* [d, ffn] */
+    const float* alpha_attn;  /* [d] effective residual rate of the attention step */
+    const float* alpha_mlp;   /* [d] effective residual rate of the MLP step */
+    const float* s_qk;        /* [head_dim] query/key scale */
+} dory_layer_weights;
+
+typedef struct {
+    const void* embed_in;     /* bf16 [vocab, d], device */
+    const void* embed_out;    /* bf16 [vocab, d], device */
+    const float* s_z;         /* [vocab] logit scale, device; NULL means 1 */
+    const dory_layer_weights* layers; /* HOST array of n_in + n_rec + n_out entries (copied) */
+} dory_weights;
+
+typedef struct dory_model dory_t;
+
+#if defined(__GNUC__)
+#define DORY_API __attribute__((visibility("default")))
+#else
+#define DORY_API
+#endif
+
+/* Validates the config, copies the pointer tables.  No CUDA call is made.
+ * On success *out receives a handle to release with dory_destroy. */
+DORY_API int dory_create(const dory_config* cfg, const dory_weights* w, dory_t** out);
+
+/* Bytes of the KV region for max_batch sequences of up to max_ctx positions,
+ * k loops and the given cache mode (pure host function):
+ *   2 (K,V) * n_kv * head_dim * 2 B * max_batch *
+ *   sum over layers l of mult_l * slots_l,
+ * slots_l = max_ctx on full layers and min(max_ctx, window) on sliding-window
+ * layers (a ring: position p lives in slot p mod slots_l); mult_l = k for
+ * recurrent layers in per-loop mode, else 1.  Returns 0 on bad arguments.
+ * Layout: for l = 0..L-1, for slice = 0..mult_l-1: K then V, each
+ * [max_batch][n_kv][slots_l][head_dim] bf16. */
+DORY_API size_t dory_kv_bytes(const dory_config* cfg, int max_batch, int max_ctx, int k, int cache_mode);
+
+/* Bytes of scratch for calls of up to max_batch sequences x max_chunk tokens
+ * (pure host function).  Returns 0 on bad arguments. */
+DORY_API size_t dory_workspace_bytes(const dory_config* cfg, int max_batch, int max_chunk);
+
+/* Attaches caller memory (device, 256-byte aligned) and capacities to the
+ * handle and resets every sequence to length 0.  kv_bytes must be at least
+ * dory_kv_bytes(cfg, max_batch, max_ctx, k_max, cache_mode) and ws_bytes at
+ * least dory_workspace_bytes(cfg, max_batch, max_chunk).  In per-loop mode
+ * every later call must use cache_mode and the same k (<= k_max). */
+DORY_API int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes,
+              int max_batch, int max_ctx, int max_chunk, int k_max, int cache_mode);
+
+/* Prefill: appends T tokens to each of B sequences (all at the same current
+ * length P0) and runs the forward at loop count k.  tokens: device int32
+ * [B, T].  Prompts longer than max_chunk are processed in chunks of max_chunk
+ * tokens (chunked prefill).  logits: device fp32, [B, vocab] for the last
+ * position of each sequence, or [B, T, vocab] when all_logits != 0; may be
+ * NULL.  Requires B <= max_batch and P0 + T <= max_ctx. */
+DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k, int cache_mode,
+                 float* logits, int all_logits, void* stream);
+
+/* Decode: appends one token to each of B sequences at the current length and
+ * runs the forward at loop count k.  tokens: device int32 [B].  logits:
+ * device fp32 [B, vocab] or NULL; next: device int32 [B] greedy tokens or
+ * NULL. */
+DORY_API int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
+                     float* logits, int32_t* next, void* stream);
+
+/* Current length of the sequences (host state; no CUDA call). */
+DORY_API int dory_length(const dory_t* m, int* out);
+
+/* Resets every sequence to length 0 (host state only; cache contents are
+ * simply overwritten by later calls). */
+DORY_API int dory_reset(dory_t* m);
+
+/* Releases the handle (not the caller's memory). */
+DORY_API int dory_destroy(dory_t* m);
+
+/* Static description of a status code. */
+DORY_API const char* dory_strerror(int status);
+
+/* Synchronises `stream` and reads the device status word of the bound
+ * workspace: *out = 0 if every bounded device wait completed, else a code
+ * naming the kernel and wait that expired.  The word is cleared. */
+DORY_API int dory_device_status(dory_t* m, int* out, void* stream);
+
+/* Number of kernels the last dory_prefill / dory_decode_step launched. */
+DORY_API int dory_last_launch_count(const dory_t* m, int* out);
+
+/* ---- inspection entry points used by the tests (same conventions) ----- */
+
+/* Copies the final hidden states of the last call (the LM-head input, fp32)
+ * for all processed rows of the last chunk: [B * C, d], row = b * C + t,
+ * C = tokens per sequence in that chunk.  dst: device fp32. */
+DORY_API int dory_debug_hidden(dory_t* m, float* dst, int max_rows, void* stream);
+
+/* Byte offset of the K (which = 0) or V (which = 1) block of (layer, slice)
+ * inside the KV region, and its ring size in slots. */
+DORY_API int dory_debug_kv_offset(const dory_t* m, int layer, int slice, int which,
+                         size_t* offset, int* slots);
+
+/* C[M, N] (fp32, row stride ldc) = A[M, K] . B[N, K]^T with A and B bf16
+ * row-major (device), through the tensor-core GEMM of the forward pass. */
+DORY_API int dory_debug_gemm(const void* A, const void* B, float* C, int M, int N, int K, int ldc,
+                    void* stream);
+
+/* The attention step alone, as the forward pass runs it (test inspection):
+ * q [B*C, n_q, head_dim], k_cur / v_cur [B*C, n_kv, head_dim], gate
+ * [B*C, n_q*head_dim] (already sigmoid), k_cache / v_cache
+ * [B, n_kv, S, head_dim] holding positions < P0 in ring slot p mod S;
+ * out [B*C, n_q*head_dim] = softmax-weighted values times gate.  window <= 0
+ * means full causal; scale <= 0 means sqrt(head_dim).  All bf16, device. */
+DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur,
+                                  const void* k_cache, const void* v_cache, const void* gate,
+                                  void* out, int B, int C, int P0, int S, int n_q, int n_kv,
+                                  int head_dim, int window, float scale, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DORY_H */

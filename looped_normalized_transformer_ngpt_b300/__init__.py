@@ -1,0 +1,296 @@
+"""Python binding of libdory, the CUDA library behind include/dory.h.
+
+Argument marshalling only: every step of the forward pass runs in the
+library's kernels.  PyTorch is used for device memory and streams.  If the
+library is not built, or no CUDA device is present, the compute calls raise;
+there is no fallback path.
+
+Low-level: the C functions under the same names (dory_create, dory_bind,
+dory_prefill, dory_decode_step, dory_kv_bytes, ...), taking ctypes
+structures and raw device pointers.  High-level: `Model`, which uploads a
+weight dictionary, allocates the KV cache and workspace with torch and binds
+them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB
+
+DORY_OK = 0
+DORY_EINVAL = -1
+DORY_ENOMEM = -2
+DORY_ECUDA = -3
+DORY_ECAPACITY = -4
+DORY_EKMISMATCH = -5
+DORY_EUNBOUND = -6
+DORY_EDEVICE = -7
+DORY_EUNSUPPORTED = -8
+
+LAST_LOOP = 0
+PER_LOOP = 1
+
+
+class DoryConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("d", "n_in", "n_rec", "n_out", "n_q", "n_kv", "head_dim", "ffn", "vocab",
+                 "window", "full_every", "full_offset", "rope")] + [
+        ("rope_base_swa", ctypes.c_float), ("rope_base_full", ctypes.c_float),
+        ("softmax_scale", ctypes.c_float)]
+
+
+class DoryLayerWeights(ctypes.Structure):
+    _fields_ = [("w_qkvg", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("w_upgate", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("alpha_attn", ctypes.c_void_p), ("alpha_mlp", ctypes.c_void_p),
+                ("s_qk", ctypes.c_void_p)]
+
+
+class DoryWeights(ctypes.Structure):
+    _fields_ = [("embed_in", ctypes.c_void_p), ("embed_out", ctypes.c_void_p),
+                ("s_z", ctypes.c_void_p), ("layers", ctypes.POINTER(DoryLayerWeights))]
+
+
+class DoryError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "dory_create": (_I, [ctypes.POINTER(DoryConfig), ctypes.POINTER(DoryWeights), ctypes.POINTER(_P)]),
+    "dory_kv_bytes": (ctypes.c_size_t, [ctypes.POINTER(DoryConfig), _I, _I, _I, _I]),
+    "dory_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DoryConfig), _I, _I]),
+    "dory_bind": (_I, [_P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _I, _I, _I, _I, _I]),
+    "dory_prefill": (_I, [_P, _P, _I, _I, _I, _I, _P, _I, _P]),
+    "dory_decode_step": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "dory_length": (_I, [_P, ctypes.POINTER(_I)]),
+    "dory_reset": (_I, [_P]),
+    "dory_destroy": (_I, [_P]),
+    "dory_strerror": (ctypes.c_char_p, [_I]),
+    "dory_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
+    "dory_last_launch_count": (_I, [_P, ctypes.POINTER(_I)]),
+    "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
+    "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
+    "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                  ctypes.c_float, _P]),
+}
+
+
+def lib():
+    """The loaded libdory.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is not built; run __graft_entry__.build()")
+        h = ctypes.CDLL(LIB)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = h
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().dory_strerror(code).decode()
+
+
+def _check(fn, rc):
+    if rc != DORY_OK:
+        raise DoryError(fn, rc)
+
+
+def config_from_shape(shape) -> DoryConfig:
+    """DoryConfig from an object with the fields of synth.Shape."""
+    return DoryConfig(d=shape.d, n_in=shape.n_in, n_rec=shape.n_rec, n_out=shape.n_out,
+                      n_q=shape.n_q, n_kv=shape.n_kv, head_dim=shape.head_dim, ffn=shape.ffn,
+                      vocab=shape.vocab, window=shape.window, full_every=shape.full_every,
+                      full_offset=shape.full_offset, rope=1 if shape.rope else 0,
+                      rope_base_swa=shape.rope_base_swa, rope_base_full=shape.rope_base_full,
+                      softmax_scale=0.0)
+
+
+def kv_bytes(cfg: DoryConfig, max_batch: int, max_ctx: int, k: int, cache_mode: int) -> int:
+    return int(lib().dory_kv_bytes(ctypes.byref(cfg), max_batch, max_ctx, k, cache_mode))
+
+
+def workspace_bytes(cfg: DoryConfig, max_batch: int, max_chunk: int) -> int:
+    return int(lib().dory_workspace_bytes(ctypes.byref(cfg), max_batch, max_chunk))
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+class Model:
+    """Device-resident looped nGPT: weights, KV cache and workspace held as
+    torch tensors, compute through libdory.
+
+    weights: dict like synth.make_weights() returns (numpy or torch, values
+    bf16-exact); matrices are uploaded as bf16, vectors as fp32."""
+
+    def __init__(self, shape, weights, max_batch, max_ctx, max_chunk, k_max=1,
+                 cache_mode=LAST_LOOP, device="cuda"):
+        import torch
+        if not torch.cuda.is_available():
+            raise RuntimeError("libdory needs a CUDA device")
+        self.shape = shape
+        self.cfg = config_from_shape(shape)
+        self.device = torch.device(device)
+        L = lib()
+
+        def bf(x):
+            return torch.as_tensor(x).to(self.device, torch.bfloat16).contiguous()
+
+        def f32(x):
+            return torch.as_tensor(x).to(self.device, torch.float32).contiguous()
+
+        self._keep = []
+        self.embed_in = bf(weights["embed_in"])
+        self.embed_out = bf(weights["embed_out"])
+        self.s_z = f32(weights["s_z"]) if weights.get("s_z") is not None else None
+        n = shape.n_layers
+        self._layers = (DoryLayerWeights * n)()
+        for l, lw in enumerate(weights["layers"]):
+            qkvg = torch.cat([bf(lw["w_q"]), bf(lw["w_k"]), bf(lw["w_v"]), bf(lw["w_g"])], 0)
+            upg = torch.cat([bf(lw["w_up"]), bf(lw["w_sl"])], 0)
+            t = dict(qkvg=qkvg, o=bf(lw["w_o"]), upg=upg.contiguous(), down=bf(lw["w_down"]),
+                     aa=f32(lw["alpha_attn"]), am=f32(lw["alpha_mlp"]), sqk=f32(lw["s_qk"]))
+            self._keep.append(t)
+            self._layers[l] = DoryLayerWeights(t["qkvg"].data_ptr(), t["o"].data_ptr(),
+                                               t["upg"].data_ptr(), t["down"].data_ptr(),
+                                               t["aa"].data_ptr(), t["am"].data_ptr(),
+                                               t["sqk"].data_ptr())
+        w = DoryWeights(self.embed_in.data_ptr(), self.embed_out.data_ptr(),
+                        self.s_z.data_ptr() if self.s_z is not None else 0, self._layers)
+        h = ctypes.c_void_p()
+        _check("dory_create", L.dory_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(h)))
+        self.handle = h
+        self.bind(max_batch, max_ctx, max_chunk, k_max, cache_mode)
+
+    def bind(self, max_batch, max_ctx, max_chunk, k_max=1, cache_mode=LAST_LOOP):
+        import torch
+        kvb = kv_bytes(self.cfg, max_batch, max_ctx, k_max, cache_mode)
+        wsb = workspace_bytes(self.cfg, max_batch, max_chunk)
+        if kvb == 0 or wsb == 0:
+            raise DoryError("dory_kv_bytes/dory_workspace_bytes", DORY_EINVAL)
+        self.kv = torch.zeros(kvb, dtype=torch.uint8, device=self.device)
+        self.ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        _check("dory_bind", lib().dory_bind(self.handle, _ptr(self.kv), kvb, _ptr(self.ws), wsb,
+                                            max_batch, max_ctx, max_chunk, k_max, cache_mode))
+        self.max_batch, self.max_ctx, self.max_chunk = max_batch, max_ctx, max_chunk
+        self.k_max, self.cache_mode = k_max, cache_mode
+
+    # ------------------------------------------------------------- calls
+    def prefill(self, tokens, k, cache_mode=None, all_logits=False, logits=None, stream=None):
+        """tokens: int32 device tensor [B, T].  Returns fp32 logits
+        [B, V] (last position) or [B, T, V]."""
+        import torch
+        B, T = tokens.shape
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        if logits is None:
+            shp = (B, T, self.shape.vocab) if all_logits else (B, self.shape.vocab)
+            logits = torch.empty(shp, dtype=torch.float32, device=self.device)
+        _check("dory_prefill", lib().dory_prefill(self.handle, _ptr(tokens), B, T, k, mode,
+                                                  _ptr(logits), 1 if all_logits else 0,
+                                                  _stream_ptr(stream)))
+        return logits
+
+    def decode(self, tokens, k, cache_mode=None, logits=None, next_tokens=None, stream=None):
+        """tokens: int32 device tensor [B].  Returns (logits [B, V], next [B])."""
+        import torch
+        B = tokens.shape[0]
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        if logits is None:
+            logits = torch.empty((B, self.shape.vocab), dtype=torch.float32, device=self.device)
+        if next_tokens is None:
+            next_tokens = torch.empty((B,), dtype=torch.int32, device=self.device)
+        _check("dory_decode_step", lib().dory_decode_step(self.handle, _ptr(tokens), B, k, mode,
+                                                          _ptr(logits), _ptr(next_tokens),
+                                                          _stream_ptr(stream)))
+        return logits, next_tokens
+
+    def hidden(self, rows, stream=None):
+        """Final hidden states (LM-head input) of the last chunk, [rows, d] fp32."""
+        import torch
+        out = torch.empty((rows, self.shape.d), dtype=torch.float32, device=self.device)
+        _check("dory_debug_hidden", lib().dory_debug_hidden(self.handle, _ptr(out), rows,
+                                                            _stream_ptr(stream)))
+        return out
+
+    def kv_block(self, layer, slc, which):
+        """View of the K (which=0) or V (which=1) block of (layer, slice):
+        bf16 [max_batch, n_kv, slots, head_dim]."""
+        import torch
+        off = ctypes.c_size_t()
+        slots = ctypes.c_int()
+        _check("dory_debug_kv_offset", lib().dory_debug_kv_offset(
+            self.handle, layer, slc, which, ctypes.byref(off), ctypes.byref(slots)))
+        sh = self.shape
+        n = self.max_batch * sh.n_kv * slots.value * sh.head_dim
+        raw = self.kv[off.value: off.value + 2 * n]
+        return raw.view(torch.bfloat16).view(self.max_batch, sh.n_kv, slots.value, sh.head_dim)
+
+    def length(self):
+        v = ctypes.c_int()
+        _check("dory_length", lib().dory_length(self.handle, ctypes.byref(v)))
+        return v.value
+
+    def reset(self):
+        _check("dory_reset", lib().dory_reset(self.handle))
+
+    def device_status(self, stream=None):
+        v = ctypes.c_int()
+        _check("dory_device_status", lib().dory_device_status(self.handle, ctypes.byref(v),
+                                                              _stream_ptr(stream)))
+        return v.value
+
+    def launch_count(self):
+        v = ctypes.c_int()
+        _check("dory_last_launch_count", lib().dory_last_launch_count(self.handle, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().dory_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def debug_gemm(A, B, C=None, stream=None):
+    """C = A @ B^T through the library's tensor-core GEMM (A [M,K], B [N,K]
+    bf16 device tensors; C fp32 [M, N])."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check("dory_debug_gemm", lib().dory_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K,
+                                                    C.stride(0), _stream_ptr(stream)))
+    return C
+
+
+def debug_attention(q, k_cur, v_cur, k_cache, v_cache, gate, out, B, C, P0, S, n_q, n_kv,
+                    head_dim, window, scale=0.0, stream=None):
+    """The library's attention kernel alone (all tensors bf16 on the device)."""
+    _check("dory_debug_attention", lib().dory_debug_attention(
+        _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(k_cache), _ptr(v_cache), _ptr(gate), _ptr(out),
+        B, C, P0, S, n_q, n_kv, head_dim, window, scale, _stream_ptr(stream)))
+    return out

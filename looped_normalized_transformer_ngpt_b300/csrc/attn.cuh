@@ -1,0 +1,291 @@
+// attn.cuh - masked grouped-query attention over cached and current keys.
+//
+// "Dory1.0-4B: A Looped Normalized-GPT", Architecture: grouped-query
+// attention (G = n_q / n_kv query heads share one kv head), 3:1 interleave
+// of sliding-window and full causal layers, input-dependent sigmoid gate on
+// the attention output.  Last-Loop KV Caching: keys of earlier positions come
+// from the cache slice (final-loop entries, or loop-i entries in per-loop
+// mode), keys of the positions processed by this call come from this loop's
+// own projections.
+//
+//   o_h(t) = sum_j softmax_j(scale * q_h(t) . k_{h/G}(j)) v_{h/G}(j),
+//   j visible from t iff j <= t and (full layer or t - j < W);
+//   out_h(t) = o_h(t) * sigmoid(g_h(t))            (bf16)
+//
+// q and k arrive already RoPE-rotated, L2-normalised and s_qk-scaled.  The
+// normalisation of the concatenated gated output before the output
+// projection is not applied here: the projection is linear and the nGPT step
+// normalises its result, so a positive per-row scale of the projection input
+// cancels exactly.
+//
+// One CTA = (sequence b, kv head, block of 64/G query positions); its 64
+// rows are (position, head-in-group) pairs so every K/V tile staged in shared
+// memory serves all G heads.  4 warps x 16 rows, mma.sync m16n8k16 bf16 with
+// fp32 accumulation, online softmax in fp32 (exp2), K/V tiles of 64 keys
+// double-buffered with cp.async, XOR-swizzled 16-byte chunks for ldmatrix.
+#pragma once
+#include "ptx.cuh"
+
+namespace dory {
+
+struct AttnArgs {
+  const __nv_bfloat16* q;        // [B*C, n_q, dh]
+  const __nv_bfloat16* k_cur;    // [B*C, n_kv, dh]
+  const __nv_bfloat16* v_cur;
+  const __nv_bfloat16* k_cache;  // [max_batch, n_kv, S, dh] (this layer/slice)
+  const __nv_bfloat16* v_cache;
+  const __nv_bfloat16* gate;     // [B*C, n_q*dh], sigmoid(g)
+  __nv_bfloat16* out;            // [B*C, n_q*dh]
+  int C, P0, S;                  // tokens per sequence in the call, first position, ring slots
+  int n_q, n_kv;
+  int window;                    // 0 = full causal
+  float scale_log2;              // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int DH>
+struct AttnCfg {
+  static constexpr int BR = 64, BKEY = 64;
+  static constexpr int CH = DH / 8;                 // 16-byte chunks per row
+  static constexpr int SWZ = CH < 8 ? CH - 1 : 7;   // XOR mask on the chunk index
+  static constexpr size_t SMEM = (size_t)(BR * DH + 4 * BKEY * DH) * 2;
+};
+
+template <int DH>
+__device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
+  using Cf = AttnCfg<DH>;
+  return (uint32_t)(row * DH + ((chunk ^ (row & Cf::SWZ)) << 3)) * 2u;   // bytes
+}
+
+template <int DH>
+__global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
+  using Cf = AttnCfg<DH>;
+  constexpr int BR = Cf::BR, BKEY = Cf::BKEY, CH = Cf::CH;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* sK = sQ + BR * DH;             // [2][BKEY*DH]
+  __nv_bfloat16* sV = sK + 2 * BKEY * DH;       // [2][BKEY*DH]
+  const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.n_q / a.n_kv, BQ = BR / G;
+  const int qb = gridDim.x - 1 - blockIdx.x;    // longest rows first
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int q0 = qb * BQ;
+  const int nqv = min(BQ, a.C - q0);
+  const int p_lo = a.P0 + q0, p_hi = a.P0 + q0 + nqv - 1;
+  const int k_lo = a.window > 0 ? max(0, p_lo - a.window + 1) : 0;
+  const int k_hi = p_hi;
+  const int nblk = (k_hi - k_lo) / BKEY + 1;
+
+  // ---- Q tile: row r = (position i = r / G, head hg = r % G)
+  for (int idx = tid; idx < BR * CH; idx += 128) {
+    const int r = idx / CH, c = idx % CH;
+    const int i = r / G, hg = r % G;
+    const bool ok = i < nqv;
+    const __nv_bfloat16* src =
+        ok ? a.q + (((long long)b * a.C + q0 + i) * a.n_q + kvh * G + hg) * DH + c * 8 : a.q;
+    cp_async16(sQa + swz_off<DH>(r, c), src, ok);
+  }
+  auto load_kv = [&](int blk, int buf) {
+    const int kb0 = k_lo + blk * BKEY;
+    for (int idx = tid; idx < BKEY * CH; idx += 128) {
+      const int r = idx / CH, c = idx % CH;
+      const int j = kb0 + r;
+      const bool ok = j <= k_hi;
+      const __nv_bfloat16 *ks = a.k_cur, *vs = a.v_cur;
+      if (ok) {
+        long long off;
+        if (j < a.P0) {
+          off = (((long long)b * a.n_kv + kvh) * a.S + (j % a.S)) * DH + c * 8;
+          ks = a.k_cache + off;
+          vs = a.v_cache + off;
+        } else {
+          off = (((long long)b * a.C + (j - a.P0)) * a.n_kv + kvh) * DH + c * 8;
+          ks = a.k_cur + off;
+          vs = a.v_cur + off;
+        }
+      }
+      const uint32_t o = swz_off<DH>(r, c) + (uint32_t)(buf * BKEY * DH * 2);
+      cp_async16(sKa + o, ks, ok);
+      cp_async16(sVa + o, vs, ok);
+    }
+  };
+  load_kv(0, 0);
+  cp_async_commit();
+
+  const int g = lane >> 2, t4 = lane & 3;
+  uint32_t qf[DH / 16][4];
+  float o[DH / 8][4];
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  // query position of this thread's two rows (row = 16 warp + g + 8 half)
+  int qpos[2];
+  bool qok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = warp * 16 + g + 8 * h;
+    const int i = r / G;
+    qok[h] = i < nqv;
+    qpos[h] = a.P0 + q0 + i;
+  }
+
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int buf = blk & 1;
+    if (blk + 1 < nblk) {
+      load_kv(blk + 1, buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (blk == 0) {
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        const int r = warp * 16 + (lane & 15);
+        const int c = 2 * kk + (lane >> 4);
+        ldsm_x4(sQa + swz_off<DH>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+      }
+    }
+    const uint32_t kbase = sKa + (uint32_t)(buf * BKEY * DH * 2);
+    const uint32_t vbase = sVa + (uint32_t)(buf * BKEY * DH * 2);
+
+    // ---- S = Q K^T  (16 x 64 per warp)
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        const int key = 16 * np + (lane & 7) + ((lane >> 4) & 1) * 8;
+        const int c = 2 * kk + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz_off<DH>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(s[2 * np], qf[kk], b0, b1);
+        mma_bf16_16816(s[2 * np + 1], qf[kk], b2, b3);
+      }
+    }
+    // ---- mask, online softmax
+    const int kb0 = k_lo + blk * BKEY;
+    float corr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = kb0 + 8 * nt + 2 * t4 + e;
+          const int rel = qpos[h] - j;
+          const bool vis = qok[h] && j <= k_hi && rel >= 0 && (a.window <= 0 || rel < a.window);
+          float v = s[nt][2 * h + e] * a.scale_log2;
+          v = vis ? v : -INFINITY;
+          s[nt][2 * h + e] = v;
+          mx = fmaxf(mx, v);
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run[h], mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      corr[h] = exp2f(m_run[h] - m_use);
+      m_run[h] = m_new;
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float p = exp2f(s[nt][2 * h + e] - m_use);
+          s[nt][2 * h + e] = p;
+          ls += p;
+        }
+      }
+      l_run[h] = l_run[h] * corr[h] + ls;
+    }
+#pragma unroll
+    for (int i = 0; i < DH / 8; ++i) {
+      o[i][0] *= corr[0];
+      o[i][1] *= corr[0];
+      o[i][2] *= corr[1];
+      o[i][3] *= corr[1];
+    }
+    // ---- O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < DH / 16; ++dp) {
+        const int key = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = 2 * dp + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + swz_off<DH>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- normalise, gate, store
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = l_run[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (!qok[h]) continue;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    const int r = warp * 16 + g + 8 * h;
+    const int i = r / G, hg = r % G;
+    const long long row = (long long)b * a.C + q0 + i;
+    const long long base = row * a.n_q * DH + (long long)(kvh * G + hg) * DH;
+#pragma unroll
+    for (int nt = 0; nt < DH / 8; ++nt) {
+      const int dim = 8 * nt + 2 * t4;
+      const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162*>(a.gate + base + dim);
+      const float2 gf = __bfloat1622float2(gt);
+      const uint32_t pk = pack_bf16x2(o[nt][2 * h] * inv * gf.x, o[nt][2 * h + 1] * inv * gf.y);
+      *reinterpret_cast<uint32_t*>(a.out + base + dim) = pk;
+    }
+  }
+}
+
+}  // namespace dory

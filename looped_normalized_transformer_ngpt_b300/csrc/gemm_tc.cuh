@@ -1,0 +1,352 @@
+// gemm_tc.cuh - tcgen05 / TMEM BF16 GEMM for the dense projections of the
+// looped nGPT layer (QKV+gate, output, up+gate, down, LM head), with the
+// per-projection epilogues fused.
+//
+//   C[m, n] = sum_k A[m, k] * B[n, k]      A: activations [M, K] bf16
+//                                          B: weights     [N, K] bf16
+//
+// Persistent, warp-specialised, one CTA per SM (192 threads):
+//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage,
+//               128-byte swizzle, STAGES-deep ring of shared-memory buffers;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16 into
+//               one of two TMEM accumulators (2 x BN fp32 columns);
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32 (w % 4) .. +31, i.e. tile rows), fused math, stores.
+// The epilogue of tile i overlaps the MMAs of tile i + 1.
+//
+// Epilogues (projection names from "Dory1.0-4B: A Looped Normalized-GPT",
+// Architecture):
+//   EPI_F32     fp32 store, optional per-column scale (LM head: s_z).
+//   EPI_QKVG    columns are [q heads | k heads | v heads | gate]; q and k heads
+//               get RoPE (rotate-half, table lookup), L2 normalisation over the
+//               head and the s_qk scale; the gate gets a sigmoid; all stored
+//               as bf16 in head-major rows.
+//   EPI_SWIGLU  B tile = 64/128 rows of W_up and the same rows of W_sl; the
+//               epilogue forms m = u * SiLU(v) and stores m as bf16.
+#pragma once
+#include "ptx.cuh"
+
+namespace dory {
+
+enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2 };
+
+struct GemmArgs {
+  int M, N, K;          // N: output columns of the GEMM (for SWIGLU: 2 * ffn)
+  int tiles_m, tiles_n;
+  int b_second;         // SWIGLU: row offset of W_sl inside B (= ffn)
+  int* status;
+  // EPI_F32
+  float* out;
+  long long ldo;
+  const float* col_scale;   // may be null
+  // EPI_QKVG
+  __nv_bfloat16 *q, *k, *v, *g;
+  int n_q, n_kv, head_dim;
+  const float* s_qk;
+  const float2* rope;       // [rows_per_seq][head_dim / 2] (cos, sin), or null
+  int rows_per_seq;
+  // EPI_SWIGLU
+  __nv_bfloat16* m_out;
+  int ldm;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
+  uint4 a, b;
+  a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
+  a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
+  b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
+  b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
+  reinterpret_cast<uint4*>(dst)[0] = a;
+  reinterpret_cast<uint4*>(dst)[1] = b;
+}
+
+// ------------------------------------------------------------- epilogues
+template <int BN>
+__device__ __forceinline__ void epi_f32(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+  const bool row_ok = row < a.M;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 16) {
+    if (n0 + c >= a.N) break;                       // uniform across the warp
+    float v[16];
+    tmem_ld16(tacc + c, v);
+    if (!row_ok) continue;
+    float* dst = a.out + (long long)row * a.ldo + n0 + c;
+    const int nvalid = min(16, a.N - n0 - c);
+    if (a.col_scale) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i < nvalid) v[i] *= a.col_scale[n0 + c + i];
+    }
+    if (nvalid == 16 && (a.ldo & 3) == 0) {
+#pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+      for (int i = 0; i < nvalid; ++i) dst[i] = v[i];
+    }
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int row, int tn) {
+  constexpr int H = BN / 2;
+  const int col0 = tn * H;                          // column of m
+#pragma unroll 1
+  for (int c = 0; c < H; c += 16) {
+    float u[16], s[16];
+    tmem_ld16(tacc + c, u);
+    tmem_ld16(tacc + H + c, s);
+    if (row < a.M) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) u[i] = u[i] * (s[i] * sigmoidf_(s[i]));
+      store_bf16x16(a.m_out + (long long)row * a.ldm + col0 + c, u);
+    }
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+  const int dh = a.head_dim, half = dh >> 1;
+  const int nq = a.n_q, nkv = a.n_kv;
+  const bool row_ok = row < a.M;
+  const int t = row_ok ? row % a.rows_per_seq : 0;
+#pragma unroll 1
+  for (int hc = 0; hc < BN; hc += dh) {
+    const int gcol = n0 + hc;
+    if (gcol >= a.N) break;
+    const int head = gcol / dh;
+    if (head < nq + nkv) {
+      // q or k head: RoPE, per-head L2 norm, s_qk
+      const bool is_q = head < nq;
+      __nv_bfloat16* dst = is_q ? a.q + ((long long)row * nq + head) * dh
+                                : a.k + ((long long)row * nkv + (head - nq)) * dh;
+      float ss = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < dh; c += 16) {
+        float v[16];
+        tmem_ld16(tacc + hc + c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss += v[i] * v[i];
+      }
+      const float inv = 1.0f / sqrtf(fmaxf(ss, 1e-12f));
+#pragma unroll 1
+      for (int c = 0; c < half; c += 16) {
+        float x1[16], x2[16];
+        tmem_ld16(tacc + hc + c, x1);
+        tmem_ld16(tacc + hc + half + c, x2);
+        if (!row_ok) continue;
+        if (a.rope) {
+          const float2* cs = a.rope + (long long)t * half + c;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 r = cs[i];
+            const float y1 = x1[i] * r.x - x2[i] * r.y;
+            const float y2 = x2[i] * r.x + x1[i] * r.y;
+            x1[i] = y1;
+            x2[i] = y2;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x1[i] *= inv * a.s_qk[c + i];
+          x2[i] *= inv * a.s_qk[half + c + i];
+        }
+        store_bf16x16(dst + c, x1);
+        store_bf16x16(dst + half + c, x2);
+      }
+    } else if (head < nq + 2 * nkv) {
+      __nv_bfloat16* dst = a.v + ((long long)row * nkv + (head - nq - nkv)) * dh;
+#pragma unroll 1
+      for (int c = 0; c < dh; c += 16) {
+        float v[16];
+        tmem_ld16(tacc + hc + c, v);
+        if (row_ok) store_bf16x16(dst + c, v);
+      }
+    } else {
+      __nv_bfloat16* dst = a.g + ((long long)row * nq + (head - nq - 2 * nkv)) * dh;
+#pragma unroll 1
+      for (int c = 0; c < dh; c += 16) {
+        float v[16];
+        tmem_ld16(tacc + hc + c, v);
+        if (!row_ok) continue;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = sigmoidf_(v[i]);
+        store_bf16x16(dst + c, v);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------- the kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+  using C = GemmCfg<BN>;
+  constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;   // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;       // [2]
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = args.tiles_m * args.tiles_n;
+  const int KB = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int tm = tile % args.tiles_m, tn = tile / args.tiles_m;
+        const int m0 = tm * BM;
+        int nb0, nb1;
+        if (EPI == EPI_SWIGLU) {
+          nb0 = tn * (BN / 2);
+          nb1 = args.b_second + tn * (BN / 2);
+        } else {
+          nb0 = tn * BN;
+          nb1 = tn * BN + BN / 2;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, args.status, DEV_GEMM_PRODUCER)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* a_dst = smem + stage * C::STAGE_BYTES;
+          uint8_t* b_dst = a_dst + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, &full_bar[stage], kb * BK, m0);
+          tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
+          tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, args.status, DEV_GEMM_MMA_TMEM)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, args.status, DEV_GEMM_MMA_FULL)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t adesc = tc_sdesc_sw128(a_addr);
+          const uint64_t bdesc = tc_sdesc_sw128(a_addr + C::A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // +32 bytes per 16-element K step inside the swizzled 128-byte row
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+      }
+      // no MMA may be in flight when TMEM is released
+      tc_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, args.status, DEV_GEMM_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int quarter = warp & 3;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int tm = tile % args.tiles_m, tn = tile / args.tiles_m;
+      const int row = tm * BM + quarter * 32 + lane;
+      const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
+      if (EPI == EPI_F32) epi_f32<BN>(args, tacc, row, tn * BN);
+      if (EPI == EPI_QKVG) epi_qkvg<BN>(args, tacc, row, tn * BN);
+      if (EPI == EPI_SWIGLU) epi_swiglu<BN>(args, tacc, row, tn);
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  if (*abort_flag) {
+    // error path: give in-flight bulk copies time to land before the CTA's
+    // shared memory is released
+    for (int i = 0; i < 64; ++i) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dory

@@ -1,0 +1,301 @@
+// rowops.cuh - per-token kernels of the looped nGPT forward pass (HBM-bound):
+// embedding gather + normalisation, the nGPT residual step, loop-boundary
+// transforms, the KV-cache writer, the RoPE table and the greedy argmax.
+//
+// One CTA (128 threads) per token row; each thread owns up to 4 chunks of 8
+// consecutive elements (d <= 4096), loaded and stored as 16/32-byte vectors;
+// row sums of squares are reduced with warp shuffles and one shared-memory
+// step.  Normalisation: N(v) = v / sqrt(max(sum v^2, 1e-12)).
+#pragma once
+#include "ptx.cuh"
+
+namespace dory {
+
+constexpr int kRowThreads = 128;
+constexpr int kRowMaxChunks = 4;
+
+enum : int { DEV_BAD_TOKEN = 0x21 };
+
+__device__ __forceinline__ float block_sum128(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  return red[0] + red[1] + red[2] + red[3];
+}
+
+__device__ __forceinline__ void load8(const float* p, float* v) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float* v) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float* v) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+// h = N(E_in[token]); tokens [B, ld_tok], row = b * C + t.
+__global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t* tokens, int ld_tok,
+                                                            int C, const __nv_bfloat16* E, int V,
+                                                            int d, float* h32, __nv_bfloat16* hb,
+                                                            int* status) {
+  __shared__ float red[4];
+  const long long row = blockIdx.x;
+  const int b = (int)(row / C), t = (int)(row % C);
+  int tok = tokens[(long long)b * ld_tok + t];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0 && status) atomicCAS(status, 0, DEV_BAD_TOKEN);
+    tok = 0;
+  }
+  const int nch = d / 8;
+  float v[kRowMaxChunks][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+      load8_bf16(E + (long long)tok * d + ch * 8, v[j]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[j][i] * v[j][i];
+    }
+  }
+  const float inv = 1.0f / sqrtf(fmaxf(block_sum128(ss, red), 1e-12f));
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[j][i] *= inv;
+      store8(h32 + row * d + ch * 8, v[j]);
+      store8_bf16(hb + row * d + ch * 8, v[j]);
+    }
+  }
+}
+
+// nGPT residual step ("Dory1.0-4B: A Looped Normalized-GPT", Architecture):
+// h <- N(h + alpha * (N(y) - h)), y = the sublayer's projection output.
+__global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __nv_bfloat16* hb,
+                                                                  const float* y,
+                                                                  const float* alpha, int d) {
+  __shared__ float red[4];
+  const long long row = blockIdx.x;
+  const int nch = d / 8;
+  float yv[kRowMaxChunks][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+      load8(y + row * d + ch * 8, yv[j]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += yv[j][i] * yv[j][i];
+    }
+  }
+  const float inv_y = 1.0f / sqrtf(fmaxf(block_sum128(ss, red), 1e-12f));
+  float su = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+      float hv[8], av[8];
+      load8(h32 + row * d + ch * 8, hv);
+      load8(alpha + ch * 8, av);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float u = hv[i] + av[i] * (yv[j][i] * inv_y - hv[i]);
+        yv[j][i] = u;
+        su += u * u;
+      }
+    }
+  }
+  const float inv_u = 1.0f / sqrtf(fmaxf(block_sum128(su, red), 1e-12f));
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) yv[j][i] *= inv_u;
+      store8(h32 + row * d + ch * 8, yv[j]);
+      store8_bf16(hb + row * d + ch * 8, yv[j]);
+    }
+  }
+}
+
+// Loop-boundary transforms ("Dory1.0-4B: A Looped Normalized-GPT", Training
+// with Loops): the state starts as x; before each pass of the shared block
+// the block input is N(s + x); the state after a pass is the normalised block
+// output; the output block receives the final state.
+enum BoundaryMode : int {
+  BND_SAVE_X = 0,      // x = h (input block output); h is also s_0
+  BND_ENTER_FIRST = 1, // h = N(s_0 + x) with s_0 = x held in h
+  BND_ENTER_NEXT = 2,  // s = N(h); h = N(s + x)
+  BND_EXIT = 3,        // h = N(h)  (final state s_k)
+};
+
+__global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_bfloat16* hb,
+                                                               float* x32, int d, int mode) {
+  __shared__ float red[4];
+  const long long row = blockIdx.x;
+  const int nch = d / 8;
+  if (mode == BND_SAVE_X) {
+    for (int ch = threadIdx.x; ch < nch; ch += kRowThreads) {
+      float v[8];
+      load8(h32 + row * d + ch * 8, v);
+      store8(x32 + row * d + ch * 8, v);
+    }
+    return;
+  }
+  float hv[kRowMaxChunks][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+      load8(h32 + row * d + ch * 8, hv[j]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += hv[j][i] * hv[j][i];
+    }
+  }
+  if (mode != BND_ENTER_FIRST) {
+    const float inv = 1.0f / sqrtf(fmaxf(block_sum128(ss, red), 1e-12f));
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hv[j][i] *= inv;
+  }
+  if (mode != BND_EXIT) {
+    ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j) {
+      const int ch = threadIdx.x + j * kRowThreads;
+      if (ch < nch) {
+        float xv[8];
+        load8(x32 + row * d + ch * 8, xv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          hv[j][i] += xv[i];
+          ss += hv[j][i] * hv[j][i];
+        }
+      }
+    }
+    const float inv = 1.0f / sqrtf(fmaxf(block_sum128(ss, red), 1e-12f));
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hv[j][i] *= inv;
+  }
+#pragma unroll
+  for (int j = 0; j < kRowMaxChunks; ++j) {
+    const int ch = threadIdx.x + j * kRowThreads;
+    if (ch < nch) {
+      store8(h32 + row * d + ch * 8, hv[j]);
+      store8_bf16(hb + row * d + ch * 8, hv[j]);
+    }
+  }
+}
+
+// KV-cache writer: positions P0 + t for t in [t_first, C) of every sequence
+// go to ring slot (P0 + t) mod S of this layer/slice.  grid = (C - t_first, B),
+// block covers n_kv * dh / 8 16-byte chunks (K and V).
+__global__ void kv_write_kernel(const __nv_bfloat16* k_cur, const __nv_bfloat16* v_cur,
+                                __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int C, int P0,
+                                int S, int t_first, int n_kv, int dh) {
+  const int t = t_first + blockIdx.x, b = blockIdx.y;
+  const int slot = (P0 + t) % S;
+  const int cpr = dh / 8;
+  for (int idx = threadIdx.x; idx < n_kv * cpr; idx += blockDim.x) {
+    const int h = idx / cpr, c = idx % cpr;
+    const long long src = (((long long)b * C + t) * n_kv + h) * dh + c * 8;
+    const long long dst = (((long long)b * n_kv + h) * S + slot) * dh + c * 8;
+    *reinterpret_cast<uint4*>(k_cache + dst) = *reinterpret_cast<const uint4*>(k_cur + src);
+    *reinterpret_cast<uint4*>(v_cache + dst) = *reinterpret_cast<const uint4*>(v_cur + src);
+  }
+}
+
+// RoPE table for the positions of one call: tab[t][i] = (cos, sin) of
+// (P0 + t) * base^(-2i/dh); the angle is formed and reduced mod 2 pi in fp64
+// so long contexts keep full fp32 accuracy.
+__global__ void rope_table_kernel(float2* tab, int C, int P0, int dh, double base) {
+  const int half = dh / 2;
+  const long long n = (long long)C * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / half), i = (int)(idx % half);
+    const double inv_freq = pow(base, -2.0 * i / dh);
+    double ang = (double)(P0 + t) * inv_freq;
+    const double two_pi = 6.283185307179586476925286766559;
+    ang -= floor(ang / two_pi) * two_pi;
+    double s, c;
+    sincos(ang, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+// Greedy token per row: argmax of logits[row, 0..V), lowest index on ties.
+__global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V, int32_t* next) {
+  __shared__ float bv[32];
+  __shared__ int bi[32];
+  const long long row = blockIdx.x;
+  const float* z = logits + row * V;
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = z[i];
+    if (v > best) {           // strictly greater: keeps the lowest index per thread
+      best = v;
+      idx = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ov > best || (ov == best && oi < idx)) {
+      best = ov;
+      idx = oi;
+    }
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    bv[w] = best;
+    bi[w] = idx;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    best = threadIdx.x < nw ? bv[threadIdx.x] : -INFINITY;
+    idx = threadIdx.x < nw ? bi[threadIdx.x] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      if (ov > best || (ov == best && oi < idx)) {
+        best = ov;
+        idx = oi;
+      }
+    }
+    if (threadIdx.x == 0) next[row] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
+}  // namespace dory

@@ -1,0 +1,133 @@
+"""Kernel-level GPU checks through the C ABI's inspection entry points:
+the tcgen05 GEMM against a plain fp32 matmul of the same bf16 operands, and
+the attention kernel against exact mask probes and the oracle's attention."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+    _build.build()
+    dory.lib()
+    return dory
+
+
+def _bf16(t):
+    import torch
+    return t.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1, 256, 64), (200, 384, 128), (2, 512, 1024),
+                                   (300, 1000, 200), (1024, 2560, 1024), (8192, 1024, 1024),
+                                   (513, 2816, 2816), (4, 32000, 1024)])
+def test_gemm_matches_fp32_matmul(dev, M, N, K):
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N * 3 + K)
+    A = _bf16(torch.randn(M, K, device="cuda", generator=g))
+    B = _bf16(torch.randn(N, K, device="cuda", generator=g))
+    C = dev.debug_gemm(A, B)
+    ref = A.float() @ B.float().T
+    torch.cuda.synchronize()
+    err = (C - ref).abs().max().item()
+    # fp32 accumulation of exact bf16 products: error grows like sqrt(K) ulps
+    assert err <= 2e-5 * math.sqrt(K) * ref.abs().max().item() + 1e-4, err
+
+
+def test_gemm_repeatable_and_strided_output(dev):
+    import torch
+    A = _bf16(torch.randn(777, 512, device="cuda"))
+    B = _bf16(torch.randn(640, 512, device="cuda"))
+    big = torch.full((777, 700), 7.0, device="cuda")
+    dev.debug_gemm(A, B, C=big[:, :640])
+    c2 = dev.debug_gemm(A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(big[:, :640], c2)
+    assert torch.all(big[:, 640:] == 7.0)
+
+
+def _attn_case(dev, B, C, P0, W, nq, nkv, dh, seed, uniform=False, S=None):
+    """Random (or uniform-score one-hot) attention inputs; returns GPU output
+    and the inputs as float64 numpy."""
+    import torch
+    rng = np.random.default_rng(seed)
+    L = P0 + C
+    S = S or (L if W <= 0 else min(W, max(L, 1)))
+    if uniform:
+        kvec = np.zeros(dh); kvec[0] = 1.0
+        q = np.tile(kvec, (B, C, nq, 1))
+        k_all = np.tile(kvec, (B, L, nkv, 1))
+        v_all = np.zeros((B, L, nkv, dh))
+        for j in range(L):
+            v_all[:, j, :, j % dh] = 1.0
+        gate = np.ones((B, C, nq * dh))
+    else:
+        q = oracle.l2n(rng.standard_normal((B, C, nq, dh)))
+        k_all = oracle.l2n(rng.standard_normal((B, L, nkv, dh)))
+        v_all = rng.standard_normal((B, L, nkv, dh)) * 0.3
+        gate = 1.0 / (1.0 + np.exp(-rng.standard_normal((B, C, nq * dh))))
+    bf = lambda x: torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+    qb, kb, vb, gb = bf(q), bf(k_all), bf(v_all), bf(gate)
+    # cache: positions < P0 in ring slot p mod S, layout [B, nkv, S, dh]
+    kc = torch.zeros((B, nkv, S, dh), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    for p in range(max(0, P0 - S), P0):
+        kc[:, :, p % S] = kb[:, p]
+        vc[:, :, p % S] = vb[:, p]
+    cur_k = kb[:, P0:].contiguous().view(B * C, nkv, dh).cuda()
+    cur_v = vb[:, P0:].contiguous().view(B * C, nkv, dh).cuda()
+    out = torch.zeros((B * C, nq * dh), dtype=torch.bfloat16, device="cuda")
+    dev.debug_attention(qb.view(B * C, nq, dh).cuda(), cur_k, cur_v, kc.cuda(), vc.cuda(),
+                        gb.view(B * C, nq * dh).cuda(), out, B, C, P0, S, nq, nkv, dh, W)
+    torch.cuda.synchronize()
+    f64 = lambda t: t.float().double().numpy()
+    return out.float().cpu().numpy().reshape(B, C, nq, dh), f64(qb), f64(kb), f64(vb), f64(gb)
+
+
+@pytest.mark.parametrize("dh", [32, 128])
+@pytest.mark.parametrize("W,P0,C", [(16, 0, 64), (16, 40, 37), (5, 10, 1), (0, 0, 100),
+                                    (0, 71, 1), (1, 3, 20), (512, 0, 130)])
+def test_attention_mask_is_exact(dev, dh, W, P0, C):
+    """Equal scores and one-hot values e_(j mod dh): every output is
+    count / n with n = |visible keys|, so the bf16 result equals the value
+    formed the same way in float32 exactly."""
+    nq, nkv, B = 4, 2, 2
+    out, *_ = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 0, uniform=True)
+    for t in range(C):
+        p = P0 + t
+        lo = 0 if W <= 0 else max(0, p - W + 1)
+        n = p - lo + 1
+        cnt = np.zeros(dh)
+        for j in range(lo, p + 1):
+            cnt[j % dh] += 1
+        want = (cnt.astype(np.float32) * (np.float32(1.0) / np.float32(n))).astype(np.float32)
+        want = want.astype(np.float32)
+        import torch
+        want_bf = torch.tensor(want).to(torch.bfloat16).float().numpy()
+        for b in range(B):
+            for h in range(nq):
+                assert np.array_equal(out[b, t, h], want_bf), (t, b, h)
+
+
+@pytest.mark.parametrize("dh,nq,nkv", [(32, 4, 2), (128, 8, 2), (128, 16, 4), (64, 4, 4)])
+@pytest.mark.parametrize("W,P0,C", [(16, 0, 64), (24, 50, 30), (0, 0, 130), (0, 33, 1),
+                                    (512, 600, 1), (8, 9, 17)])
+def test_attention_matches_oracle(dev, dh, nq, nkv, W, P0, C):
+    B = 2
+    out, q, k_all, v_all, gate = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 1)
+    G = nq // nkv
+    L = P0 + C
+    qpos = np.arange(P0, L)
+    for b in range(B):
+        for h in range(nq):
+            o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G], qpos,
+                                 np.arange(L), W, W <= 0, math.sqrt(dh))
+            want = o * gate[b].reshape(C, nq, dh)[:, h]
+            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
