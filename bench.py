@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Throughput of the looped normalized-GPT forward pass on B300.
+
+One step = one request pass over the small looped nGPT (d = 1024, 4 input /
+10 recurrent / 4 output layers, 8 q / 2 kv heads, head_dim 128, SwiGLU 2816,
+vocab 32000, window 512, 3:1 sliding-window : full): prefill of 4 x 2048
+uniform-random tokens at loop count k (default 4) with the last-loop KV cache,
+then 8 greedy decode steps of the same 4 sequences.  Weights are random
+unit-norm bf16 matrices (synthetic; no trained checkpoint), tokens seeded.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Under torchrun each rank runs its own replica on its own GPU with its own
+sequences (no collective on the data path); the reported value is the tokens
+of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "looped fwd tokens/s at k=1/2/4 (prefill, decode); % of BF16 TC / HBM roofline"
+BATCH, SEQ, DECODE = 4, 2048, 8
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------ distribution
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    _, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return world
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def dist_max(x: float, device=None) -> float:
+    """Maximum of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(tokens_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------ work model
+def layer_params(sh):
+    hq, hk = sh.n_q * sh.head_dim, sh.n_kv * sh.head_dim
+    return {"qkvg": sh.d * (2 * hq + 2 * hk), "o": sh.d * hq, "upgate": 2 * sh.ffn * sh.d,
+            "down": sh.d * sh.ffn}
+
+
+def visible_keys(sh, layer, P0, C):
+    """Sum over the C query positions P0..P0+C-1 of the number of visible keys."""
+    tot = 0
+    for t in range(P0, P0 + C):
+        tot += t + 1 if sh.is_full(layer) else min(t + 1, sh.window)
+    return tot
+
+
+def step_flops(sh, B, C, k, P0=0, logit_rows=None):
+    """Algorithmic FLOPs of one forward step (B sequences x C tokens at
+    positions P0..), per kernel class: GEMMs on the rows produced, attention
+    over visible (query, key) pairs only, LM head on the logit rows."""
+    lp = layer_params(sh)
+    apps = [l for l in range(sh.n_in)] + [l for _ in range(k)
+                                          for l in range(sh.n_in, sh.n_in + sh.n_rec)] + \
+        [l for l in range(sh.n_in + sh.n_rec, sh.n_layers)]
+    M = B * C
+    f = {"qkvg_gemm": 0, "o_gemm": 0, "upgate_gemm": 0, "down_gemm": 0, "attention": 0}
+    for l in apps:
+        f["qkvg_gemm"] += 2 * M * lp["qkvg"]
+        f["o_gemm"] += 2 * M * lp["o"]
+        f["upgate_gemm"] += 2 * M * lp["upgate"]
+        f["down_gemm"] += 2 * M * lp["down"]
+        f["attention"] += 4 * sh.n_q * sh.head_dim * visible_keys(sh, l, P0, C) * B
+    rows = B if logit_rows is None else logit_rows
+    f["lm_head"] = 2 * rows * sh.vocab * sh.d
+    return f
+
+
+def step_row_bytes(sh, B, C, k):
+    """Algorithmic HBM bytes of the per-token row kernels of one step."""
+    apps = sh.n_in + sh.n_out + k * sh.n_rec
+    M = B * C
+    return {"ngpt_update": 2 * apps * M * sh.d * (4 + 4 + 4 + 2),
+            "boundary": (k + 2) * M * sh.d * (4 + 4 + 4 + 2),
+            "embed": M * sh.d * (2 + 4 + 2),
+            "kv_write": sh.n_layers * M * 2 * sh.n_kv * sh.head_dim * 2 * 2}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        src = os.path.join(ROOT, e["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return float(e["bytes_per_launch"]) if h == e["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import synth
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    _build.build()
+    sh = synth.SMALL
+    K, D = args.k, args.decode
+    w = synth.make_weights(sh)
+    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=SEQ + D, max_chunk=SEQ, k_max=max(K, 4),
+                   cache_mode=dory.LAST_LOOP, device=dev)
+    del w
+    prompt_np = synth.tokens(sh, BATCH, SEQ, seed=1000 + rank)
+    first_np = synth.tokens(sh, BATCH, 1, seed=2000 + rank)[:, 0]
+    prompt = torch.tensor(prompt_np, device=dev)
+    first = torch.tensor(first_np, device=dev)
+    V = sh.vocab
+    logits = torch.empty((BATCH, V), dtype=torch.float32, device=dev)
+    dlogits = torch.empty((BATCH, V), dtype=torch.float32, device=dev)
+    nxt = torch.empty((D, BATCH), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def prefill_part(k):
+        m.reset()
+        m.prefill(prompt, k, logits=logits, stream=stream)
+
+    def decode_part(k):
+        for s in range(D):
+            m.decode(first if s == 0 else nxt[s - 1], k, logits=dlogits, next_tokens=nxt[s],
+                     stream=stream)
+
+    def launches_of(k):
+        prefill_part(k)
+        n = m.launch_count()
+        decode_part(k)
+        n += D * m.launch_count()
+        return n
+
+    def capture(fn, warm):
+        g = torch.cuda.CUDAGraph()
+        if warm:
+            with torch.cuda.stream(stream):
+                fn()                               # eager warm-up (lazy init)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def replay(g, n):
+        # CUDAGraph.replay launches on the current stream
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                g.replay()
+
+    def time_graph(g, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(g, n)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # ---- headline: K steps of (prefill + D decodes) at loop count K
+    with torch.cuda.stream(stream):
+        n_launch = launches_of(K)
+    g_step = capture(lambda: (prefill_part(K), decode_part(K)), warm=True)
+    replay(g_step, args.warmup)
+    stream.synchronize()
+    dist_barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(g_step, args.steps)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        dist_barrier()
+    ms_step = dist_max(e0.elapsed_time(e1) / args.steps, dev)
+    tok_step = BATCH * SEQ + BATCH * D
+    value = aggregate_throughput(tok_step, world, ms_step / 1e3)
+    assert m.device_status(stream) == 0, "device status word set during the timed steps"
+
+    # ---- per-k breakdown: prefill and decode timed separately
+    per_k = {}
+    for k in args.per_k:
+        gp = capture(lambda: prefill_part(k), warm=False)
+        replay(gp, 2)
+        tp = time_graph(gp, max(3, args.steps // 4))
+        # decode graph: positions SEQ .. SEQ+D-1 after an eager prefill; every
+        # replay redoes the same D steps (same work; ring contents repeat)
+        with torch.cuda.stream(stream):
+            prefill_part(k)
+        gd = capture(lambda: decode_part(k), warm=False)
+        replay(gd, 2)
+        td = time_graph(gd, max(3, args.steps // 4))
+        fl = step_flops(sh, BATCH, SEQ, k)
+        per_k[str(k)] = {"prefill_tok_s": round(BATCH * SEQ / (tp / 1e3), 1),
+                         "prefill_ms": round(tp, 3),
+                         "prefill_tflops": round(sum(fl.values()) / (tp / 1e3) / 1e12, 1),
+                         "decode_tok_s": round(BATCH * D / (td / 1e3), 1),
+                         "decode_ms_per_token_step": round(td / D, 3)}
+        del gp, gd
+
+    # ---- roofline: per-launch event timing over one eager step at K
+    m.profile_begin(1 << 16)
+    with torch.cuda.stream(stream):
+        prefill_part(K)
+    prof = m.profile_end()
+    peaks, peak_src = load_peaks()
+    fl = step_flops(sh, BATCH, SEQ, K)
+    rb = step_row_bytes(sh, BATCH, SEQ, K)
+    classes = []
+    for name, (ms, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        if name in fl:
+            ach = fl[name] / (ms / 1e3) / 1e12
+            classes.append((ms, name, cnt, "tensor", ach, "TFLOP/s", fl[name] / cnt))
+        elif name in rb:
+            ach = rb[name] / (ms / 1e3) / 1e9
+            classes.append((ms, name, cnt, "hbm", ach, "GB/s", rb[name] / cnt))
+        else:
+            classes.append((ms, name, cnt, None, None, None, None))
+    classes.sort(reverse=True)
+    top = next(c for c in classes if c[3] is not None)
+    ms, name, cnt, bound, ach, unit, per_launch = top
+    peak = peaks["bf16_tflops_sustained"] if bound == "tensor" else peaks["hbm_gbs"]
+    roofline = {"bound": bound, "kernel": name, "achieved": round(ach, 1), "peak": peak,
+                "peak_source": f"{peak_src} ({'bf16 sustained' if bound == 'tensor' else 'hbm copy'})",
+                "unit": unit, "frac": round(ach / peak, 4),
+                "traffic": traffic_for(name, "small_prefill_4x2048"),
+                "algorithmic_per_launch": per_launch, "launches": cnt,
+                "avg_launch_us": round(ms / cnt * 1e3, 2)}
+    breakdown = {c[1]: {"ms": round(c[0], 3), "launches": c[2],
+                        "achieved": None if c[4] is None else round(c[4], 1), "unit": c[5]}
+                 for c in classes}
+
+    # ---- end to end through the public API with host buffers
+    host_prompt = torch.tensor(prompt_np).pin_memory()
+    host_first = torch.tensor(first_np).pin_memory()
+    host_out = torch.empty((D, BATCH), dtype=torch.int32).pin_memory()
+    d_prompt = torch.empty_like(prompt)
+    d_first = torch.empty_like(first)
+
+    def e2e_step():
+        d_prompt.copy_(host_prompt, non_blocking=True)
+        d_first.copy_(host_first, non_blocking=True)
+        m.reset()
+        m.prefill(d_prompt, K, logits=logits, stream=stream)
+        for s in range(D):
+            m.decode(d_first if s == 0 else nxt[s - 1], K, logits=dlogits, next_tokens=nxt[s],
+                     stream=stream)
+        host_out.copy_(nxt, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        n_e2e = max(3, args.steps // 2)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        stream.synchronize()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+    t_e2e = dist_max(t_e2e, dev)
+    e2e = {"value": round(aggregate_throughput(tok_step, world, t_e2e), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(host_prompt.numel() * 4 + host_first.numel() * 4),
+           "d2h_bytes_per_step": int(host_out.numel() * 4),
+           "note": "eager C-ABI calls (no graph), pinned host tokens in, greedy tokens out"}
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded uniform tokens, random unit-norm bf16 weights)",
+           "config": {"workload": f"small looped nGPT prefill {BATCH}x{SEQ} + {D} greedy decode "
+                                  f"steps at k={K}, last-loop KV cache",
+                      "batch": BATCH, "seq_len": SEQ, "decode_steps": D, "k": K,
+                      "cache_mode": "last_loop", "parallelism": f"replicas x{world}",
+                      "graph": "whole step captured in one CUDA graph",
+                      "l2": "not flushed: each step streams 575 MB of weights and ~200 MB of "
+                            "activations, > 126 MB L2"},
+           "roofline": roofline, "gpu_launches": int(n_launch * args.steps),
+           "clocks": clk.summary(), "e2e": e2e, "per_k": per_k, "breakdown": breakdown}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(K, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ CPU oracle
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_sample(k, n_tokens, n_decode, weights=None):
+    """Times the oracle (float32) on one sequence of the workload: prefill of
+    n_tokens then n_decode decode steps.  Returns (seconds, tokens)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    sh = synth.SMALL
+    w = weights if weights is not None else synth.make_weights(sh)
+    o = oracle.Oracle(sh, w, dtype=np.float32)
+    tok = synth.tokens(sh, 1, n_tokens, seed=1000)
+    t0 = time.perf_counter()
+    r = o.prefill(tok, k, oracle.LAST_LOOP)
+    nxt = np.argmax(r["logits"][:, -1], axis=-1)
+    for _ in range(n_decode):
+        nxt = o.decode(nxt, k, oracle.LAST_LOOP)["next"]
+    return time.perf_counter() - t0, n_tokens + n_decode
+
+
+def cpu_baseline(k, budget_s=20.0):
+    import synth
+    w = synth.make_weights(synth.SMALL)
+    t_small, n_small = oracle_sample(k, 32, 1, w)          # calibration
+    per_tok = t_small / n_small
+    n = int(max(32, min(SEQ, budget_s / max(per_tok, 1e-6))))
+    t, ntok = oracle_sample(k, n, 2, w)
+    return {"value": round(ntok / t, 2), "unit": "tokens/s", "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"numpy float32 oracle, 1 sequence: prefill {n} tokens + 2 decode steps "
+                      f"at k={k} (last-loop), small looped nGPT; {t:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    w = synth.make_weights(synth.SMALL)
+    K = args.k
+    t1, n1 = oracle_sample(K, 16, 0, w)
+    n_steps = args.steps + args.warmup
+    per_step_budget = max(0.5, 150.0 / n_steps)
+    n = int(max(8, min(SEQ, per_step_budget / (t1 / n1))))
+    times = []
+    for i in range(n_steps):
+        t, ntok = oracle_sample(K, n, 0, w)
+        if i >= args.warmup:
+            times.append(t)
+    ms = 1e3 * sum(times) / len(times)
+    val = n / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
+           "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded uniform tokens, random unit-norm bf16 weights)",
+           "config": {"workload": f"small looped nGPT prefill at k={K}, last-loop KV cache "
+                                  f"(bounded sample: 1 x {n} tokens per step)",
+                      "batch": 1, "seq_len": n, "k": K, "cache_mode": "last_loop"},
+           "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "kind": "oracle",
+                            "cores": _blas_threads(),
+                            "sample": f"1 sequence x {n} tokens prefill per step"},
+           "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["dory", "reference"], default="dory")
+    ap.add_argument("--k", type=int, default=4, help="loop count of the timed step")
+    ap.add_argument("--decode", type=int, default=DECODE)
+    ap.add_argument("--per-k", type=lambda s: [int(x) for x in s.split(",") if x],
+                    default=[1, 2, 4])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)          # at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

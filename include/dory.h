@@ -175,6 +175,36 @@ DORY_API int dory_device_status(dory_t* m, int* out, void* stream);
 /* Number of kernels the last dory_prefill / dory_decode_step launched. */
 DORY_API int dory_last_launch_count(const dory_t* m, int* out);
 
+/* ---- per-kernel timing ------------------------------------------------ */
+
+/* Kernel classes for dory_profile_end (one per step of the forward pass). */
+typedef enum {
+    DORY_K_EMBED = 0,       /* token gather + normalisation */
+    DORY_K_ROPE = 1,        /* RoPE cos/sin table for the call's positions */
+    DORY_K_QKVG_GEMM = 2,   /* QKV + gate projection, RoPE / q-k norm / sigmoid fused */
+    DORY_K_ATTENTION = 3,   /* masked GQA attention over cached + current keys */
+    DORY_K_KV_WRITE = 4,    /* KV-cache writer */
+    DORY_K_O_GEMM = 5,      /* output projection */
+    DORY_K_NGPT_UPDATE = 6, /* nGPT residual step */
+    DORY_K_UPGATE_GEMM = 7, /* up + SiLU-gate projection, SwiGLU fused */
+    DORY_K_DOWN_GEMM = 8,   /* down projection */
+    DORY_K_BOUNDARY = 9,    /* loop-boundary re-injection / normalisation */
+    DORY_K_LM_HEAD = 10,    /* logits */
+    DORY_K_ARGMAX = 11,     /* greedy token */
+    DORY_K_COUNT = 12
+} dory_kernel_class;
+
+/* Starts recording a CUDA-event pair around each of the next max_launches
+ * kernel launches of this handle (events are created on first use; no device
+ * memory).  Launches beyond max_launches are not timed.  Not for use inside
+ * stream capture. */
+DORY_API int dory_profile_begin(dory_t* m, int max_launches);
+
+/* Stops recording, synchronises the recorded events and writes, per kernel
+ * class, the summed elapsed milliseconds (ms[DORY_K_COUNT]) and the number of
+ * timed launches (launches[DORY_K_COUNT]). */
+DORY_API int dory_profile_end(dory_t* m, double* ms, int* launches);
+
 /* ---- inspection entry points used by the tests (same conventions) ----- */
 
 /* Copies the final hidden states of the last call (the LM-head input, fp32)

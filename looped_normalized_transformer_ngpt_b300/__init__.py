@@ -31,6 +31,9 @@ DORY_EUNSUPPORTED = -8
 LAST_LOOP = 0
 PER_LOOP = 1
 
+KERNEL_CLASSES = ("embed", "rope", "qkvg_gemm", "attention", "kv_write", "o_gemm", "ngpt_update",
+                  "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax")
+
 
 class DoryConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
@@ -77,6 +80,8 @@ _SIGS = {
     "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
     "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
     "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "dory_profile_begin": (_I, [_P, _I]),
+    "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                   ctypes.c_float, _P]),
 }
@@ -261,6 +266,18 @@ class Model:
         v = ctypes.c_int()
         _check("dory_last_launch_count", lib().dory_last_launch_count(self.handle, ctypes.byref(v)))
         return v.value
+
+    def profile_begin(self, max_launches=65536):
+        _check("dory_profile_begin", lib().dory_profile_begin(self.handle, max_launches))
+
+    def profile_end(self):
+        """{kernel class: (total ms, launches)} for the launches since
+        profile_begin."""
+        n = len(KERNEL_CLASSES)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int * n)()
+        _check("dory_profile_end", lib().dory_profile_end(self.handle, ms, cnt))
+        return {KERNEL_CLASSES[i]: (ms[i], cnt[i]) for i in range(n)}
 
     def close(self):
         if getattr(self, "handle", None):

@@ -207,6 +207,11 @@ struct dory_model {
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
   int launches = 0;
+  // optional per-launch event timing
+  bool prof_on = false;
+  int prof_used = 0;
+  std::vector<cudaEvent_t> prof_ev;   // 2 per launch
+  std::vector<int> prof_cls;
 };
 
 namespace {
@@ -222,8 +227,21 @@ T* wsp(dory_model* m, size_t off) {
     if (_rc != DORY_OK) return _rc;   \
   } while (0)
 
-int launched(dory_model* m) {
-  ++m->launches;
+// Brackets every launch: optional start/end events (profiling) and the
+// launch counter.
+void pb(dory_model* m, int cls, cudaStream_t st) {
+  if (m->prof_on && m->prof_used < (int)m->prof_cls.size()) {
+    m->prof_cls[m->prof_used] = cls;
+    cudaEventRecord(m->prof_ev[2 * m->prof_used], st);
+  }
+}
+int pe(dory_model* m, cudaStream_t st, int rc = DORY_OK) {
+  if (m->prof_on && m->prof_used < (int)m->prof_cls.size()) {
+    cudaEventRecord(m->prof_ev[2 * m->prof_used + 1], st);
+    ++m->prof_used;
+  }
+  m->launches += 1;
+  if (rc != DORY_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
@@ -253,8 +271,8 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   ga.s_qk = w.s_qk;
   ga.rope = c.rope ? wsp<float2>(m, full ? m->L.rope_full : m->L.rope_swa) : nullptr;
   ga.rows_per_seq = C;
-  DORY_TRY(launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st));
-  ++m->launches;
+  pb(m, DORY_K_QKVG_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st)));
 
   // attention over cached + current keys
   const int S = slots_of(c, l, m->max_ctx);
@@ -278,18 +296,21 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   aa.window = full ? 0 : c.window;
   const float scale = c.softmax_scale > 0.f ? c.softmax_scale : sqrtf((float)c.head_dim);
   aa.scale_log2 = scale * 1.4426950408889634f;
-  if (c.head_dim == 32) DORY_TRY(launch_attn<32>(aa, B, st));
-  if (c.head_dim == 64) DORY_TRY(launch_attn<64>(aa, B, st));
-  if (c.head_dim == 128) DORY_TRY(launch_attn<128>(aa, B, st));
-  ++m->launches;
+  pb(m, DORY_K_ATTENTION, st);
+  int arc = DORY_EUNSUPPORTED;
+  if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
+  if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
+  if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
+  DORY_TRY(pe(m, st, arc));
 
   // KV write: the last min(C, S) positions of the call
   if (store) {
     const int t_first = C > S ? C - S : 0;
     dim3 grid(C - t_first, B);
+    pb(m, DORY_K_KV_WRITE, st);
     kv_write_kernel<<<grid, 64, 0, st>>>(ga.k, ga.v, kc, vc, C, P0, S, t_first, c.n_kv,
                                          c.head_dim);
-    DORY_TRY(launched(m));
+    DORY_TRY(pe(m, st));
   }
 
   // output projection + nGPT step
@@ -300,12 +321,13 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   go.status = status;
   go.out = wsp<float>(m, m->L.y32);
   go.ldo = c.d;
-  DORY_TRY(launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st));
-  ++m->launches;
+  pb(m, DORY_K_O_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
+  pb(m, DORY_K_NGPT_UPDATE, st);
   ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
                                                 wsp<__nv_bfloat16>(m, m->L.hb),
                                                 wsp<float>(m, m->L.y32), w.alpha_attn, c.d);
-  DORY_TRY(launched(m));
+  DORY_TRY(pe(m, st));
 
   // SwiGLU MLP + nGPT step
   GemmArgs gu{};
@@ -316,8 +338,8 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gu.status = status;
   gu.m_out = wsp<__nv_bfloat16>(m, m->L.m);
   gu.ldm = c.ffn;
-  DORY_TRY(launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st));
-  ++m->launches;
+  pb(m, DORY_K_UPGATE_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
   GemmArgs gd{};
   gd.M = M;
   gd.N = c.d;
@@ -325,19 +347,21 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gd.status = status;
   gd.out = wsp<float>(m, m->L.y32);
   gd.ldo = c.d;
-  DORY_TRY(launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st));
-  ++m->launches;
+  pb(m, DORY_K_DOWN_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
+  pb(m, DORY_K_NGPT_UPDATE, st);
   ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
                                                 wsp<__nv_bfloat16>(m, m->L.hb),
                                                 wsp<float>(m, m->L.y32), w.alpha_mlp, c.d);
-  return launched(m);
+  return pe(m, st);
 }
 
 int boundary(dory_model* m, int M, int mode, cudaStream_t st) {
+  pb(m, DORY_K_BOUNDARY, st);
   boundary_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
                                              wsp<__nv_bfloat16>(m, m->L.hb),
                                              wsp<float>(m, m->L.x32), m->cfg.d, mode);
-  return launched(m);
+  return pe(m, st);
 }
 
 // One forward step over B sequences x C tokens at positions P0 .. P0+C-1.
@@ -360,18 +384,21 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   if (c.rope) {
     const int n = C * (c.head_dim / 2);
     const int blocks = (n + 255) / 256;
+    pb(m, DORY_K_ROPE, st);
     rope_table_kernel<<<blocks, 256, 0, st>>>(wsp<float2>(m, m->L.rope_swa), C, P0, c.head_dim,
                                              (double)c.rope_base_swa);
-    DORY_TRY(launched(m));
+    DORY_TRY(pe(m, st));
+    pb(m, DORY_K_ROPE, st);
     rope_table_kernel<<<blocks, 256, 0, st>>>(wsp<float2>(m, m->L.rope_full), C, P0, c.head_dim,
                                              (double)c.rope_base_full);
-    DORY_TRY(launched(m));
+    DORY_TRY(pe(m, st));
   }
+  pb(m, DORY_K_EMBED, st);
   embed_kernel<<<M, kRowThreads, 0, st>>>(tokens, ld_tok, C,
                                           reinterpret_cast<const __nv_bfloat16*>(m->embed_in),
                                           c.vocab, c.d, wsp<float>(m, m->L.h32),
                                           wsp<__nv_bfloat16>(m, m->L.hb), status);
-  DORY_TRY(launched(m));
+  DORY_TRY(pe(m, st));
 
   for (int l = 0; l < c.n_in; ++l)
     DORY_TRY(run_layer(m, l, 0, true, B, C, P0, tm_hb, tm_att, tm_m, st));
@@ -408,8 +435,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       gl.M = B;
       gl.ldo = ld_seq * c.vocab;
       gl.out = logits + (long long)t_out0 * c.vocab;
-      DORY_TRY(launch_gemm<kGemmBN, EPI_F32>(tm_last, m->tm_embed_out, gl, st));
-      ++m->launches;
+      pb(m, DORY_K_LM_HEAD, st);
+      DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_last, m->tm_embed_out, gl, st)));
     } else {
       for (int b = 0; b < B; ++b) {
         CUtensorMap tm_rows;
@@ -418,8 +445,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
           return DORY_ECUDA;
         gl.M = n_logit_rows;
         gl.out = logits + ((long long)b * ld_seq + t_out0) * c.vocab;
-        DORY_TRY(launch_gemm<kGemmBN, EPI_F32>(tm_rows, m->tm_embed_out, gl, st));
-        ++m->launches;
+        pb(m, DORY_K_LM_HEAD, st);
+        DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_rows, m->tm_embed_out, gl, st)));
       }
     }
   }
@@ -569,8 +596,9 @@ int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_m
   const int r = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st);
   if (r != DORY_OK) return r;
   if (next) {
+    pb(m, DORY_K_ARGMAX, st);
     argmax_kernel<<<B, 1024, 0, st>>>(logits, m->cfg.vocab, next);
-    return launched(m);
+    return pe(m, st);
   }
   return DORY_OK;
 }
@@ -591,7 +619,43 @@ int dory_reset(dory_t* m) {
 
 int dory_destroy(dory_t* m) {
   if (!m) return DORY_EINVAL;
+  for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
   delete m;
+  return DORY_OK;
+}
+
+int dory_profile_begin(dory_t* m, int max_launches) {
+  if (!m || max_launches <= 0) return DORY_EINVAL;
+  if ((int)m->prof_cls.size() < max_launches) {
+    while ((int)m->prof_ev.size() < 2 * max_launches) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return DORY_ECUDA;
+      m->prof_ev.push_back(e);
+    }
+    m->prof_cls.assign(max_launches, 0);
+  }
+  m->prof_used = 0;
+  m->prof_on = true;
+  return DORY_OK;
+}
+
+int dory_profile_end(dory_t* m, double* ms, int* launches) {
+  if (!m || !ms || !launches) return DORY_EINVAL;
+  if (!m->prof_on) return DORY_EINVAL;
+  m->prof_on = false;
+  for (int c = 0; c < DORY_K_COUNT; ++c) {
+    ms[c] = 0.0;
+    launches[c] = 0;
+  }
+  for (int i = 0; i < m->prof_used; ++i) {
+    if (cudaEventSynchronize(m->prof_ev[2 * i + 1]) != cudaSuccess) return DORY_ECUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, m->prof_ev[2 * i], m->prof_ev[2 * i + 1]) != cudaSuccess)
+      return DORY_ECUDA;
+    ms[m->prof_cls[i]] += t;
+    launches[m->prof_cls[i]] += 1;
+  }
+  m->prof_used = 0;
   return DORY_OK;
 }
 

@@ -138,8 +138,13 @@ def test_kv_slots_hold_the_right_positions(dev, mode):
                     if p < 0:
                         continue
                     g = blk[:B, :, slot]                                   # [B, nkv, dh]
-                    dist = np.linalg.norm(ref[:B] - g[:, :, None, :], axis=-1).sum(axis=1)
-                    assert np.all(np.argmin(dist, axis=-1) == p), (l, sl, which, slot)
+                    if which == 0:
+                        # rotated keys are unique per position: the slot's
+                        # position is decided exactly by the nearest match.
+                        # (Values are not: in layer 0 they depend on the
+                        # token alone, so repeated tokens repeat them.)
+                        dist = np.linalg.norm(ref[:B] - g[:, :, None, :], axis=-1).sum(axis=1)
+                        assert np.all(np.argmin(dist, axis=-1) == p), (l, sl, slot)
                     np.testing.assert_allclose(g, ref[:B, :, p], atol=2e-2)
 
 
