@@ -227,11 +227,18 @@ DORY_API int dory_debug_gemm(const void* A, const void* B, float* C, int M, int 
  * [B*C, n_q*head_dim] (already sigmoid), k_cache / v_cache
  * [B, n_kv, S, head_dim] holding positions < P0 in ring slot p mod S;
  * out [B*C, n_q*head_dim] = softmax-weighted values times gate.  window <= 0
- * means full causal; scale <= 0 means sqrt(head_dim).  All bf16, device. */
+ * means full causal; scale <= 0 means sqrt(head_dim).  All bf16, device.
+ * With C == 1 the split-key decode kernels run and need `scratch`: device
+ * memory of at least dory_debug_attention_scratch_bytes(B, n_q, head_dim)
+ * bytes (ignored otherwise). */
 DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur,
                                   const void* k_cache, const void* v_cache, const void* gate,
                                   void* out, int B, int C, int P0, int S, int n_q, int n_kv,
-                                  int head_dim, int window, float scale, void* stream);
+                                  int head_dim, int window, float scale, void* scratch,
+                                  size_t scratch_bytes, void* stream);
+
+/* Scratch bytes dory_debug_attention needs for one-token (decode) calls. */
+DORY_API size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim);
 
 #ifdef __cplusplus
 }

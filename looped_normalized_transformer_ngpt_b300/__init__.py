@@ -83,7 +83,8 @@ _SIGS = {
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
-                                  ctypes.c_float, _P]),
+                                  ctypes.c_float, _P, ctypes.c_size_t, _P]),
+    "dory_debug_attention_scratch_bytes": (ctypes.c_size_t, [_I, _I, _I]),
 }
 
 
@@ -306,8 +307,13 @@ def debug_gemm(A, B, C=None, stream=None):
 
 def debug_attention(q, k_cur, v_cur, k_cache, v_cache, gate, out, B, C, P0, S, n_q, n_kv,
                     head_dim, window, scale=0.0, stream=None):
-    """The library's attention kernel alone (all tensors bf16 on the device)."""
+    """The library's attention step alone (all tensors bf16 on the device);
+    one-token calls run the split-key decode kernels on a torch scratch buffer."""
+    import torch
+    nbytes = int(lib().dory_debug_attention_scratch_bytes(B, n_q, head_dim))
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=out.device) if C == 1 else None
     _check("dory_debug_attention", lib().dory_debug_attention(
         _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(k_cache), _ptr(v_cache), _ptr(gate), _ptr(out),
-        B, C, P0, S, n_q, n_kv, head_dim, window, scale, _stream_ptr(stream)))
+        B, C, P0, S, n_q, n_kv, head_dim, window, scale, _ptr(scratch), nbytes,
+        _stream_ptr(stream)))
     return out

@@ -289,3 +289,187 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
 }
 
 }  // namespace dory
+
+namespace dory {
+
+// ---------------------------------------------------------------------------
+// Decode attention (one new token per sequence), split over the keys.
+//
+// The new token at position P0 sees its own current-loop key/value and the
+// cached keys of earlier positions (final-loop or loop-i entries; "Dory1.0-4B:
+// A Looped Normalized-GPT", Last-Loop KV Caching).  The visible keys are cut
+// into splits of `chunk` keys; one CTA = (split, kv head, sequence) serves
+// all G query heads of that kv head from one shared-memory copy of each K/V
+// tile and writes an un-normalised partial (o, running max m, sum l) per
+// head.  The combine kernel merges the splits, normalises, applies the gate.
+// Memory-bound: each K/V byte is read once per loop, with 16-byte loads.
+// ---------------------------------------------------------------------------
+constexpr int kDecMaxSplits = 128;
+constexpr int kDecTile = 64;
+constexpr int kDecMaxG = 8;
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;        // [B, n_q, dh]
+  const __nv_bfloat16* k_cur;    // [B, n_kv, dh]
+  const __nv_bfloat16* v_cur;
+  const __nv_bfloat16* k_cache;  // [max_batch, n_kv, S, dh]
+  const __nv_bfloat16* v_cache;
+  int P0, S, n_q, n_kv, window;
+  float scale_log2;
+  int chunk, n_splits;
+  float* part_o;                 // [B, n_q, kDecMaxSplits, dh]
+  float* part_ml;                // [B, n_q, kDecMaxSplits, 2]
+};
+
+template <int DH>
+__global__ void __launch_bounds__(128) attn_decode_split_kernel(const DecodeArgs a) {
+  constexpr int KP = DH + 8;                            // padded bf16 row (conflict-free)
+  __shared__ __align__(16) __nv_bfloat16 ks[kDecTile * KP];
+  __shared__ __align__(16) __nv_bfloat16 vs[kDecTile * DH];
+  __shared__ float qs[kDecMaxG * DH];
+  __shared__ float ps[kDecMaxG * kDecTile];
+  __shared__ float m_s[kDecMaxG], l_s[kDecMaxG], c_s[kDecMaxG];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.n_q / a.n_kv;
+  const int p = a.P0;
+  const int lo = a.window > 0 ? max(0, p - a.window + 1) : 0;
+  const int k0 = lo + split * a.chunk;
+  const int k1 = min(k0 + a.chunk, p + 1);
+  for (int i = tid; i < G * DH; i += 128) {
+    const int g = i / DH, d = i % DH;
+    qs[i] = __bfloat162float(a.q[((long long)b * a.n_q + kvh * G + g) * DH + d]);
+  }
+  if (tid < G) {
+    m_s[tid] = -INFINITY;
+    l_s[tid] = 0.f;
+  }
+  constexpr int ITEMS = kDecMaxG * DH / 128;
+  float o[ITEMS];
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) o[i] = 0.f;
+  constexpr int CPR = DH / 8;                           // 16-byte chunks per row
+  for (int t0 = k0; t0 < k1; t0 += kDecTile) {
+    const int n = min(kDecTile, k1 - t0);
+    __syncthreads();
+    for (int i = tid; i < kDecTile * CPR; i += 128) {
+      const int r = i / CPR, c = i % CPR;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (r < n) {
+        const int j = t0 + r;
+        long long off;
+        const __nv_bfloat16 *kb, *vb;
+        if (j < a.P0) {
+          off = (((long long)b * a.n_kv + kvh) * a.S + (j % a.S)) * DH + c * 8;
+          kb = a.k_cache;
+          vb = a.v_cache;
+        } else {
+          off = ((long long)b * a.n_kv + kvh) * DH + c * 8;
+          kb = a.k_cur;
+          vb = a.v_cur;
+        }
+        kv = *reinterpret_cast<const uint4*>(kb + off);
+        vv = *reinterpret_cast<const uint4*>(vb + off);
+      }
+      *reinterpret_cast<uint4*>(ks + r * KP + c * 8) = kv;
+      *reinterpret_cast<uint4*>(vs + r * DH + c * 8) = vv;
+    }
+    __syncthreads();
+    // scores for (head g, key r)
+    for (int i = tid; i < G * kDecTile; i += 128) {
+      const int g = i / kDecTile, r = i % kDecTile;
+      float s = -INFINITY;
+      if (r < n) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPR; ++c) {
+          float kf[8];
+          const uint4 u = *reinterpret_cast<const uint4*>(ks + r * KP + c * 8);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            kf[2 * e] = f.x;
+            kf[2 * e + 1] = f.y;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(qs[g * DH + c * 8 + e], kf[e], acc);
+        }
+        s = acc * a.scale_log2;
+      }
+      ps[g * kDecTile + r] = s;
+    }
+    __syncthreads();
+    // online softmax per head (warp w handles heads w, w + 4, ...)
+    for (int g = warp; g < G; g += 4) {
+      const float s0 = ps[g * kDecTile + lane], s1 = ps[g * kDecTile + lane + 32];
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_old = m_s[g];
+      const float m_new = fmaxf(m_old, mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float p0 = exp2f(s0 - m_use), p1 = exp2f(s1 - m_use);
+      ps[g * kDecTile + lane] = p0;
+      ps[g * kDecTile + lane + 32] = p1;
+      const float sum = warp_sum(p0 + p1);
+      if (lane == 0) {
+        const float corr = exp2f(m_old - m_use);
+        c_s[g] = corr;
+        l_s[g] = l_s[g] * corr + sum;
+        m_s[g] = m_new;
+      }
+    }
+    __syncthreads();
+    // o[g][d] = corr * o + sum_r p[g][r] v[r][d]
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      const int i = tid + it * 128;
+      const int g = i / DH, d = i % DH;
+      if (g < G) {
+        float acc = o[it] * c_s[g];
+        for (int r = 0; r < n; ++r)
+          acc = fmaf(ps[g * kDecTile + r], __bfloat162float(vs[r * DH + d]), acc);
+        o[it] = acc;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) {
+    const int i = tid + it * 128;
+    const int g = i / DH, d = i % DH;
+    if (g < G) {
+      const long long base = (((long long)b * a.n_q + kvh * G + g) * kDecMaxSplits + split);
+      a.part_o[base * DH + d] = o[it];
+      if (d == 0) {
+        a.part_ml[base * 2] = m_s[g];
+        a.part_ml[base * 2 + 1] = l_s[g];
+      }
+    }
+  }
+}
+
+// Merges the splits of every (sequence, head): out = gate * sum_s o_s 2^(m_s - M)
+// / sum_s l_s 2^(m_s - M).  grid = B * n_q, block = dh.
+__global__ void attn_decode_combine_kernel(const float* part_o, const float* part_ml, int n_splits,
+                                           int n_q, int dh, const __nv_bfloat16* gate,
+                                           __nv_bfloat16* out) {
+  const long long bh = blockIdx.x;
+  const int d = threadIdx.x;
+  const float* ml = part_ml + bh * kDecMaxSplits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ml[2 * s]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float w = ml[2 * s] == -INFINITY ? 0.f : exp2f(ml[2 * s] - M);
+    L += ml[2 * s + 1] * w;
+    acc += part_o[(bh * kDecMaxSplits + s) * dh + d] * w;
+  }
+  const long long b = bh / n_q, h = bh % n_q;
+  const long long idx = (b * n_q + h) * dh + d;
+  const float gt = __bfloat162float(gate[idx]);
+  out[idx] = __float2bfloat16_rn(L > 0.f ? acc * (1.0f / L) * gt : 0.f);
+}
+
+}  // namespace dory

@@ -28,6 +28,7 @@
 #include "dory.h"
 #include "attn.cuh"
 #include "gemm_tc.cuh"
+#include "gemv.cuh"
 #include "rowops.cuh"
 
 using namespace dory;
@@ -37,7 +38,8 @@ namespace {
 constexpr int kGemmBN = 256;
 
 struct WsLayout {
-  size_t status, h32, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, total;
+  size_t status, h32, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, gy, dec_o, dec_ml,
+      total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -65,6 +67,13 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.m = take(M * (size_t)c.ffn * 2);
   L.rope_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);
   L.rope_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
+  // few-row projections (decode): fp32 output of the QKV+gate / up+gate GEMV
+  const size_t nq = (size_t)(2 * c.n_q + 2 * c.n_kv) * c.head_dim;
+  const size_t wide = nq > 2 * (size_t)c.ffn ? nq : 2 * (size_t)c.ffn;
+  L.gy = take((size_t)kGemvMaxM * wide * 4);
+  // split-KV decode attention partials
+  L.dec_o = take((size_t)max_batch * c.n_q * kDecMaxSplits * c.head_dim * 4);
+  L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
   L.total = off;
   return L;
 }
@@ -100,7 +109,7 @@ int validate_config(const dory_config* c) {
   if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) return DORY_EUNSUPPORTED;
   if (c->d % 128 || c->d > 8 * kRowThreads * kRowMaxChunks) return DORY_EUNSUPPORTED;
   if (c->ffn % (kGemmBN / 2)) return DORY_EUNSUPPORTED;
-  if (64 % (c->n_q / c->n_kv)) return DORY_EUNSUPPORTED;
+  if (64 % (c->n_q / c->n_kv) || c->n_q / c->n_kv > kDecMaxG) return DORY_EUNSUPPORTED;
   if (c->vocab % 16) return DORY_EUNSUPPORTED;
   if (kGemmBN % c->head_dim) return DORY_EUNSUPPORTED;
   if (c->rope && (!(c->rope_base_swa > 0) || !(c->rope_base_full > 0))) return DORY_EINVAL;
@@ -183,6 +192,41 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
   const int G = a.n_q / a.n_kv, BQ = AttnCfg<DH>::BR / G;
   dim3 grid((a.C + BQ - 1) / BQ, a.n_kv, B);
   attn_prefill_kernel<DH><<<grid, 128, AttnCfg<DH>::SMEM, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
+// Y[M, N] (row stride ldy) = scale * X[M, K] . W[N, K]^T for M <= kGemvMaxM.
+int launch_gemv(const __nv_bfloat16* X, int ldx, int M, const void* W, int N, int K, float* Y,
+                int ldy, const float* scale, cudaStream_t st) {
+  const int grid = (N + kGemvRowsPerCta - 1) / kGemvRowsPerCta;
+  const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(W);
+  if (M <= 4)
+    gemv_kernel<4><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
+  else if (M <= 8)
+    gemv_kernel<8><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
+  else
+    gemv_kernel<16><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
+  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
+// Split-KV decode attention: partial kernel + combine.
+template <int DH>
+int launch_decode_attn(DecodeArgs a, int B, const __nv_bfloat16* gate, __nv_bfloat16* out,
+                       cudaStream_t st) {
+  const int lo = a.window > 0 ? (a.P0 - a.window + 1 > 0 ? a.P0 - a.window + 1 : 0) : 0;
+  const int n_keys = a.P0 - lo + 1;
+  int target = 2 * num_sms() / (B * a.n_kv);
+  if (target < 1) target = 1;
+  int chunk = (n_keys + target - 1) / target;
+  const int min_chunk = (n_keys + kDecMaxSplits - 1) / kDecMaxSplits;
+  if (chunk < min_chunk) chunk = min_chunk;
+  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+  a.chunk = chunk;
+  a.n_splits = (n_keys + chunk - 1) / chunk;
+  attn_decode_split_kernel<DH><<<dim3(a.n_splits, a.n_kv, B), 128, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return DORY_ECUDA;
+  attn_decode_combine_kernel<<<B * a.n_q, DH, 0, st>>>(a.part_o, a.part_ml, a.n_splits, a.n_q, DH,
+                                                      gate, out);
   return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
@@ -271,8 +315,22 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   ga.s_qk = w.s_qk;
   ga.rope = c.rope ? wsp<float2>(m, full ? m->L.rope_full : m->L.rope_swa) : nullptr;
   ga.rows_per_seq = C;
-  pb(m, DORY_K_QKVG_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st)));
+  const bool few = M <= kGemvMaxM;
+  __nv_bfloat16* hb = wsp<__nv_bfloat16>(m, m->L.hb);
+  float* gy = wsp<float>(m, m->L.gy);
+  if (few) {
+    pb(m, DORY_K_QKVG_GEMM, st);
+    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_qkvg, ga.N, c.d, gy, ga.N, nullptr, st)));
+    pb(m, DORY_K_QKVG_GEMM, st);
+    const int nheads = 2 * c.n_q + 2 * c.n_kv;
+    const int thr = c.head_dim / 2 > 32 ? c.head_dim / 2 : 32;
+    qkvg_post_kernel<<<dim3(M, nheads), thr, 0, st>>>(gy, M, c.n_q, c.n_kv, c.head_dim, w.s_qk,
+                                                       ga.rope, C, ga.q, ga.k, ga.v, ga.g);
+    DORY_TRY(pe(m, st));
+  } else {
+    pb(m, DORY_K_QKVG_GEMM, st);
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st)));
+  }
 
   // attention over cached + current keys
   const int S = slots_of(c, l, m->max_ctx);
@@ -298,9 +356,29 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   aa.scale_log2 = scale * 1.4426950408889634f;
   pb(m, DORY_K_ATTENTION, st);
   int arc = DORY_EUNSUPPORTED;
-  if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
-  if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
-  if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
+  if (C == 1) {
+    DecodeArgs da{};
+    da.q = aa.q;
+    da.k_cur = aa.k_cur;
+    da.v_cur = aa.v_cur;
+    da.k_cache = aa.k_cache;
+    da.v_cache = aa.v_cache;
+    da.P0 = P0;
+    da.S = S;
+    da.n_q = c.n_q;
+    da.n_kv = c.n_kv;
+    da.window = aa.window;
+    da.scale_log2 = aa.scale_log2;
+    da.part_o = wsp<float>(m, m->L.dec_o);
+    da.part_ml = wsp<float>(m, m->L.dec_ml);
+    if (c.head_dim == 32) arc = launch_decode_attn<32>(da, B, aa.gate, aa.out, st);
+    if (c.head_dim == 64) arc = launch_decode_attn<64>(da, B, aa.gate, aa.out, st);
+    if (c.head_dim == 128) arc = launch_decode_attn<128>(da, B, aa.gate, aa.out, st);
+  } else {
+    if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
+    if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
+    if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
+  }
   DORY_TRY(pe(m, st, arc));
 
   // KV write: the last min(C, S) positions of the call
@@ -322,7 +400,10 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   go.out = wsp<float>(m, m->L.y32);
   go.ldo = c.d;
   pb(m, DORY_K_O_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
+  if (few)
+    DORY_TRY(pe(m, st, launch_gemv(aa.out, hq, M, w.w_o, c.d, hq, go.out, c.d, nullptr, st)));
+  else
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
   pb(m, DORY_K_NGPT_UPDATE, st);
   ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
                                                 wsp<__nv_bfloat16>(m, m->L.hb),
@@ -338,8 +419,18 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gu.status = status;
   gu.m_out = wsp<__nv_bfloat16>(m, m->L.m);
   gu.ldm = c.ffn;
-  pb(m, DORY_K_UPGATE_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
+  if (few) {
+    pb(m, DORY_K_UPGATE_GEMM, st);
+    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_upgate, 2 * c.ffn, c.d, gy, 2 * c.ffn, nullptr,
+                                   st)));
+    pb(m, DORY_K_UPGATE_GEMM, st);
+    const int n = M * c.ffn;
+    swiglu_post_kernel<<<(n + 255) / 256, 256, 0, st>>>(gy, M, c.ffn, gu.m_out);
+    DORY_TRY(pe(m, st));
+  } else {
+    pb(m, DORY_K_UPGATE_GEMM, st);
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
+  }
   GemmArgs gd{};
   gd.M = M;
   gd.N = c.d;
@@ -348,7 +439,11 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gd.out = wsp<float>(m, m->L.y32);
   gd.ldo = c.d;
   pb(m, DORY_K_DOWN_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
+  if (few)
+    DORY_TRY(pe(m, st, launch_gemv(gu.m_out, c.ffn, M, w.w_down, c.d, c.ffn, gd.out, c.d, nullptr,
+                                   st)));
+  else
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
   pb(m, DORY_K_NGPT_UPDATE, st);
   ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
                                                 wsp<__nv_bfloat16>(m, m->L.hb),
@@ -426,7 +521,13 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     gl.status = status;
     gl.col_scale = m->s_z;
     gl.ldo = c.vocab;
-    if (n_logit_rows == 1) {
+    if (n_logit_rows == 1 && B <= kGemvMaxM) {
+      pb(m, DORY_K_LM_HEAD, st);
+      DORY_TRY(pe(m, st, launch_gemv(wsp<__nv_bfloat16>(m, m->L.hb) + (size_t)(C - 1) * c.d,
+                                     C * c.d, B, m->embed_out, c.vocab, c.d,
+                                     logits + (long long)t_out0 * c.vocab,
+                                     (int)(ld_seq * c.vocab), m->s_z, st)));
+    } else if (n_logit_rows == 1) {
       // one row per sequence: a strided view of hb (row stride C * d)
       CUtensorMap tm_last;
       if (!encode_bf16(&tm_last, m->ws + m->L.hb + (size_t)(C - 1) * c.d * 2, B, c.d,
@@ -732,12 +833,21 @@ int dory_debug_gemm(const void* A, const void* B, float* C, int M, int N, int K,
   return launch_gemm<kGemmBN, EPI_F32>(ta, tb, g, static_cast<cudaStream_t>(stream));
 }
 
+size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim) {
+  if (B <= 0 || n_q <= 0 || head_dim <= 0) return 0;
+  return align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4) +
+         align256((size_t)B * n_q * kDecMaxSplits * 2 * 4);
+}
+
 int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, const void* k_cache,
                          const void* v_cache, const void* gate, void* out, int B, int C, int P0,
                          int S, int n_q, int n_kv, int head_dim, int window, float scale,
-                         void* stream) {
+                         void* scratch, size_t scratch_bytes, void* stream) {
   if (!q || !k_cur || !v_cur || !gate || !out || B <= 0 || C <= 0 || P0 < 0 || n_q <= 0 ||
-      n_kv <= 0 || n_q % n_kv || 64 % (n_q / n_kv))
+      n_kv <= 0 || n_q % n_kv || 64 % (n_q / n_kv) || n_q / n_kv > kDecMaxG)
+    return DORY_EINVAL;
+  if (C == 1 && (!scratch || ((uintptr_t)scratch & 255) ||
+                 scratch_bytes < dory_debug_attention_scratch_bytes(B, n_q, head_dim)))
     return DORY_EINVAL;
   if (P0 > 0 && (!k_cache || !v_cache || S <= 0)) return DORY_EINVAL;
   AttnArgs a{};
@@ -756,6 +866,27 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
   a.window = window > 0 ? window : 0;
   a.scale_log2 = (scale > 0.f ? scale : sqrtf((float)head_dim)) * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (C == 1) {
+    DecodeArgs da{};
+    da.q = a.q;
+    da.k_cur = a.k_cur;
+    da.v_cur = a.v_cur;
+    da.k_cache = a.k_cache;
+    da.v_cache = a.v_cache;
+    da.P0 = P0;
+    da.S = a.S;
+    da.n_q = n_q;
+    da.n_kv = n_kv;
+    da.window = a.window;
+    da.scale_log2 = a.scale_log2;
+    da.part_o = static_cast<float*>(scratch);
+    da.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                          align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4));
+    if (head_dim == 32) return launch_decode_attn<32>(da, B, a.gate, a.out, st);
+    if (head_dim == 64) return launch_decode_attn<64>(da, B, a.gate, a.out, st);
+    if (head_dim == 128) return launch_decode_attn<128>(da, B, a.gate, a.out, st);
+    return DORY_EUNSUPPORTED;
+  }
   if (head_dim == 32) return launch_attn<32>(a, B, st);
   if (head_dim == 64) return launch_attn<64>(a, B, st);
   if (head_dim == 128) return launch_attn<128>(a, B, st);
