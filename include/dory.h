@@ -240,6 +240,34 @@ DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* 
 /* Scratch bytes dory_debug_attention needs for one-token (decode) calls. */
 DORY_API size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim);
 
+/* One-token (decode) attention that needs no memory from the caller beyond
+ * its inputs and outputs, and allocates none.  The paper has no counterpart:
+ * this exists for callers that cannot hand the library any scratch memory,
+ * such as a plug-in running inside a host program that owns every device
+ * allocation and gives its extensions neither an allocator nor a workspace,
+ * or a latency-critical serving loop that forbids cudaMalloc after start-up
+ * because it can block and synchronise the device.
+ *
+ * Arguments and result are those of dory_debug_attention with C == 1 (q
+ * [B, n_q, head_dim], k_cur / v_cur [B, n_kv, head_dim], gate and out
+ * [B, n_q * head_dim], cache [B, n_kv, S, head_dim] holding positions < P0 in
+ * slot p mod S; bf16, device).  The split-key partial results live in a fixed
+ * 16 MiB array inside the library; every GPU that loads the library holds it
+ * until the process exits.  Calls with
+ * dory_debug_attention_scratch_bytes(B, n_q, head_dim) > 16 MiB are refused
+ * with DORY_ECAPACITY before any launch (for head_dim 128 that is
+ * B * n_q > 252).  The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress, device current); make that first call
+ * before any stream capture.  All calls share the one array and leave it
+ * holding their partials; nothing in it needs to start at zero, but calls
+ * whose kernels overlap on the GPU (other streams, other threads) race on it,
+ * so serialise them. */
+DORY_API int dory_decode_attention_noalloc(const void* q, const void* k_cur, const void* v_cur,
+                                           const void* k_cache, const void* v_cache,
+                                           const void* gate, void* out, int B, int P0, int S,
+                                           int n_q, int n_kv, int head_dim, int window,
+                                           float scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

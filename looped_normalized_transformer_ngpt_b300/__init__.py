@@ -85,6 +85,8 @@ _SIGS = {
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                   ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "dory_debug_attention_scratch_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "dory_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                           _I, ctypes.c_float, _P]),
 }
 
 

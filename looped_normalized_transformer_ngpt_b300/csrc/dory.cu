@@ -894,3 +894,71 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Decode attention without caller scratch: the split-key partials go to a
+// fixed array in device memory that the library owns for the process's life.
+// ------------------------------------------------------------------------
+static constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;   // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device (host code cannot use the symbol itself as a device pointer).
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return DORY_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORY_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DORY_OK;
+}
+}  // namespace
+
+extern "C" int dory_decode_attention_noalloc(const void* q, const void* k_cur, const void* v_cur,
+                                             const void* k_cache, const void* v_cache,
+                                             const void* gate, void* out, int B, int P0, int S,
+                                             int n_q, int n_kv, int head_dim, int window,
+                                             float scale, void* stream) {
+  if (!q || !k_cur || !v_cur || !gate || !out || B <= 0 || P0 < 0 || n_q <= 0 || n_kv <= 0 ||
+      n_q % n_kv || n_q / n_kv > kDecMaxG)
+    return DORY_EINVAL;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return DORY_EUNSUPPORTED;
+  if (P0 > 0 && (!k_cache || !v_cache || S <= 0)) return DORY_EINVAL;
+  const size_t need = dory_debug_attention_scratch_bytes(B, n_q, head_dim);
+  if (need == 0 || need > kNoAllocScratchBytes) return DORY_ECAPACITY;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != DORY_OK) return rc;
+  DecodeArgs da{};
+  da.q = static_cast<const __nv_bfloat16*>(q);
+  da.k_cur = static_cast<const __nv_bfloat16*>(k_cur);
+  da.v_cur = static_cast<const __nv_bfloat16*>(v_cur);
+  da.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  da.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  da.P0 = P0;
+  da.S = S > 0 ? S : 1;
+  da.n_q = n_q;
+  da.n_kv = n_kv;
+  da.window = window > 0 ? window : 0;
+  da.scale_log2 = (scale > 0.f ? scale : sqrtf((float)head_dim)) * 1.4426950408889634f;
+  // every split writes the partials the combine step reads: nothing to clear
+  da.part_o = static_cast<float*>(scratch);
+  da.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                        align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4));
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(gate);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (head_dim == 32) return launch_decode_attn<32>(da, B, g, o, st);
+  if (head_dim == 64) return launch_decode_attn<64>(da, B, g, o, st);
+  return launch_decode_attn<128>(da, B, g, o, st);
+}
