@@ -468,12 +468,37 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_target(args):
+    """One eager prefill (4 x 2048, loop count --k) and one decode step of the
+    benchmark workload, nothing else: the target for ncu launch lists and
+    kernel captures."""
+    import torch
+
+    import synth
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+    _build.build()
+    sh = synth.SMALL
+    w = synth.make_weights(sh)
+    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=SEQ + 1, max_chunk=SEQ, k_max=max(args.k, 4),
+                   cache_mode=dory.LAST_LOOP)
+    prompt = torch.tensor(synth.tokens(sh, BATCH, SEQ, seed=1000), device="cuda")
+    first = torch.tensor(synth.tokens(sh, BATCH, 1, seed=2000)[:, 0], device="cuda")
+    m.prefill(prompt, args.k)
+    m.decode(first, args.k)
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    print(json.dumps({"profile_target": "ok", "k": args.k, "launches_decode": m.launch_count()}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["dory", "reference"], default="dory")
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+                    help="profile: one eager prefill + decode step only (ncu target)")
     ap.add_argument("--k", type=int, default=4, help="loop count of the timed step")
     ap.add_argument("--decode", type=int, default=DECODE)
     ap.add_argument("--per-k", type=lambda s: [int(x) for x in s.split(",") if x],
@@ -484,6 +509,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)          # at least 3 warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "profile":
+        run_profile_target(args)
     else:
         run_gpu(args)
 
