@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
   __nv_bfloat16* sK = sQ + BR * DH;             // [2][BKEY*DH]
   __nv_bfloat16* sV = sK + 2 * BKEY * DH;       // [2][BKEY*DH]
   const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+  pdl_wait();
+  pdl_trigger();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv, BQ = BR / G;
@@ -329,6 +331,8 @@ __global__ void __launch_bounds__(128) attn_decode_split_kernel(const DecodeArgs
   __shared__ float qs[kDecMaxG * DH];
   __shared__ float ps[kDecMaxG * kDecTile];
   __shared__ float m_s[kDecMaxG], l_s[kDecMaxG], c_s[kDecMaxG];
+  pdl_wait();
+  pdl_trigger();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv;
@@ -455,6 +459,8 @@ __global__ void __launch_bounds__(128) attn_decode_split_kernel(const DecodeArgs
 __global__ void attn_decode_combine_kernel(const float* part_o, const float* part_ml, int n_splits,
                                            int n_q, int dh, const __nv_bfloat16* gate,
                                            __nv_bfloat16* out) {
+  pdl_wait();
+  pdl_trigger();
   const long long bh = blockIdx.x;
   const int d = threadIdx.x;
   const float* ml = part_ml + bh * kDecMaxSplits * 2;

@@ -108,7 +108,8 @@ int validate_config(const dory_config* c) {
   if (c->n_q % c->n_kv) return DORY_EINVAL;
   if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) return DORY_EUNSUPPORTED;
   if (c->d % 128 || c->d > 8 * kRowThreads * kRowMaxChunks) return DORY_EUNSUPPORTED;
-  if (c->ffn % (kGemmBN / 2)) return DORY_EUNSUPPORTED;
+  if (c->ffn % (kGemmBN / 2) || c->ffn > kGemvMaxK / 2 || c->d > kGemvMaxK / 2)
+    return DORY_EUNSUPPORTED;
   if (64 % (c->n_q / c->n_kv) || c->n_q / c->n_kv > kDecMaxG) return DORY_EUNSUPPORTED;
   if (c->vocab % 16) return DORY_EUNSUPPORTED;
   if (kGemmBN % c->head_dim) return DORY_EUNSUPPORTED;
@@ -148,6 +149,23 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialisation (see pdl_wait in ptx.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int g_num_sms = 0;
 int num_sms() {
   if (g_num_sms == 0) {
@@ -176,8 +194,10 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
   const int tiles = args.tiles_m * args.tiles_n;
   if (tiles == 0) return DORY_OK;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, 192, Cf::SMEM, st>>>(ta, tb, args);
-  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+  return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(192), Cf::SMEM, st, ta, tb, args) ==
+                 cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
 }
 
 template <int DH>
@@ -191,22 +211,54 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
   }
   const int G = a.n_q / a.n_kv, BQ = AttnCfg<DH>::BR / G;
   dim3 grid((a.C + BQ - 1) / BQ, a.n_kv, B);
-  attn_prefill_kernel<DH><<<grid, 128, AttnCfg<DH>::SMEM, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+  return launch_k(attn_prefill_kernel<DH>, grid, dim3(128), AttnCfg<DH>::SMEM, st, a) ==
+                 cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
 }
 
-// Y[M, N] (row stride ldy) = scale * X[M, K] . W[N, K]^T for M <= kGemvMaxM.
+// Y[M, N] (row stride ldy) = scale * X[M, K] . W[N, K]^T for M <= kGemvMaxM, or,
+// with pair_off > 0, m_out[M, N] = (X W[n]^T) * SiLU(X W[n + pair_off]^T).
+template <int MM, int J, bool SW>
+cudaError_t gemv_go(int grid, cudaStream_t st, const __nv_bfloat16* X, int ldx, int M,
+                    const __nv_bfloat16* W, int N, int K, int S, float* Y, int ldy,
+                    const float* scale, int pair_off, __nv_bfloat16* m_out, int ldm) {
+  return launch_k(gemv_kernel<MM, J, SW>, dim3(grid), dim3(kGemvThreads), 0, st, X, ldx, M, W, N,
+                  K, S, Y, ldy, scale, pair_off, m_out, ldm);
+}
+
+template <int MM, bool SW>
+cudaError_t gemv_j(int J, int grid, cudaStream_t st, const __nv_bfloat16* X, int ldx, int M,
+                   const __nv_bfloat16* W, int N, int K, int S, float* Y, int ldy,
+                   const float* scale, int pair_off, __nv_bfloat16* m_out, int ldm) {
+  if (J <= 2) return gemv_go<MM, 2, SW>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+  if (J <= 4) return gemv_go<MM, 4, SW>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+  if (SW) return cudaErrorInvalidValue;
+  if (J <= 6) return gemv_go<MM, 6, false>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+  return gemv_go<MM, 8, false>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+}
+
 int launch_gemv(const __nv_bfloat16* X, int ldx, int M, const void* W, int N, int K, float* Y,
-                int ldy, const float* scale, cudaStream_t st) {
-  const int grid = (N + kGemvRowsPerCta - 1) / kGemvRowsPerCta;
+                int ldy, const float* scale, cudaStream_t st, int pair_off = 0,
+                __nv_bfloat16* m_out = nullptr, int ldm = 0) {
+  const bool sw = pair_off > 0;
+  const int jmax = sw ? 4 : 8;
+  const int kc = (K + 255) / 256;                  // 256-element chunks per row
+  int S = 1;
+  while ((kc + S - 1) / S > jmax && S < kGemvWarps) S *= 2;
+  const int J = (kc + S - 1) / S;
+  if (J > jmax || M > kGemvMaxM) return DORY_EUNSUPPORTED;
+  const int rows_per_cta = kGemvWarps / S;
+  const int grid = (N + rows_per_cta - 1) / rows_per_cta;
   const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(W);
+  cudaError_t e;
   if (M <= 4)
-    gemv_kernel<4><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
-  else if (M <= 8)
-    gemv_kernel<8><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
+    e = sw ? gemv_j<4, true>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, pair_off, m_out, ldm)
+           : gemv_j<4, false>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, 0, m_out, ldm);
   else
-    gemv_kernel<16><<<grid, kGemvWarps * 32, 0, st>>>(X, ldx, M, w, N, K, Y, ldy, scale);
-  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+    e = sw ? gemv_j<16, true>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, pair_off, m_out, ldm)
+           : gemv_j<16, false>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, 0, m_out, ldm);
+  return e == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
 // Split-KV decode attention: partial kernel + combine.
@@ -223,11 +275,14 @@ int launch_decode_attn(DecodeArgs a, int B, const __nv_bfloat16* gate, __nv_bflo
   chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
   a.chunk = chunk;
   a.n_splits = (n_keys + chunk - 1) / chunk;
-  attn_decode_split_kernel<DH><<<dim3(a.n_splits, a.n_kv, B), 128, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return DORY_ECUDA;
-  attn_decode_combine_kernel<<<B * a.n_q, DH, 0, st>>>(a.part_o, a.part_ml, a.n_splits, a.n_q, DH,
-                                                      gate, out);
-  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+  if (launch_k(attn_decode_split_kernel<DH>, dim3(a.n_splits, a.n_kv, B), dim3(128), 0, st, a) !=
+      cudaSuccess)
+    return DORY_ECUDA;
+  return launch_k(attn_decode_combine_kernel, dim3(B * a.n_q), dim3(DH), 0, st,
+                  (const float*)a.part_o, (const float*)a.part_ml, a.n_splits, a.n_q, DH, gate,
+                  out) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
 }
 
 }  // namespace
@@ -289,6 +344,14 @@ int pe(dory_model* m, cudaStream_t st, int rc = DORY_OK) {
   return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
+int ngpt_update(dory_model* m, int M, const float* alpha, cudaStream_t st) {
+  return launch_k(ngpt_update_kernel, dim3(M), dim3(kRowThreads), 0, st, wsp<float>(m, m->L.h32),
+                  wsp<__nv_bfloat16>(m, m->L.hb), (const float*)wsp<float>(m, m->L.y32), alpha,
+                  m->cfg.d) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
 int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
               const CUtensorMap& tm_hb, const CUtensorMap& tm_att, const CUtensorMap& tm_m,
               cudaStream_t st) {
@@ -324,9 +387,12 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     pb(m, DORY_K_QKVG_GEMM, st);
     const int nheads = 2 * c.n_q + 2 * c.n_kv;
     const int thr = c.head_dim / 2 > 32 ? c.head_dim / 2 : 32;
-    qkvg_post_kernel<<<dim3(M, nheads), thr, 0, st>>>(gy, M, c.n_q, c.n_kv, c.head_dim, w.s_qk,
-                                                       ga.rope, C, ga.q, ga.k, ga.v, ga.g);
-    DORY_TRY(pe(m, st));
+    DORY_TRY(pe(m, st,
+                launch_k(qkvg_post_kernel, dim3(M, nheads), dim3(thr), 0, st, (const float*)gy, M,
+                         c.n_q, c.n_kv, c.head_dim, w.s_qk, (const float2*)ga.rope, C, ga.q, ga.k,
+                         ga.v, ga.g) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
   } else {
     pb(m, DORY_K_QKVG_GEMM, st);
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st)));
@@ -386,9 +452,12 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     const int t_first = C > S ? C - S : 0;
     dim3 grid(C - t_first, B);
     pb(m, DORY_K_KV_WRITE, st);
-    kv_write_kernel<<<grid, 64, 0, st>>>(ga.k, ga.v, kc, vc, C, P0, S, t_first, c.n_kv,
-                                         c.head_dim);
-    DORY_TRY(pe(m, st));
+    DORY_TRY(pe(m, st,
+                launch_k(kv_write_kernel, grid, dim3(64), 0, st, (const __nv_bfloat16*)ga.k,
+                         (const __nv_bfloat16*)ga.v, kc, vc, C, P0, S, t_first, c.n_kv,
+                         c.head_dim) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
   }
 
   // output projection + nGPT step
@@ -405,10 +474,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   else
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
   pb(m, DORY_K_NGPT_UPDATE, st);
-  ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
-                                                wsp<__nv_bfloat16>(m, m->L.hb),
-                                                wsp<float>(m, m->L.y32), w.alpha_attn, c.d);
-  DORY_TRY(pe(m, st));
+  DORY_TRY(pe(m, st, ngpt_update(m, M, w.alpha_attn, st)));
 
   // SwiGLU MLP + nGPT step
   GemmArgs gu{};
@@ -421,12 +487,8 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gu.ldm = c.ffn;
   if (few) {
     pb(m, DORY_K_UPGATE_GEMM, st);
-    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_upgate, 2 * c.ffn, c.d, gy, 2 * c.ffn, nullptr,
-                                   st)));
-    pb(m, DORY_K_UPGATE_GEMM, st);
-    const int n = M * c.ffn;
-    swiglu_post_kernel<<<(n + 255) / 256, 256, 0, st>>>(gy, M, c.ffn, gu.m_out);
-    DORY_TRY(pe(m, st));
+    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_upgate, c.ffn, c.d, nullptr, 0, nullptr, st,
+                                   c.ffn, gu.m_out, c.ffn)));
   } else {
     pb(m, DORY_K_UPGATE_GEMM, st);
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
@@ -445,18 +507,17 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   else
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
   pb(m, DORY_K_NGPT_UPDATE, st);
-  ngpt_update_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
-                                                wsp<__nv_bfloat16>(m, m->L.hb),
-                                                wsp<float>(m, m->L.y32), w.alpha_mlp, c.d);
-  return pe(m, st);
+  return pe(m, st, ngpt_update(m, M, w.alpha_mlp, st));
 }
 
 int boundary(dory_model* m, int M, int mode, cudaStream_t st) {
   pb(m, DORY_K_BOUNDARY, st);
-  boundary_kernel<<<M, kRowThreads, 0, st>>>(wsp<float>(m, m->L.h32),
-                                             wsp<__nv_bfloat16>(m, m->L.hb),
-                                             wsp<float>(m, m->L.x32), m->cfg.d, mode);
-  return pe(m, st);
+  return pe(m, st,
+            launch_k(boundary_kernel, dim3(M), dim3(kRowThreads), 0, st, wsp<float>(m, m->L.h32),
+                     wsp<__nv_bfloat16>(m, m->L.hb), wsp<float>(m, m->L.x32), m->cfg.d, mode) ==
+                    cudaSuccess
+                ? DORY_OK
+                : DORY_ECUDA);
 }
 
 // One forward step over B sequences x C tokens at positions P0 .. P0+C-1.
@@ -480,20 +541,28 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     const int n = C * (c.head_dim / 2);
     const int blocks = (n + 255) / 256;
     pb(m, DORY_K_ROPE, st);
-    rope_table_kernel<<<blocks, 256, 0, st>>>(wsp<float2>(m, m->L.rope_swa), C, P0, c.head_dim,
-                                             (double)c.rope_base_swa);
-    DORY_TRY(pe(m, st));
+    DORY_TRY(pe(m, st,
+                launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st,
+                         wsp<float2>(m, m->L.rope_swa), C, P0, c.head_dim,
+                         (double)c.rope_base_swa) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
     pb(m, DORY_K_ROPE, st);
-    rope_table_kernel<<<blocks, 256, 0, st>>>(wsp<float2>(m, m->L.rope_full), C, P0, c.head_dim,
-                                             (double)c.rope_base_full);
-    DORY_TRY(pe(m, st));
+    DORY_TRY(pe(m, st,
+                launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st,
+                         wsp<float2>(m, m->L.rope_full), C, P0, c.head_dim,
+                         (double)c.rope_base_full) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
   }
   pb(m, DORY_K_EMBED, st);
-  embed_kernel<<<M, kRowThreads, 0, st>>>(tokens, ld_tok, C,
-                                          reinterpret_cast<const __nv_bfloat16*>(m->embed_in),
-                                          c.vocab, c.d, wsp<float>(m, m->L.h32),
-                                          wsp<__nv_bfloat16>(m, m->L.hb), status);
-  DORY_TRY(pe(m, st));
+  DORY_TRY(pe(m, st,
+              launch_k(embed_kernel, dim3(M), dim3(kRowThreads), 0, st, tokens, ld_tok, C,
+                       reinterpret_cast<const __nv_bfloat16*>(m->embed_in), c.vocab, c.d,
+                       wsp<float>(m, m->L.h32), wsp<__nv_bfloat16>(m, m->L.hb), status) ==
+                      cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA));
 
   for (int l = 0; l < c.n_in; ++l)
     DORY_TRY(run_layer(m, l, 0, true, B, C, P0, tm_hb, tm_att, tm_m, st));
@@ -698,8 +767,11 @@ int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_m
   if (r != DORY_OK) return r;
   if (next) {
     pb(m, DORY_K_ARGMAX, st);
-    argmax_kernel<<<B, 1024, 0, st>>>(logits, m->cfg.vocab, next);
-    return pe(m, st);
+    return pe(m, st,
+              launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits,
+                       m->cfg.vocab, next) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA);
   }
   return DORY_OK;
 }

@@ -1,27 +1,31 @@
 // gemv.cuh - projections for few rows (decode: M = batch <= 16).
 //
-// With M <= 16 the projections are weight-streaming (8 to 16 FLOP per weight
-// byte): the bound is HBM bandwidth, not the tensor cores.  Each warp owns
-// two weight rows, reads them once with 16-byte non-caching loads (all K
-// chunks issued before use), multiplies with the M activation rows (L1/L2
-// resident) in fp32 and reduces across the warp; one CTA = 4 warps = 8 output
-// features, so even N = 1024 spreads over 128 CTAs.
+// With M <= 16 rows the projections stream weights (2 M FLOP per 2-byte
+// weight): the bound is HBM bandwidth and load latency, not the tensor cores.
+// One warp owns one output feature (or, for SwiGLU, the pair of W_up and W_sl
+// rows of one feature) and one K segment of J x 256 elements: every lane
+// issues all J 16-byte non-caching weight loads of its segment before using
+// any, multiplies with the M activation rows (L2 resident) in fp32 and reduces
+// across the warp; the S segments of a row (S = 1, 2, 4 or 8, chosen so that
+// J <= 8) are summed through shared memory.  A CTA is 8 warps = 8 / S
+// features, so even N = 1024 spreads over 128 to 1024 CTAs with up to
+// 8 KB of weight loads in flight per warp.
 //
-//   Y[m, n] = scale[n] * sum_k X[m, k] W[n, k]     (fp32 out)
+//   Y[m, n] = scale[n] * sum_k X[m, k] W[n, k]                 (fp32 out)
+//   SwiGLU:  m_out[m, n] = u * SiLU(v),  u = X W_up[n]^T, v = X W_sl[n]^T
 //
-// The per-projection math of the tensor-core epilogues then runs as small row
-// kernels on Y: RoPE + per-head L2 norm + s_qk for q/k, copy for v, sigmoid
-// for the gate ("Dory1.0-4B: A Looped Normalized-GPT", Architecture), and
-// m = u * SiLU(v) for the SwiGLU MLP.
+// The q/k/v/gate math of the tensor-core epilogue runs on Y in a small row
+// kernel: RoPE + per-head L2 norm + s_qk for q and k, copy for v, sigmoid for
+// the gate ("Dory1.0-4B: A Looped Normalized-GPT", Architecture).
 #pragma once
 #include "ptx.cuh"
 
 namespace dory {
 
 constexpr int kGemvMaxM = 16;
-constexpr int kGemvRowsPerWarp = 2;
-constexpr int kGemvWarps = 4;
-constexpr int kGemvRowsPerCta = kGemvRowsPerWarp * kGemvWarps;
+constexpr int kGemvThreads = 256;
+constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int kGemvMaxK = kGemvWarps * 8 * 256;     // S <= 8 segments of J <= 8 chunks
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
@@ -41,69 +45,81 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-// K must be a multiple of 8; X rows are ldx elements apart.
-template <int MM>
-__global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const __nv_bfloat16* X, int ldx,
-                                                               int M, const __nv_bfloat16* W,
-                                                               int N, int K, float* Y, int ldy,
-                                                               const float* col_scale) {
+// K must be a multiple of 8; X rows are ldx elements apart (16-byte aligned).
+// SWIGLU: W holds [W_up; W_sl] and feature n uses rows n and n + pair_off.
+template <int MM, int J, bool SWIGLU>
+__global__ void __launch_bounds__(kGemvThreads)
+    gemv_kernel(const __nv_bfloat16* X, int ldx, int M, const __nv_bfloat16* W, int N, int K,
+                int S, float* Y, int ldy, const float* col_scale, int pair_off,
+                __nv_bfloat16* m_out, int ldm) {
+  constexpr int R = SWIGLU ? 2 : 1;
+  __shared__ float red[kGemvWarps][R][MM];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp;
-  if (r0 >= N) return;
-  const bool has1 = r0 + 1 < N;
-  float acc[kGemvRowsPerWarp][MM];
+  const int rows_per_cta = kGemvWarps / S;
+  const int n = blockIdx.x * rows_per_cta + warp / S;
+  const int seg = warp % S;
+  const bool valid = n < N;
+  const int kbase = seg * (J * 256) + lane * 8;
+
+  uint4 w[R][J];
 #pragma unroll
-  for (int r = 0; r < kGemvRowsPerWarp; ++r)
+  for (int r = 0; r < R; ++r) {
+    const __nv_bfloat16* wr = W + (long long)(valid ? n + r * pair_off : 0) * K;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int k = kbase + j * 256;
+      w[r][j] = (valid && k < K) ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float acc[R][MM];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int m = 0; m < MM; ++m) acc[r][m] = 0.f;
-  const __nv_bfloat16* w0 = W + (long long)r0 * K;
-  const __nv_bfloat16* w1 = W + (long long)(has1 ? r0 + 1 : r0) * K;
-  constexpr int U = 4;   // K chunks of 256 elements in flight per lane
-  for (int kb = lane * 8; kb < K; kb += 256 * U) {
-    uint4 a[U], b[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int k = kb + u * 256;
-      if (k < K) {
-        a[u] = ld_stream16(w0 + k);
-        b[u] = ld_stream16(w1 + k);
-      }
-    }
+  for (int j = 0; j < J; ++j) {
+    const int k = kbase + j * 256;
+    if (valid && k < K) {
+      float fw[R][8];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int k = kb + u * 256;
-      if (k < K) {
-        float fa[8], fb[8];
-        bf16x8_to_f32(a[u], fa);
-        bf16x8_to_f32(b[u], fb);
+      for (int r = 0; r < R; ++r) bf16x8_to_f32(w[r][j], fw[r]);
 #pragma unroll
-        for (int m = 0; m < MM; ++m) {
-          if (m < M) {
-            float fx[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (long long)m * ldx + k), fx);
+      for (int m = 0; m < MM; ++m) {
+        if (m < M) {
+          float fx[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (long long)m * ldx + k), fx);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              acc[0][m] = fmaf(fa[i], fx[i], acc[0][m]);
-              acc[1][m] = fmaf(fb[i], fx[i], acc[1][m]);
-            }
-          }
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[r][m] = fmaf(fw[r][i], fx[i], acc[r][m]);
         }
       }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kGemvRowsPerWarp; ++r)
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int m = 0; m < MM; ++m) acc[r][m] = warp_sum(acc[r][m]);
-  if (lane == 0) {
-#pragma unroll
-    for (int r = 0; r < kGemvRowsPerWarp; ++r) {
-      const int n = r0 + r;
-      if (n >= N) break;
-      const float sc = col_scale ? col_scale[n] : 1.f;
-#pragma unroll
-      for (int m = 0; m < MM; ++m)
-        if (m < M) Y[(long long)m * ldy + n] = acc[r][m] * sc;
+    for (int m = 0; m < MM; ++m) {
+      const float v = warp_sum(acc[r][m]);
+      if (lane == 0) red[warp][r][m] = v;
+    }
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < rows_per_cta * MM) {
+    const int rl = t / MM, m = t % MM;
+    const int nn = blockIdx.x * rows_per_cta + rl;
+    if (nn < N && m < M) {
+      float s0 = 0.f, s1 = 0.f;
+      for (int sg = 0; sg < S; ++sg) {
+        s0 += red[rl * S + sg][0][m];
+        if (SWIGLU) s1 += red[rl * S + sg][R - 1][m];
+      }
+      if (SWIGLU)
+        m_out[(long long)m * ldm + nn] = __float2bfloat16_rn(s0 * (s1 / (1.0f + __expf(-s1))));
+      else
+        Y[(long long)m * ldy + nn] = s0 * (col_scale ? col_scale[nn] : 1.f);
     }
   }
 }
@@ -116,6 +132,8 @@ __global__ void qkvg_post_kernel(const float* Y, int M, int n_q, int n_kv, int d
                                  __nv_bfloat16* q, __nv_bfloat16* k, __nv_bfloat16* v,
                                  __nv_bfloat16* g) {
   __shared__ float red[8];
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x, head = blockIdx.y;
   const int half = dh / 2, i = threadIdx.x;
   const bool own = i < half;
@@ -153,17 +171,6 @@ __global__ void qkvg_post_kernel(const float* Y, int M, int n_q, int n_kv, int d
     __nv_bfloat16* dst = g + ((long long)row * n_q + head - n_q - 2 * n_kv) * dh;
     dst[i] = __float2bfloat16_rn(1.0f / (1.0f + __expf(-x1)));
     dst[i + half] = __float2bfloat16_rn(1.0f / (1.0f + __expf(-x2)));
-  }
-}
-
-// m = u * SiLU(v) from Y [M, 2F] = [u | v] (fp32) to bf16 [M, F].
-__global__ void swiglu_post_kernel(const float* Y, int M, int F, __nv_bfloat16* m_out) {
-  const long long n = (long long)M * F;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long r = idx / F, c = idx % F;
-    const float u = Y[r * 2 * F + c], s = Y[r * 2 * F + F + c];
-    m_out[idx] = __float2bfloat16_rn(u * (s / (1.0f + __expf(-s))));
   }
 }
 

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t* token
                                                             int d, float* h32, __nv_bfloat16* hb,
                                                             int* status) {
   __shared__ float red[4];
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int b = (int)(row / C), t = (int)(row % C);
   int tok = tokens[(long long)b * ld_tok + t];
@@ -98,6 +100,8 @@ __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __
                                                                   const float* y,
                                                                   const float* alpha, int d) {
   __shared__ float red[4];
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int nch = d / 8;
   float yv[kRowMaxChunks][8];
@@ -155,6 +159,8 @@ enum BoundaryMode : int {
 __global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_bfloat16* hb,
                                                                float* x32, int d, int mode) {
   __shared__ float red[4];
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int nch = d / 8;
   if (mode == BND_SAVE_X) {
@@ -220,6 +226,8 @@ __global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_
 __global__ void kv_write_kernel(const __nv_bfloat16* k_cur, const __nv_bfloat16* v_cur,
                                 __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int C, int P0,
                                 int S, int t_first, int n_kv, int dh) {
+  pdl_wait();
+  pdl_trigger();
   const int t = t_first + blockIdx.x, b = blockIdx.y;
   const int slot = (P0 + t) % S;
   const int cpr = dh / 8;
@@ -236,6 +244,8 @@ __global__ void kv_write_kernel(const __nv_bfloat16* k_cur, const __nv_bfloat16*
 // (P0 + t) * base^(-2i/dh); the angle is formed and reduced mod 2 pi in fp64
 // so long contexts keep full fp32 accuracy.
 __global__ void rope_table_kernel(float2* tab, int C, int P0, int dh, double base) {
+  pdl_wait();
+  pdl_trigger();
   const int half = dh / 2;
   const long long n = (long long)C * half;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
@@ -255,6 +265,8 @@ __global__ void rope_table_kernel(float2* tab, int C, int P0, int dh, double bas
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V, int32_t* next) {
   __shared__ float bv[32];
   __shared__ int bi[32];
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const float* z = logits + row * V;
   float best = -INFINITY;
