@@ -36,10 +36,13 @@ using namespace dory;
 namespace {
 
 constexpr int kGemmBN = 256;
+constexpr int kSwapBN = 64;         // activation rows per tile of the swapped GEMM
+constexpr int kSwapMaxM = 128;      // batched decode through the swapped GEMM up to this
+constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 
 struct WsLayout {
-  size_t status, h32, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, gy, dec_o, dec_ml,
-      total;
+  size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, gy, dec_o,
+      dec_ml, dec_cnt, parts, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -56,6 +59,7 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   const size_t hq = (size_t)c.n_q * c.head_dim, hk = (size_t)c.n_kv * c.head_dim;
   L.status = take(256);
   L.h32 = take(M * c.d * 4);
+  L.h32b = take((size_t)max_batch * c.d * 4);   // decode: second hidden-state buffer
   L.x32 = take(M * c.d * 4);
   L.hb = take(M * c.d * 2);
   L.y32 = take(M * c.d * 4);
@@ -74,6 +78,13 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   // split-KV decode attention partials
   L.dec_o = take((size_t)max_batch * c.n_q * kDecMaxSplits * c.head_dim * 4);
   L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
+  L.dec_cnt = take((size_t)max_batch * c.n_kv * 4);   // split tickets, zero between launches
+  // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
+  if (max_batch > kGemvMaxM) {
+    const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
+    const size_t w2 = wide > (size_t)c.d ? wide : (size_t)c.d;
+    L.parts = take((size_t)kSwapMaxParts * rows * w2 * 4);
+  }
   L.total = off;
   return L;
 }
@@ -191,10 +202,13 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
   const int cols = EPI == EPI_SWIGLU ? args.N / 2 : args.N;
   const int bn_out = EPI == EPI_SWIGLU ? BN / 2 : BN;
   args.tiles_n = (cols + bn_out - 1) / bn_out;
-  const int tiles = args.tiles_m * args.tiles_n;
+  if (EPI != EPI_PARTS) args.k_splits = 1;
+  if (args.k_splits < 1) return DORY_EINVAL;
+  const int tiles = args.tiles_m * args.tiles_n * args.k_splits;
   if (tiles == 0) return DORY_OK;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(192), Cf::SMEM, st, ta, tb, args) ==
+  return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM, st, ta, tb,
+                  args) ==
                  cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
@@ -217,48 +231,93 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
              : DORY_ECUDA;
 }
 
-// Y[M, N] (row stride ldy) = scale * X[M, K] . W[N, K]^T for M <= kGemvMaxM, or,
-// with pair_off > 0, m_out[M, N] = (X W[n]^T) * SiLU(X W[n + pair_off]^T).
-template <int MM, int J, bool SW>
-cudaError_t gemv_go(int grid, cudaStream_t st, const __nv_bfloat16* X, int ldx, int M,
-                    const __nv_bfloat16* W, int N, int K, int S, float* Y, int ldy,
-                    const float* scale, int pair_off, __nv_bfloat16* m_out, int ldm) {
-  return launch_k(gemv_kernel<MM, J, SW>, dim3(grid), dim3(kGemvThreads), 0, st, X, ldx, M, W, N,
-                  K, S, Y, ldy, scale, pair_off, m_out, ldm);
+// Few-row projection (M <= kGemvMaxM), see gemv.cuh.  The caller fills
+// X/ldx (or, for the fused nGPT step, h_in/y_in/alpha/h_out with K = d), W, N,
+// K, M and either Y/ldy/col_scale or (SwiGLU) pair_off/m_out/ldm.
+template <int MM, int J, bool SW, bool PRE>
+cudaError_t gemv_go(const GemvArgs& a, int grid, cudaStream_t st) {
+  const size_t smem = PRE ? (size_t)a.M * a.K * 2 : 0;
+  static bool attr = false;
+  if (PRE && !attr) {
+    if (cudaFuncSetAttribute(gemv_kernel<MM, J, SW, PRE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemvMaxM * kGemvPreMaxD * 2) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    attr = true;
+  }
+  return launch_k(gemv_kernel<MM, J, SW, PRE>, dim3(grid), dim3(kGemvThreads), smem, st, a);
 }
 
-template <int MM, bool SW>
-cudaError_t gemv_j(int J, int grid, cudaStream_t st, const __nv_bfloat16* X, int ldx, int M,
-                   const __nv_bfloat16* W, int N, int K, int S, float* Y, int ldy,
-                   const float* scale, int pair_off, __nv_bfloat16* m_out, int ldm) {
-  if (J <= 2) return gemv_go<MM, 2, SW>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
-  if (J <= 4) return gemv_go<MM, 4, SW>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+template <int MM, bool SW, bool PRE>
+cudaError_t gemv_j(const GemvArgs& a, int J, int grid, cudaStream_t st) {
+  if (J <= 2) return gemv_go<MM, 2, SW, PRE>(a, grid, st);
+  if (J <= 4) return gemv_go<MM, 4, SW, PRE>(a, grid, st);
   if (SW) return cudaErrorInvalidValue;
-  if (J <= 6) return gemv_go<MM, 6, false>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
-  return gemv_go<MM, 8, false>(grid, st, X, ldx, M, W, N, K, S, Y, ldy, scale, pair_off, m_out, ldm);
+  if (J <= 6) return gemv_go<MM, 6, false, PRE>(a, grid, st);
+  return gemv_go<MM, 8, false, PRE>(a, grid, st);
 }
 
-int launch_gemv(const __nv_bfloat16* X, int ldx, int M, const void* W, int N, int K, float* Y,
-                int ldy, const float* scale, cudaStream_t st, int pair_off = 0,
-                __nv_bfloat16* m_out = nullptr, int ldm = 0) {
-  const bool sw = pair_off > 0;
+int launch_gemv(GemvArgs a, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr;
+  const bool pre = a.h_in != nullptr;
   const int jmax = sw ? 4 : 8;
-  const int kc = (K + 255) / 256;                  // 256-element chunks per row
+  const int kc = (a.K + 255) / 256;                // 256-element chunks per row
   int S = 1;
   while ((kc + S - 1) / S > jmax && S < kGemvWarps) S *= 2;
   const int J = (kc + S - 1) / S;
-  if (J > jmax || M > kGemvMaxM) return DORY_EUNSUPPORTED;
-  const int rows_per_cta = kGemvWarps / S;
-  const int grid = (N + rows_per_cta - 1) / rows_per_cta;
-  const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(W);
+  if (J > jmax || a.M > kGemvMaxM || a.M <= 0 || a.K % 8) return DORY_EUNSUPPORTED;
+  if (pre && a.K > kGemvPreMaxD) return DORY_EUNSUPPORTED;
+  a.S = S;
+  const int fpi = kGemvWarps / S;
+  a.n_iters = (a.N + fpi - 1) / fpi;
+  const int grid = a.n_iters < 3 * num_sms() ? a.n_iters : 3 * num_sms();
   cudaError_t e;
-  if (M <= 4)
-    e = sw ? gemv_j<4, true>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, pair_off, m_out, ldm)
-           : gemv_j<4, false>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, 0, m_out, ldm);
+  if (a.M <= 4)
+    e = sw ? (pre ? gemv_j<4, true, true>(a, J, grid, st) : gemv_j<4, true, false>(a, J, grid, st))
+           : (pre ? gemv_j<4, false, true>(a, J, grid, st) : gemv_j<4, false, false>(a, J, grid, st));
   else
-    e = sw ? gemv_j<16, true>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, pair_off, m_out, ldm)
-           : gemv_j<16, false>(J, grid, st, X, ldx, M, w, N, K, S, Y, ldy, scale, 0, m_out, ldm);
+    e = sw ? (pre ? gemv_j<16, true, true>(a, J, grid, st) : gemv_j<16, true, false>(a, J, grid, st))
+           : (pre ? gemv_j<16, false, true>(a, J, grid, st)
+                  : gemv_j<16, false, false>(a, J, grid, st));
   return e == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
+// One-token attention of the forward pass (fused split merge, gate and KV
+// write), see attn_decode_kernel.  Fills chunk / n_splits.
+template <int DH, bool RAW>
+int launch_dec_attn(DecAttnArgs a, int B, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_decode_kernel<DH, RAW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DecCfg<DH>::SMEM) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  const int lo = a.window > 0 ? (a.P0 - a.window + 1 > 0 ? a.P0 - a.window + 1 : 0) : 0;
+  const int n_cache = a.P0 - lo;                      // cached keys (the new token is extra)
+  // enough CTAs to fill the SMs twice, but at least kDecMinTiles tiles per
+  // split so that the prologue and merge of a CTA stay small against its keys
+  int splits = (2 * num_sms() + B * a.n_kv - 1) / (B * a.n_kv);
+  if (splits > kDecMaxSplits) splits = kDecMaxSplits;
+  if (splits < 1) splits = 1;
+  int chunk = (n_cache + splits - 1) / splits;
+  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+  if (chunk < kDecMinTiles * kDecTile) chunk = kDecMinTiles * kDecTile;
+  a.chunk = chunk;
+  a.n_splits = n_cache > 0 ? (n_cache + chunk - 1) / chunk : 1;
+  return launch_k(attn_decode_kernel<DH, RAW>, dim3(a.n_splits, a.n_kv, B), dim3(128),
+                  DecCfg<DH>::SMEM, st, a) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
+template <bool RAW>
+int dec_attn(const DecAttnArgs& a, int B, int head_dim, cudaStream_t st) {
+  if (head_dim == 32) return launch_dec_attn<32, RAW>(a, B, st);
+  if (head_dim == 64) return launch_dec_attn<64, RAW>(a, B, st);
+  if (head_dim == 128) return launch_dec_attn<128, RAW>(a, B, st);
+  return DORY_EUNSUPPORTED;
 }
 
 // Split-KV decode attention: partial kernel + combine.
@@ -305,6 +364,7 @@ struct dory_model {
   int len = 0;
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
+  int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
   int launches = 0;
   // optional per-launch event timing
   bool prof_on = false;
@@ -344,23 +404,266 @@ int pe(dory_model* m, cudaStream_t st, int rc = DORY_OK) {
   return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
-int ngpt_update(dory_model* m, int M, const float* alpha, cudaStream_t st) {
-  return launch_k(ngpt_update_kernel, dim3(M), dim3(kRowThreads), 0, st, wsp<float>(m, m->L.h32),
-                  wsp<__nv_bfloat16>(m, m->L.hb), (const float*)wsp<float>(m, m->L.y32), alpha,
-                  m->cfg.d) == cudaSuccess
-             ? DORY_OK
-             : DORY_ECUDA;
+// Hidden-state bookkeeping of one forward step.  The fp32 hidden state of the
+// step's rows lives in one of two workspace buffers (h32 / h32b); `pend`,
+// when set, is the residual rate of an nGPT step that is still owed: the true
+// hidden state is N(h + pend * (N(y32) - h)).  The decode path leaves that
+// step to the next kernel (a projection forms it in its prologue, a boundary
+// kernel before its own transform); the prefill path applies it at once.
+struct StepState {
+  int hsel = 0;
+  const float* pend = nullptr;
+};
+
+float* hbuf(dory_model* m, int sel) { return wsp<float>(m, sel ? m->L.h32b : m->L.h32); }
+
+int ngpt_update(dory_model* m, int M, float* h, const float* alpha, cudaStream_t st,
+                const float* y = nullptr, int n_parts = 1, long long part_stride = 0) {
+  pb(m, DORY_K_NGPT_UPDATE, st);
+  return pe(m, st,
+            launch_k(ngpt_update_kernel, dim3(M), dim3(kRowThreads), 0, st, h,
+                     wsp<__nv_bfloat16>(m, m->L.hb),
+                     y ? y : (const float*)wsp<float>(m, m->L.y32), alpha, m->cfg.d, n_parts,
+                     part_stride) == cudaSuccess
+                ? DORY_OK
+                : DORY_ECUDA);
 }
 
+// Applies an owed nGPT step in place (h and its bf16 copy hb).
+int flush_pending(dory_model* m, StepState& s, int M, cudaStream_t st) {
+  if (!s.pend) return DORY_OK;
+  const float* al = s.pend;
+  s.pend = nullptr;
+  return ngpt_update(m, M, hbuf(m, s.hsel), al, st);
+}
+
+// Cache block of (layer, slice): K (which = 0) or V (which = 1).
+__nv_bfloat16* kv_block(dory_model* m, int l, int slice, int which) {
+  return reinterpret_cast<__nv_bfloat16*>(
+      m->kv + kv_offset(m->cfg, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, slice, which));
+}
+
+float attn_scale_log2(const dory_config& c) {
+  const float scale = c.softmax_scale > 0.f ? c.softmax_scale : sqrtf((float)c.head_dim);
+  return scale * 1.4426950408889634f;
+}
+
+// One layer for one new token per sequence (decode, B <= kGemvMaxM rows):
+// five kernels.  QKV + gate GEMV (owed nGPT step fused) -> attention (RoPE /
+// q-k norm in its prologue, split merge, gate and KV write fused) -> output
+// GEMV -> up + gate GEMV with SwiGLU (attention nGPT step fused) -> down GEMV
+// (its nGPT step is owed to the next kernel).
+int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0, StepState& s,
+                     cudaStream_t st) {
+  const dory_config& c = m->cfg;
+  const dory_layer_weights& w = m->layers[l];
+  const int M = B;
+  const int hq = c.n_q * c.head_dim;
+  const int nqkvg = (2 * c.n_q + 2 * c.n_kv) * c.head_dim;
+  const bool full = layer_full(c, l);
+  const bool fuse = c.d <= kGemvPreMaxD;
+  float* y32 = wsp<float>(m, m->L.y32);
+  float* gy = wsp<float>(m, m->L.gy);
+  __nv_bfloat16* att = wsp<__nv_bfloat16>(m, m->L.att);
+  __nv_bfloat16* mo = wsp<__nv_bfloat16>(m, m->L.m);
+  if (!fuse) DORY_TRY(flush_pending(m, s, M, st));
+
+  auto with_pending = [&](GemvArgs& g) {
+    if (s.pend) {
+      g.h_in = hbuf(m, s.hsel);
+      g.y_in = y32;
+      g.alpha = s.pend;
+      g.h_out = hbuf(m, s.hsel ^ 1);
+      s.hsel ^= 1;
+      s.pend = nullptr;
+    } else {
+      g.X = wsp<__nv_bfloat16>(m, m->L.hb);
+      g.ldx = c.d;
+    }
+  };
+
+  // QKV + gate projection -> fp32 rows [q | k | v | g]
+  GemvArgs gq{};
+  gq.M = M;
+  gq.W = static_cast<const __nv_bfloat16*>(w.w_qkvg);
+  gq.N = nqkvg;
+  gq.K = c.d;
+  gq.Y = gy;
+  gq.ldy = nqkvg;
+  with_pending(gq);
+  pb(m, DORY_K_QKVG_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemv(gq, st)));
+
+  // attention over the cached keys + the new token, KV write fused
+  DecAttnArgs da{};
+  da.y = gy;
+  da.ldy = nqkvg;
+  da.n_parts = 1;
+  da.part_stride = 0;
+  da.s_qk = w.s_qk;
+  da.rope = c.rope ? wsp<float2>(m, full ? m->L.rope_full : m->L.rope_swa) : nullptr;
+  da.k_cache = kv_block(m, l, slice, 0);
+  da.v_cache = kv_block(m, l, slice, 1);
+  da.store = store ? 1 : 0;
+  da.P0 = P0;
+  da.S = slots_of(c, l, m->max_ctx);
+  da.n_q = c.n_q;
+  da.n_kv = c.n_kv;
+  da.window = full ? 0 : c.window;
+  da.scale_log2 = attn_scale_log2(c);
+  da.part_o = wsp<float>(m, m->L.dec_o);
+  da.part_ml = wsp<float>(m, m->L.dec_ml);
+  da.counter = wsp<int>(m, m->L.dec_cnt);
+  da.out = att;
+  pb(m, DORY_K_ATTENTION, st);
+  DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
+
+  // output projection; its nGPT step is owed
+  GemvArgs go{};
+  go.M = M;
+  go.X = att;
+  go.ldx = hq;
+  go.W = static_cast<const __nv_bfloat16*>(w.w_o);
+  go.N = c.d;
+  go.K = hq;
+  go.Y = y32;
+  go.ldy = c.d;
+  pb(m, DORY_K_O_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemv(go, st)));
+  s.pend = w.alpha_attn;
+  if (!fuse) DORY_TRY(flush_pending(m, s, M, st));
+
+  // up + gate projection with SwiGLU
+  GemvArgs gu{};
+  gu.M = M;
+  gu.W = static_cast<const __nv_bfloat16*>(w.w_upgate);
+  gu.N = c.ffn;
+  gu.K = c.d;
+  gu.pair_off = c.ffn;
+  gu.m_out = mo;
+  gu.ldm = c.ffn;
+  with_pending(gu);
+  pb(m, DORY_K_UPGATE_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemv(gu, st)));
+
+  // down projection; its nGPT step is owed
+  GemvArgs gd{};
+  gd.M = M;
+  gd.X = mo;
+  gd.ldx = c.ffn;
+  gd.W = static_cast<const __nv_bfloat16*>(w.w_down);
+  gd.N = c.d;
+  gd.K = c.ffn;
+  gd.Y = y32;
+  gd.ldy = c.d;
+  pb(m, DORY_K_DOWN_GEMM, st);
+  DORY_TRY(pe(m, st, launch_gemv(gd, st)));
+  s.pend = w.alpha_mlp;
+  return DORY_OK;
+}
+
+// Swapped split-K projection for a decode batch: parts[s][row][n] (fp32) =
+// X[row, K range s] . W[n, K range s]^T; returns the number of splits.
+int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int rows,
+              int K, float* parts, int& n_parts, cudaStream_t st) {
+  GemmArgs g{};
+  g.M = n_out;
+  g.N = rows;
+  g.K = K;
+  g.status = wsp<int>(m, m->L.status);
+  g.out = parts;
+  g.ldo = n_out;
+  g.part_stride = (long long)rows * n_out;
+  const int units = ((n_out + 127) / 128) * ((rows + kSwapBN - 1) / kSwapBN);
+  const int kb = (K + 63) / 64;
+  int sp = (num_sms() + units - 1) / units;
+  if (sp > kSwapMaxParts) sp = kSwapMaxParts;
+  if (sp > kb / 2) sp = kb / 2;
+  if (sp < 1) sp = 1;
+  g.k_splits = sp;
+  n_parts = sp;
+  return launch_gemm<kSwapBN, EPI_PARTS>(tw, tx, g, st);
+}
+
+// One layer for one new token per sequence with more sequences than the GEMV
+// handles (kGemvMaxM < B <= kSwapMaxM): weights are the 128-row operand of
+// the tensor-core GEMM, the batch the 64-row one, K split over the SMs; the
+// attention, nGPT-step and SwiGLU kernels add the partial sums.
+int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0,
+                      const CUtensorMap& tx_hb, const CUtensorMap& tx_att,
+                      const CUtensorMap& tx_m, StepState& s, cudaStream_t st) {
+  const dory_config& c = m->cfg;
+  const dory_layer_weights& w = m->layers[l];
+  const int hq = c.n_q * c.head_dim;
+  const int nqkvg = (2 * c.n_q + 2 * c.n_kv) * c.head_dim;
+  const bool full = layer_full(c, l);
+  DORY_TRY(flush_pending(m, s, B, st));
+  float* h = hbuf(m, s.hsel);
+  float* parts = wsp<float>(m, m->L.parts);
+  __nv_bfloat16* att = wsp<__nv_bfloat16>(m, m->L.att);
+  __nv_bfloat16* mo = wsp<__nv_bfloat16>(m, m->L.m);
+  int np = 1;
+
+  pb(m, DORY_K_QKVG_GEMM, st);
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_qkvg[l], tx_hb, nqkvg, B, c.d, parts, np, st)));
+
+  DecAttnArgs da{};
+  da.y = parts;
+  da.ldy = nqkvg;
+  da.n_parts = np;
+  da.part_stride = (long long)B * nqkvg;
+  da.s_qk = w.s_qk;
+  da.rope = c.rope ? wsp<float2>(m, full ? m->L.rope_full : m->L.rope_swa) : nullptr;
+  da.k_cache = kv_block(m, l, slice, 0);
+  da.v_cache = kv_block(m, l, slice, 1);
+  da.store = store ? 1 : 0;
+  da.P0 = P0;
+  da.S = slots_of(c, l, m->max_ctx);
+  da.n_q = c.n_q;
+  da.n_kv = c.n_kv;
+  da.window = full ? 0 : c.window;
+  da.scale_log2 = attn_scale_log2(c);
+  da.part_o = wsp<float>(m, m->L.dec_o);
+  da.part_ml = wsp<float>(m, m->L.dec_ml);
+  da.counter = wsp<int>(m, m->L.dec_cnt);
+  da.out = att;
+  pb(m, DORY_K_ATTENTION, st);
+  DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
+
+  pb(m, DORY_K_O_GEMM, st);
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_o[l], tx_att, c.d, B, hq, parts, np, st)));
+  DORY_TRY(ngpt_update(m, B, h, w.alpha_attn, st, parts, np, (long long)B * c.d));
+
+  pb(m, DORY_K_UPGATE_GEMM, st);
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_upgate[l], tx_hb, 2 * c.ffn, B, c.d, parts, np, st)));
+  pb(m, DORY_K_UPGATE_GEMM, st);
+  DORY_TRY(pe(m, st,
+              launch_k(swiglu_parts_kernel, dim3((c.ffn + 8 * kRowThreads - 1) / (8 * kRowThreads), B),
+                       dim3(kRowThreads), 0, st, (const float*)parts, c.ffn, np,
+                       (long long)B * 2 * c.ffn, mo) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA));
+
+  pb(m, DORY_K_DOWN_GEMM, st);
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_down[l], tx_m, c.d, B, c.ffn, parts, np, st)));
+  return ngpt_update(m, B, h, w.alpha_mlp, st, parts, np, (long long)B * c.d);
+}
+
+// One layer for C tokens per sequence (prefill chunks; also decode with more
+// rows than the GEMV handles): tensor-core GEMMs with fused epilogues, or the
+// GEMV for few rows; prefill or one-token attention; nGPT steps applied
+// at once.
 int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
               const CUtensorMap& tm_hb, const CUtensorMap& tm_att, const CUtensorMap& tm_m,
-              cudaStream_t st) {
+              StepState& s, cudaStream_t st) {
   const dory_config& c = m->cfg;
   const dory_layer_weights& w = m->layers[l];
   const int M = B * C;
   const int hq = c.n_q * c.head_dim;
   int* status = wsp<int>(m, m->L.status);
   const bool full = layer_full(c, l);
+  DORY_TRY(flush_pending(m, s, M, st));
+  float* h = hbuf(m, s.hsel);
 
   // QKV + gate projection with RoPE / q-k normalisation / sigmoid fused
   GemmArgs ga{};
@@ -382,8 +685,17 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   __nv_bfloat16* hb = wsp<__nv_bfloat16>(m, m->L.hb);
   float* gy = wsp<float>(m, m->L.gy);
   if (few) {
+    GemvArgs g{};
+    g.M = M;
+    g.X = hb;
+    g.ldx = c.d;
+    g.W = static_cast<const __nv_bfloat16*>(w.w_qkvg);
+    g.N = ga.N;
+    g.K = c.d;
+    g.Y = gy;
+    g.ldy = ga.N;
     pb(m, DORY_K_QKVG_GEMM, st);
-    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_qkvg, ga.N, c.d, gy, ga.N, nullptr, st)));
+    DORY_TRY(pe(m, st, launch_gemv(g, st)));
     pb(m, DORY_K_QKVG_GEMM, st);
     const int nheads = 2 * c.n_q + 2 * c.n_kv;
     const int thr = c.head_dim / 2 > 32 ? c.head_dim / 2 : 32;
@@ -400,64 +712,64 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
 
   // attention over cached + current keys
   const int S = slots_of(c, l, m->max_ctx);
-  const size_t koff = kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, slice, 0);
-  const size_t voff = kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, slice, 1);
-  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(m->kv + koff);
-  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(m->kv + voff);
-  AttnArgs aa{};
-  aa.q = ga.q;
-  aa.k_cur = ga.k;
-  aa.v_cur = ga.v;
-  aa.k_cache = kc;
-  aa.v_cache = vc;
-  aa.gate = ga.g;
-  aa.out = wsp<__nv_bfloat16>(m, m->L.att);
-  aa.C = C;
-  aa.P0 = P0;
-  aa.S = S;
-  aa.n_q = c.n_q;
-  aa.n_kv = c.n_kv;
-  aa.window = full ? 0 : c.window;
-  const float scale = c.softmax_scale > 0.f ? c.softmax_scale : sqrtf((float)c.head_dim);
-  aa.scale_log2 = scale * 1.4426950408889634f;
+  __nv_bfloat16* kc = kv_block(m, l, slice, 0);
+  __nv_bfloat16* vc = kv_block(m, l, slice, 1);
+  __nv_bfloat16* att = wsp<__nv_bfloat16>(m, m->L.att);
   pb(m, DORY_K_ATTENTION, st);
-  int arc = DORY_EUNSUPPORTED;
   if (C == 1) {
-    DecodeArgs da{};
-    da.q = aa.q;
-    da.k_cur = aa.k_cur;
-    da.v_cur = aa.v_cur;
-    da.k_cache = aa.k_cache;
-    da.v_cache = aa.v_cache;
+    // one token per sequence: split-key kernel, KV write fused
+    DecAttnArgs da{};
+    da.q = ga.q;
+    da.k_cur = ga.k;
+    da.v_cur = ga.v;
+    da.gate = ga.g;
+    da.k_cache = kc;
+    da.v_cache = vc;
+    da.store = store ? 1 : 0;
     da.P0 = P0;
     da.S = S;
     da.n_q = c.n_q;
     da.n_kv = c.n_kv;
-    da.window = aa.window;
-    da.scale_log2 = aa.scale_log2;
+    da.window = full ? 0 : c.window;
+    da.scale_log2 = attn_scale_log2(c);
     da.part_o = wsp<float>(m, m->L.dec_o);
     da.part_ml = wsp<float>(m, m->L.dec_ml);
-    if (c.head_dim == 32) arc = launch_decode_attn<32>(da, B, aa.gate, aa.out, st);
-    if (c.head_dim == 64) arc = launch_decode_attn<64>(da, B, aa.gate, aa.out, st);
-    if (c.head_dim == 128) arc = launch_decode_attn<128>(da, B, aa.gate, aa.out, st);
+    da.counter = wsp<int>(m, m->L.dec_cnt);
+    da.out = att;
+    DORY_TRY(pe(m, st, dec_attn<false>(da, B, c.head_dim, st)));
   } else {
+    AttnArgs aa{};
+    aa.q = ga.q;
+    aa.k_cur = ga.k;
+    aa.v_cur = ga.v;
+    aa.k_cache = kc;
+    aa.v_cache = vc;
+    aa.gate = ga.g;
+    aa.out = att;
+    aa.C = C;
+    aa.P0 = P0;
+    aa.S = S;
+    aa.n_q = c.n_q;
+    aa.n_kv = c.n_kv;
+    aa.window = full ? 0 : c.window;
+    aa.scale_log2 = attn_scale_log2(c);
+    int arc = DORY_EUNSUPPORTED;
     if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
     if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
     if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
-  }
-  DORY_TRY(pe(m, st, arc));
-
-  // KV write: the last min(C, S) positions of the call
-  if (store) {
-    const int t_first = C > S ? C - S : 0;
-    dim3 grid(C - t_first, B);
-    pb(m, DORY_K_KV_WRITE, st);
-    DORY_TRY(pe(m, st,
-                launch_k(kv_write_kernel, grid, dim3(64), 0, st, (const __nv_bfloat16*)ga.k,
-                         (const __nv_bfloat16*)ga.v, kc, vc, C, P0, S, t_first, c.n_kv,
-                         c.head_dim) == cudaSuccess
-                    ? DORY_OK
-                    : DORY_ECUDA));
+    DORY_TRY(pe(m, st, arc));
+    // KV write: the last min(C, S) positions of the call
+    if (store) {
+      const int t_first = C > S ? C - S : 0;
+      dim3 grid(C - t_first, B);
+      pb(m, DORY_K_KV_WRITE, st);
+      DORY_TRY(pe(m, st,
+                  launch_k(kv_write_kernel, grid, dim3(64), 0, st, (const __nv_bfloat16*)ga.k,
+                           (const __nv_bfloat16*)ga.v, kc, vc, C, P0, S, t_first, c.n_kv,
+                           c.head_dim) == cudaSuccess
+                      ? DORY_OK
+                      : DORY_ECUDA));
+    }
   }
 
   // output projection + nGPT step
@@ -469,12 +781,21 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   go.out = wsp<float>(m, m->L.y32);
   go.ldo = c.d;
   pb(m, DORY_K_O_GEMM, st);
-  if (few)
-    DORY_TRY(pe(m, st, launch_gemv(aa.out, hq, M, w.w_o, c.d, hq, go.out, c.d, nullptr, st)));
-  else
+  if (few) {
+    GemvArgs g{};
+    g.M = M;
+    g.X = att;
+    g.ldx = hq;
+    g.W = static_cast<const __nv_bfloat16*>(w.w_o);
+    g.N = c.d;
+    g.K = hq;
+    g.Y = go.out;
+    g.ldy = c.d;
+    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+  } else {
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
-  pb(m, DORY_K_NGPT_UPDATE, st);
-  DORY_TRY(pe(m, st, ngpt_update(m, M, w.alpha_attn, st)));
+  }
+  DORY_TRY(ngpt_update(m, M, h, w.alpha_attn, st));
 
   // SwiGLU MLP + nGPT step
   GemmArgs gu{};
@@ -485,12 +806,20 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gu.status = status;
   gu.m_out = wsp<__nv_bfloat16>(m, m->L.m);
   gu.ldm = c.ffn;
+  pb(m, DORY_K_UPGATE_GEMM, st);
   if (few) {
-    pb(m, DORY_K_UPGATE_GEMM, st);
-    DORY_TRY(pe(m, st, launch_gemv(hb, c.d, M, w.w_upgate, c.ffn, c.d, nullptr, 0, nullptr, st,
-                                   c.ffn, gu.m_out, c.ffn)));
+    GemvArgs g{};
+    g.M = M;
+    g.X = hb;
+    g.ldx = c.d;
+    g.W = static_cast<const __nv_bfloat16*>(w.w_upgate);
+    g.N = c.ffn;
+    g.K = c.d;
+    g.pair_off = c.ffn;
+    g.m_out = gu.m_out;
+    g.ldm = c.ffn;
+    DORY_TRY(pe(m, st, launch_gemv(g, st)));
   } else {
-    pb(m, DORY_K_UPGATE_GEMM, st);
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
   }
   GemmArgs gd{};
@@ -501,26 +830,39 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   gd.out = wsp<float>(m, m->L.y32);
   gd.ldo = c.d;
   pb(m, DORY_K_DOWN_GEMM, st);
-  if (few)
-    DORY_TRY(pe(m, st, launch_gemv(gu.m_out, c.ffn, M, w.w_down, c.d, c.ffn, gd.out, c.d, nullptr,
-                                   st)));
-  else
+  if (few) {
+    GemvArgs g{};
+    g.M = M;
+    g.X = gu.m_out;
+    g.ldx = c.ffn;
+    g.W = static_cast<const __nv_bfloat16*>(w.w_down);
+    g.N = c.d;
+    g.K = c.ffn;
+    g.Y = gd.out;
+    g.ldy = c.d;
+    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+  } else {
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
-  pb(m, DORY_K_NGPT_UPDATE, st);
-  return pe(m, st, ngpt_update(m, M, w.alpha_mlp, st));
+  }
+  return ngpt_update(m, M, h, w.alpha_mlp, st);
 }
 
-int boundary(dory_model* m, int M, int mode, cudaStream_t st) {
+// Loop-boundary kernel on the current hidden buffer; an owed nGPT step is
+// applied first inside the same kernel.
+int boundary(dory_model* m, int M, int mode, StepState& s, cudaStream_t st) {
+  const float* y = s.pend ? wsp<float>(m, m->L.y32) : nullptr;
+  const float* al = s.pend;
+  s.pend = nullptr;
   pb(m, DORY_K_BOUNDARY, st);
   return pe(m, st,
-            launch_k(boundary_kernel, dim3(M), dim3(kRowThreads), 0, st, wsp<float>(m, m->L.h32),
-                     wsp<__nv_bfloat16>(m, m->L.hb), wsp<float>(m, m->L.x32), m->cfg.d, mode) ==
-                    cudaSuccess
+            launch_k(boundary_kernel, dim3(M), dim3(kRowThreads), 0, st, hbuf(m, s.hsel),
+                     wsp<__nv_bfloat16>(m, m->L.hb), wsp<float>(m, m->L.x32), m->cfg.d, mode, y, 1,
+                     (long long)0, al) == cudaSuccess
                 ? DORY_OK
                 : DORY_ECUDA);
 }
 
-// One forward step over B sequences x C tokens at positions P0 .. P0+C-1.
+// One forward step over B sequences x C tokens at positions P0..P0+C-1.
 // Logit rows: if logits != null, rows (b, t) for t >= C - n_logit_rows are
 // written to logits + (b * ld_seq + t_out0 + t - (C - n_logit_rows)) * V.
 int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int k,
@@ -529,57 +871,57 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   const int M = B * C;
   const int P0 = m->len;
   int* status = wsp<int>(m, m->L.status);
+  const bool decode = C == 1 && M <= kGemvMaxM;
+  const bool batched = C == 1 && M > kGemvMaxM && M <= kSwapMaxM;
 
   CUtensorMap tm_hb, tm_att, tm_m;
   const int hq = c.n_q * c.head_dim;
-  if (!encode_bf16(&tm_hb, m->ws + m->L.hb, M, c.d, c.d, 128) ||
-      !encode_bf16(&tm_att, m->ws + m->L.att, M, hq, hq, 128) ||
-      !encode_bf16(&tm_m, m->ws + m->L.m, M, c.ffn, c.ffn, 128))
+  const uint32_t box = batched ? kSwapBN / 2 : 128;   // activation rows per TMA box
+  if (!encode_bf16(&tm_hb, m->ws + m->L.hb, M, c.d, c.d, box) ||
+      !encode_bf16(&tm_att, m->ws + m->L.att, M, hq, hq, box) ||
+      !encode_bf16(&tm_m, m->ws + m->L.m, M, c.ffn, c.ffn, box))
     return DORY_ECUDA;
 
   if (c.rope) {
-    const int n = C * (c.head_dim / 2);
+    const int n = 2 * C * (c.head_dim / 2);
     const int blocks = (n + 255) / 256;
     pb(m, DORY_K_ROPE, st);
     DORY_TRY(pe(m, st,
                 launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st,
-                         wsp<float2>(m, m->L.rope_swa), C, P0, c.head_dim,
-                         (double)c.rope_base_swa) == cudaSuccess
-                    ? DORY_OK
-                    : DORY_ECUDA));
-    pb(m, DORY_K_ROPE, st);
-    DORY_TRY(pe(m, st,
-                launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st,
-                         wsp<float2>(m, m->L.rope_full), C, P0, c.head_dim,
-                         (double)c.rope_base_full) == cudaSuccess
+                         wsp<float2>(m, m->L.rope_swa), wsp<float2>(m, m->L.rope_full), C, P0,
+                         c.head_dim, (double)c.rope_base_swa, (double)c.rope_base_full) ==
+                        cudaSuccess
                     ? DORY_OK
                     : DORY_ECUDA));
   }
+  StepState s;
   pb(m, DORY_K_EMBED, st);
   DORY_TRY(pe(m, st,
               launch_k(embed_kernel, dim3(M), dim3(kRowThreads), 0, st, tokens, ld_tok, C,
                        reinterpret_cast<const __nv_bfloat16*>(m->embed_in), c.vocab, c.d,
-                       wsp<float>(m, m->L.h32), wsp<__nv_bfloat16>(m, m->L.hb), status) ==
-                      cudaSuccess
+                       hbuf(m, s.hsel), wsp<__nv_bfloat16>(m, m->L.hb), status) == cudaSuccess
                   ? DORY_OK
                   : DORY_ECUDA));
 
-  for (int l = 0; l < c.n_in; ++l)
-    DORY_TRY(run_layer(m, l, 0, true, B, C, P0, tm_hb, tm_att, tm_m, st));
+  auto layer = [&](int l, int slice, bool store) {
+    if (decode) return run_layer_decode(m, l, slice, store, B, P0, s, st);
+    if (batched) return run_layer_batched(m, l, slice, store, B, P0, tm_hb, tm_att, tm_m, s, st);
+    return run_layer(m, l, slice, store, B, C, P0, tm_hb, tm_att, tm_m, s, st);
+  };
+  for (int l = 0; l < c.n_in; ++l) DORY_TRY(layer(l, 0, true));
   if (c.n_rec > 0) {
-    DORY_TRY(boundary(m, M, BND_SAVE_X, st));
+    const bool per_loop = m->cache_mode == DORY_CACHE_PER_LOOP;
     for (int i = 1; i <= k; ++i) {
-      DORY_TRY(boundary(m, M, i == 1 ? BND_ENTER_FIRST : BND_ENTER_NEXT, st));
-      const bool per_loop = m->cache_mode == DORY_CACHE_PER_LOOP;
+      DORY_TRY(boundary(m, M, i == 1 ? BND_SAVE_ENTER : BND_ENTER_NEXT, s, st));
       const int slice = per_loop ? i - 1 : 0;
       const bool store = per_loop || i == k;
-      for (int l = c.n_in; l < c.n_in + c.n_rec; ++l)
-        DORY_TRY(run_layer(m, l, slice, store, B, C, P0, tm_hb, tm_att, tm_m, st));
+      for (int l = c.n_in; l < c.n_in + c.n_rec; ++l) DORY_TRY(layer(l, slice, store));
     }
-    DORY_TRY(boundary(m, M, BND_EXIT, st));
+    DORY_TRY(boundary(m, M, BND_EXIT, s, st));
   }
-  for (int l = c.n_in + c.n_rec; l < n_layers(c); ++l)
-    DORY_TRY(run_layer(m, l, 0, true, B, C, P0, tm_hb, tm_att, tm_m, st));
+  for (int l = c.n_in + c.n_rec; l < n_layers(c); ++l) DORY_TRY(layer(l, 0, true));
+  DORY_TRY(flush_pending(m, s, M, st));
+  m->hsel_last = s.hsel;
 
   if (logits && n_logit_rows > 0) {
     // LM head on the selected rows: per sequence, rows C - n .. C-1 of hb
@@ -591,11 +933,18 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     gl.col_scale = m->s_z;
     gl.ldo = c.vocab;
     if (n_logit_rows == 1 && B <= kGemvMaxM) {
+      GemvArgs g{};
+      g.M = B;
+      g.X = wsp<__nv_bfloat16>(m, m->L.hb) + (size_t)(C - 1) * c.d;
+      g.ldx = C * c.d;
+      g.W = static_cast<const __nv_bfloat16*>(m->embed_out);
+      g.N = c.vocab;
+      g.K = c.d;
+      g.Y = logits + (long long)t_out0 * c.vocab;
+      g.ldy = (int)(ld_seq * c.vocab);
+      g.col_scale = m->s_z;
       pb(m, DORY_K_LM_HEAD, st);
-      DORY_TRY(pe(m, st, launch_gemv(wsp<__nv_bfloat16>(m, m->L.hb) + (size_t)(C - 1) * c.d,
-                                     C * c.d, B, m->embed_out, c.vocab, c.d,
-                                     logits + (long long)t_out0 * c.vocab,
-                                     (int)(ld_seq * c.vocab), m->s_z, st)));
+      DORY_TRY(pe(m, st, launch_gemv(g, st)));
     } else if (n_logit_rows == 1) {
       // one row per sequence: a strided view of hb (row stride C * d)
       CUtensorMap tm_last;
@@ -718,7 +1067,13 @@ int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes, i
   m->len = 0;
   m->batch = 0;
   m->last_rows = 0;
-  if (cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess) return DORY_ECUDA;
+  m->hsel_last = 0;
+  // status word and split tickets start at zero (the tickets return to zero
+  // after every launch that uses them)
+  if (cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
+      cudaMemsetAsync(m->ws + m->L.dec_cnt, 0, (size_t)max_batch * c.n_kv * 4, 0) != cudaSuccess ||
+      cudaStreamSynchronize(0) != cudaSuccess)
+    return DORY_ECUDA;
   return DORY_OK;
 }
 
@@ -872,7 +1227,8 @@ int dory_debug_hidden(dory_t* m, float* dst, int max_rows, void* stream) {
   if (!m->bound) return DORY_EUNBOUND;
   const int rows = m->last_rows < max_rows ? m->last_rows : max_rows;
   if (rows <= 0) return DORY_EINVAL;
-  return cudaMemcpyAsync(dst, m->ws + m->L.h32, (size_t)rows * m->cfg.d * 4,
+  return cudaMemcpyAsync(dst, m->ws + (m->hsel_last ? m->L.h32b : m->L.h32),
+                         (size_t)rows * m->cfg.d * 4,
                          cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
@@ -908,7 +1264,7 @@ int dory_debug_gemm(const void* A, const void* B, float* C, int M, int N, int K,
 size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim) {
   if (B <= 0 || n_q <= 0 || head_dim <= 0) return 0;
   return align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4) +
-         align256((size_t)B * n_q * kDecMaxSplits * 2 * 4);
+         align256((size_t)B * n_q * kDecMaxSplits * 2 * 4) + align256((size_t)B * n_q * 4);
 }
 
 int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, const void* k_cache,
@@ -939,25 +1295,30 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
   a.scale_log2 = (scale > 0.f ? scale : sqrtf((float)head_dim)) * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (C == 1) {
-    DecodeArgs da{};
+    // the forward pass's one-token kernel (ready inputs, no KV write)
+    DecAttnArgs da{};
     da.q = a.q;
     da.k_cur = a.k_cur;
     da.v_cur = a.v_cur;
-    da.k_cache = a.k_cache;
-    da.v_cache = a.v_cache;
+    da.gate = a.gate;
+    da.k_cache = const_cast<__nv_bfloat16*>(a.k_cache);
+    da.v_cache = const_cast<__nv_bfloat16*>(a.v_cache);
+    da.store = 0;
     da.P0 = P0;
     da.S = a.S;
     da.n_q = n_q;
     da.n_kv = n_kv;
     da.window = a.window;
     da.scale_log2 = a.scale_log2;
-    da.part_o = static_cast<float*>(scratch);
-    da.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
-                                          align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4));
-    if (head_dim == 32) return launch_decode_attn<32>(da, B, a.gate, a.out, st);
-    if (head_dim == 64) return launch_decode_attn<64>(da, B, a.gate, a.out, st);
-    if (head_dim == 128) return launch_decode_attn<128>(da, B, a.gate, a.out, st);
-    return DORY_EUNSUPPORTED;
+    uint8_t* sc = static_cast<uint8_t*>(scratch);
+    const size_t o_bytes = align256((size_t)B * n_q * kDecMaxSplits * head_dim * 4);
+    const size_t ml_bytes = align256((size_t)B * n_q * kDecMaxSplits * 2 * 4);
+    da.part_o = reinterpret_cast<float*>(sc);
+    da.part_ml = reinterpret_cast<float*>(sc + o_bytes);
+    da.counter = reinterpret_cast<int*>(sc + o_bytes + ml_bytes);
+    da.out = a.out;
+    if (cudaMemsetAsync(da.counter, 0, (size_t)B * n_kv * 4, st) != cudaSuccess) return DORY_ECUDA;
+    return dec_attn<false>(da, B, head_dim, st);
   }
   if (head_dim == 32) return launch_attn<32>(a, B, st);
   if (head_dim == 64) return launch_attn<64>(a, B, st);

@@ -5,13 +5,15 @@
 //   C[m, n] = sum_k A[m, k] * B[n, k]      A: activations [M, K] bf16
 //                                          B: weights     [N, K] bf16
 //
-// Persistent, warp-specialised, one CTA per SM (192 threads):
+// Persistent, warp-specialised, one CTA per SM (320 threads):
 //   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage,
 //               128-byte swizzle, STAGES-deep ring of shared-memory buffers;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16 into
 //               one of two TMEM accumulators (2 x BN fp32 columns);
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32 (w % 4) .. +31, i.e. tile rows), fused math, stores.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32 (w % 4) .. +31, i.e. tile rows; warps 2..5 take the
+//               first half of the tile's columns, warps 6..9 the second),
+//               fused math, stores.
 // The epilogue of tile i overlaps the MMAs of tile i + 1.
 //
 // Epilogues (projection names from "Dory1.0-4B: A Looped Normalized-GPT",
@@ -23,12 +25,18 @@
 //               as bf16 in head-major rows.
 //   EPI_SWIGLU  B tile = 64/128 rows of W_up and the same rows of W_sl; the
 //               epilogue forms m = u * SiLU(v) and stores m as bf16.
+//   EPI_PARTS   swapped operands for few activation rows (decode batches):
+//               A = 128 weight rows, B = BN activation rows, and K split into
+//               k_splits ranges so that even a 2048-wide projection spreads
+//               over the SMs; each (weight tile, split) stores its fp32
+//               partial sum transposed, out[split][m][n] (row = activation);
+//               the consumers add the partials.
 #pragma once
 #include "ptx.cuh"
 
 namespace dory {
 
-enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2 };
+enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2, EPI_PARTS = 3 };
 
 struct GemmArgs {
   int M, N, K;          // N: output columns of the GEMM (for SWIGLU: 2 * ffn)
@@ -48,6 +56,10 @@ struct GemmArgs {
   // EPI_SWIGLU
   __nv_bfloat16* m_out;
   int ldm;
+  // EPI_PARTS: M = weight rows (N of the projection), N = activation rows,
+  // out[split * part_stride + n * ldo + m]
+  int k_splits;
+  long long part_stride;
 };
 
 template <int BN>
@@ -75,10 +87,11 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
 
 // ------------------------------------------------------------- epilogues
 template <int BN>
-__device__ __forceinline__ void epi_f32(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+__device__ __forceinline__ void epi_f32(const GemmArgs& a, uint32_t tacc, int row, int n0,
+                                        int c_lo, int c_hi) {
   const bool row_ok = row < a.M;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 16) {
+  for (int c = c_lo; c < c_hi; c += 16) {
     if (n0 + c >= a.N) break;                       // uniform across the warp
     float v[16];
     tmem_ld16(tacc + c, v);
@@ -101,11 +114,12 @@ __device__ __forceinline__ void epi_f32(const GemmArgs& a, uint32_t tacc, int ro
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int row, int tn) {
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int row, int tn,
+                                           int c_lo, int c_hi) {
   constexpr int H = BN / 2;
   const int col0 = tn * H;                          // column of m
 #pragma unroll 1
-  for (int c = 0; c < H; c += 16) {
+  for (int c = c_lo; c < c_hi; c += 16) {
     float u[16], s[16];
     tmem_ld16(tacc + c, u);
     tmem_ld16(tacc + H + c, s);
@@ -118,13 +132,14 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+__device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int row, int n0,
+                                         int c_lo, int c_hi) {
   const int dh = a.head_dim, half = dh >> 1;
   const int nq = a.n_q, nkv = a.n_kv;
   const bool row_ok = row < a.M;
   const int t = row_ok ? row % a.rows_per_seq : 0;
 #pragma unroll 1
-  for (int hc = 0; hc < BN; hc += dh) {
+  for (int hc = c_lo; hc < c_hi; hc += dh) {
     const int gcol = n0 + hc;
     if (gcol >= a.N) break;
     const int head = gcol / dh;
@@ -190,9 +205,29 @@ __device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int r
   }
 }
 
+// Transposed partial store: this thread holds weight row `row` (projection
+// feature) and BN activation rows (TMEM columns).
+template <int BN>
+__device__ __forceinline__ void epi_parts(const GemmArgs& a, uint32_t tacc, int row, int n0,
+                                          int split, int c_lo, int c_hi) {
+  float* dst = a.out + (long long)split * a.part_stride + row;
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; c += 16) {
+    if (n0 + c >= a.N) break;                       // uniform across the warp
+    float v[16];
+    tmem_ld16(tacc + c, v);
+    if (row >= a.M) continue;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (n0 + c + i < a.N) dst[(long long)(n0 + c + i) * a.ldo] = v[i];
+  }
+}
+
 // ------------------------------------------------------------- the kernel
+constexpr int kGemmThreads = 320;   // producer, MMA, 8 epilogue warps
+
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
   using C = GemmCfg<BN>;
@@ -209,8 +244,15 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = args.tiles_m * args.tiles_n;
+  const int splits = EPI == EPI_PARTS ? args.k_splits : 1;
+  const int num_tiles = args.tiles_m * args.tiles_n * splits;
   const int KB = (args.K + BK - 1) / BK;
+  // K blocks [kb_lo, kb_hi) of work unit `tile` (split = tile / (tiles_m tiles_n))
+  auto kb_range = [&](int tile, int& lo, int& hi) {
+    const int sp = tile / (args.tiles_m * args.tiles_n);
+    lo = (int)((long long)sp * KB / splits);
+    hi = (int)((long long)(sp + 1) * KB / splits);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -219,7 +261,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 128);
+      mbar_init(&tempty_bar[b], 256);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -242,8 +284,11 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int tm = tile % args.tiles_m, tn = tile / args.tiles_m;
+        const int tt = tile % (args.tiles_m * args.tiles_n);
+        const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
         const int m0 = tm * BM;
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
         int nb0, nb1;
         if (EPI == EPI_SWIGLU) {
           nb0 = tn * (BN / 2);
@@ -252,7 +297,7 @@ __global__ void __launch_bounds__(192, 1)
           nb0 = tn * BN;
           nb1 = tn * BN + BN / 2;
         }
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, args.status, DEV_GEMM_PRODUCER)) {
             *abort_flag = 1;
             break;
@@ -287,7 +332,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, args.status, DEV_GEMM_MMA_FULL)) {
             *abort_flag = 1;
             ok = false;
@@ -300,7 +347,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // +32 bytes per 16-element K step inside the swizzled 128-byte row
-            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb - kb_lo) | k);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -317,8 +364,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue warps 2..5
+    // ------------------------------------------------ epilogue warps 2..9
     const int quarter = warp & 3;
+    const int chalf = (warp - 2) >> 2;            // which half of the columns
     int it = 0;
     for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -328,12 +376,17 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int tm = tile % args.tiles_m, tn = tile / args.tiles_m;
+      const int tt = tile % (args.tiles_m * args.tiles_n);
+      const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
       const int row = tm * BM + quarter * 32 + lane;
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
-      if (EPI == EPI_F32) epi_f32<BN>(args, tacc, row, tn * BN);
-      if (EPI == EPI_QKVG) epi_qkvg<BN>(args, tacc, row, tn * BN);
-      if (EPI == EPI_SWIGLU) epi_swiglu<BN>(args, tacc, row, tn);
+      constexpr int CW = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 2;   // columns per half
+      const int c_lo = chalf * CW, c_hi = c_lo + CW;
+      if (EPI == EPI_F32) epi_f32<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      if (EPI == EPI_QKVG) epi_qkvg<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      if (EPI == EPI_SWIGLU) epi_swiglu<BN>(args, tacc, row, tn, c_lo, c_hi);
+      if (EPI == EPI_PARTS)
+        epi_parts<BN>(args, tacc, row, tn * BN, tile / (args.tiles_m * args.tiles_n), c_lo, c_hi);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }

@@ -5,18 +5,26 @@
 // One warp owns one output feature (or, for SwiGLU, the pair of W_up and W_sl
 // rows of one feature) and one K segment of J x 256 elements: every lane
 // issues all J 16-byte non-caching weight loads of its segment before using
-// any, multiplies with the M activation rows (L2 resident) in fp32 and reduces
-// across the warp; the S segments of a row (S = 1, 2, 4 or 8, chosen so that
-// J <= 8) are summed through shared memory.  A CTA is 8 warps = 8 / S
-// features, so even N = 1024 spreads over 128 to 1024 CTAs with up to
-// 8 KB of weight loads in flight per warp.
+// any, multiplies with the M activation rows in fp32 and reduces across the
+// warp; the S segments of a row (S = 1, 2, 4 or 8, chosen so that J <= 8) are
+// summed through shared memory.  A CTA iteration covers 8 / S features; CTAs
+// stride over the iterations.
+//
+// Weights never change during a forward pass, so each CTA loads its first
+// iteration's weights BEFORE waiting on the previous kernel (programmatic
+// dependent launch): the weight stream of this projection overlaps the tail
+// of the kernel before it.  Later iterations prefetch the next weights into a
+// second register set while the current ones are multiplied.
 //
 //   Y[m, n] = scale[n] * sum_k X[m, k] W[n, k]                 (fp32 out)
 //   SwiGLU:  m_out[m, n] = u * SiLU(v),  u = X W_up[n]^T, v = X W_sl[n]^T
 //
-// The q/k/v/gate math of the tensor-core epilogue runs on Y in a small row
-// kernel: RoPE + per-head L2 norm + s_qk for q and k, copy for v, sigmoid for
-// the gate ("Dory1.0-4B: A Looped Normalized-GPT", Architecture).
+// PRE variant (fused nGPT step, "Dory1.0-4B: A Looped Normalized-GPT",
+// Architecture): the activation rows are not read from memory but formed by
+// every CTA from the previous sublayer's projection output y and the hidden
+// state h:  x = N(h + alpha * (N(y) - h)),  kept in shared memory as bf16.
+// CTA 0 also stores x (fp32) as the next hidden state.  This removes the
+// separate residual-update kernel between two projections.
 #pragma once
 #include "ptx.cuh"
 
@@ -26,6 +34,26 @@ constexpr int kGemvMaxM = 16;
 constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kGemvMaxK = kGemvWarps * 8 * 256;     // S <= 8 segments of J <= 8 chunks
+constexpr int kGemvPreMaxD = 2048;                  // PRE: d <= 2048 (8 chunks per lane)
+
+struct GemvArgs {
+  const __nv_bfloat16* X;   // activations [M, ldx] (not PRE)
+  int ldx;
+  int M;
+  const __nv_bfloat16* W;   // weights [N (+ pair rows), K]
+  int N, K, S, n_iters;
+  int pair_off;             // SwiGLU: W_sl row of feature n is n + pair_off
+  float* Y;                 // fp32 [M, ldy]
+  int ldy;
+  const float* col_scale;   // may be null
+  __nv_bfloat16* m_out;     // SwiGLU bf16 [M, ldm]
+  int ldm;
+  // PRE: x = N(h_in + alpha * (N(y_in) - h_in)), rows of length K (= d)
+  const float* h_in;
+  const float* y_in;
+  const float* alpha;
+  float* h_out;             // written by CTA 0 (a different buffer from h_in)
+};
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
@@ -45,81 +73,175 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-// K must be a multiple of 8; X rows are ldx elements apart (16-byte aligned).
-// SWIGLU: W holds [W_up; W_sl] and feature n uses rows n and n + pair_off.
-template <int MM, int J, bool SWIGLU>
-__global__ void __launch_bounds__(kGemvThreads)
-    gemv_kernel(const __nv_bfloat16* X, int ldx, int M, const __nv_bfloat16* W, int N, int K,
-                int S, float* Y, int ldy, const float* col_scale, int pair_off,
-                __nv_bfloat16* m_out, int ldm) {
-  constexpr int R = SWIGLU ? 2 : 1;
-  __shared__ float red[kGemvWarps][R][MM];
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_per_cta = kGemvWarps / S;
-  const int n = blockIdx.x * rows_per_cta + warp / S;
-  const int seg = warp % S;
-  const bool valid = n < N;
-  const int kbase = seg * (J * 256) + lane * 8;
+__device__ __forceinline__ void ld8f(const float* p, float* v) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
-  uint4 w[R][J];
+// The fused nGPT step of the PRE variant: warp w forms rows w, w + 8, ...
+// (lane owns 8-element chunks lane, lane + 32, ...), keeping the row in
+// registers between the two normalisations.
+__device__ __forceinline__ void gemv_pre_rows(const GemvArgs& a, __nv_bfloat16* xs) {
+  constexpr int MAXC = kGemvPreMaxD / 256;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.K, nch = d / 8;
+  const bool store = blockIdx.x == 0 && a.h_out != nullptr;
+  for (int m = warp; m < a.M; m += kGemvWarps) {
+    float u[MAXC][8];
+    float ss = 0.f;
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const __nv_bfloat16* wr = W + (long long)(valid ? n + r * pair_off : 0) * K;
+    for (int j = 0; j < MAXC; ++j) {
+      const int ch = lane + 32 * j;
+      if (ch < nch) {
+        ld8f(a.y_in + (long long)m * d + ch * 8, u[j]);
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int k = kbase + j * 256;
-      w[r][j] = (valid && k < K) ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 8; ++i) ss += u[j][i] * u[j][i];
+      }
     }
-  }
-  float acc[R][MM];
+    const float inv_y = 1.0f / sqrtf(fmaxf(warp_sum(ss), 1e-12f));
+    float su = 0.f;
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int j = 0; j < MAXC; ++j) {
+      const int ch = lane + 32 * j;
+      if (ch < nch) {
+        float h[8], al[8];
+        ld8f(a.h_in + (long long)m * d + ch * 8, h);
+        ld8f(a.alpha + ch * 8, al);
 #pragma unroll
-    for (int m = 0; m < MM; ++m) acc[r][m] = 0.f;
+        for (int i = 0; i < 8; ++i) {
+          u[j][i] = h[i] + al[i] * (u[j][i] * inv_y - h[i]);
+          su += u[j][i] * u[j][i];
+        }
+      }
+    }
+    const float inv_u = 1.0f / sqrtf(fmaxf(warp_sum(su), 1e-12f));
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int k = kbase + j * 256;
-    if (valid && k < K) {
-      float fw[R][8];
+    for (int j = 0; j < MAXC; ++j) {
+      const int ch = lane + 32 * j;
+      if (ch < nch) {
 #pragma unroll
-      for (int r = 0; r < R; ++r) bf16x8_to_f32(w[r][j], fw[r]);
-#pragma unroll
-      for (int m = 0; m < MM; ++m) {
-        if (m < M) {
-          float fx[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (long long)m * ldx + k), fx);
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[r][m] = fmaf(fw[r][i], fx[i], acc[r][m]);
+        for (int i = 0; i < 8; ++i) u[j][i] *= inv_u;
+        uint4 p;
+        p.x = pack_bf16x2(u[j][0], u[j][1]);
+        p.y = pack_bf16x2(u[j][2], u[j][3]);
+        p.z = pack_bf16x2(u[j][4], u[j][5]);
+        p.w = pack_bf16x2(u[j][6], u[j][7]);
+        *reinterpret_cast<uint4*>(xs + (long long)m * d + ch * 8) = p;
+        if (store) {
+          float4* o = reinterpret_cast<float4*>(a.h_out + (long long)m * d + ch * 8);
+          o[0] = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
+          o[1] = make_float4(u[j][4], u[j][5], u[j][6], u[j][7]);
         }
       }
     }
   }
+}
+
+// K must be a multiple of 8; X rows are 16-byte aligned.  Dynamic shared
+// memory (PRE only): M * K bf16.
+template <int MM, int J, bool SWIGLU, bool PRE>
+__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
+  constexpr int R = SWIGLU ? 2 : 1;
+  extern __shared__ __align__(16) uint8_t gemv_smem[];
+  __shared__ float red[kGemvWarps][R][MM];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S;
+  const int fpi = kGemvWarps / S;                 // features per iteration
+  const int seg = warp % S;
+  const int kbase = seg * (J * 256) + lane * 8;
+
+  uint4 w[R][J], wn[R][J];
+  auto load_w = [&](uint4 (&dst)[R][J], int it) {
+    const int n = it * fpi + warp / S;
+    const bool valid = it < a.n_iters && n < a.N;
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r) {
+      const __nv_bfloat16* wr = a.W + (long long)(valid ? n + r * a.pair_off : 0) * a.K;
 #pragma unroll
-    for (int m = 0; m < MM; ++m) {
-      const float v = warp_sum(acc[r][m]);
-      if (lane == 0) red[warp][r][m] = v;
-    }
-  __syncthreads();
-  const int t = threadIdx.x;
-  if (t < rows_per_cta * MM) {
-    const int rl = t / MM, m = t % MM;
-    const int nn = blockIdx.x * rows_per_cta + rl;
-    if (nn < N && m < M) {
-      float s0 = 0.f, s1 = 0.f;
-      for (int sg = 0; sg < S; ++sg) {
-        s0 += red[rl * S + sg][0][m];
-        if (SWIGLU) s1 += red[rl * S + sg][R - 1][m];
+      for (int j = 0; j < J; ++j) {
+        const int k = kbase + j * 256;
+        dst[r][j] = (valid && k < a.K) ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (SWIGLU)
-        m_out[(long long)m * ldm + nn] = __float2bfloat16_rn(s0 * (s1 / (1.0f + __expf(-s1))));
-      else
-        Y[(long long)m * ldy + nn] = s0 * (col_scale ? col_scale[nn] : 1.f);
+    }
+  };
+
+  int it = blockIdx.x;
+  load_w(w, it);                                  // weights: safe before the wait
+  pdl_wait();
+  pdl_trigger();
+
+  const __nv_bfloat16* X = a.X;
+  int ldx = a.ldx;
+  if (PRE) {
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(gemv_smem);
+    gemv_pre_rows(a, xs);
+    __syncthreads();
+    X = xs;
+    ldx = a.K;
+  }
+
+  for (; it < a.n_iters; it += gridDim.x) {
+    const int nxt = it + gridDim.x;
+    if (nxt < a.n_iters) load_w(wn, nxt);
+    const int n = it * fpi + warp / S;
+    const bool valid = n < a.N;
+    float acc[R][MM];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int m = 0; m < MM; ++m) acc[r][m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int k = kbase + j * 256;
+      if (valid && k < a.K) {
+        float fw[R][8];
+#pragma unroll
+        for (int r = 0; r < R; ++r) bf16x8_to_f32(w[r][j], fw[r]);
+#pragma unroll
+        for (int m = 0; m < MM; ++m) {
+          if (m < a.M) {
+            float fx[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (long long)m * ldx + k), fx);
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[r][m] = fmaf(fw[r][i], fx[i], acc[r][m]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int m = 0; m < MM; ++m) {
+        const float v = warp_sum(acc[r][m]);
+        if (lane == 0) red[warp][r][m] = v;
+      }
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (t < fpi * MM) {
+      const int rl = t / MM, m = t % MM;
+      const int nn = it * fpi + rl;
+      if (nn < a.N && m < a.M) {
+        float s0 = 0.f, s1 = 0.f;
+        for (int sg = 0; sg < S; ++sg) {
+          s0 += red[rl * S + sg][0][m];
+          if (SWIGLU) s1 += red[rl * S + sg][R - 1][m];
+        }
+        if (SWIGLU)
+          a.m_out[(long long)m * a.ldm + nn] = __float2bfloat16_rn(s0 * (s1 / (1.0f + __expf(-s1))));
+        else
+          a.Y[(long long)m * a.ldy + nn] = s0 * (a.col_scale ? a.col_scale[nn] : 1.f);
+      }
+    }
+    __syncthreads();
+    if (nxt < a.n_iters) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < J; ++j) w[r][j] = wn[r][j];
     }
   }
 }

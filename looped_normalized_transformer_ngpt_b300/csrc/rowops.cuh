@@ -95,10 +95,14 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t* token
 }
 
 // nGPT residual step ("Dory1.0-4B: A Looped Normalized-GPT", Architecture):
-// h <- N(h + alpha * (N(y) - h)), y = the sublayer's projection output.
+// h <- N(h + alpha * (N(y) - h)), y = the sublayer's projection output (the
+// sum of n_parts partial sums part_stride apart; one part unless the
+// projection was split along K).
 __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __nv_bfloat16* hb,
                                                                   const float* y,
-                                                                  const float* alpha, int d) {
+                                                                  const float* alpha, int d,
+                                                                  int n_parts,
+                                                                  long long part_stride) {
   __shared__ float red[4];
   pdl_wait();
   pdl_trigger();
@@ -111,6 +115,12 @@ __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __
     const int ch = threadIdx.x + j * kRowThreads;
     if (ch < nch) {
       load8(y + row * d + ch * 8, yv[j]);
+      for (int p = 1; p < n_parts; ++p) {
+        float t[8];
+        load8(y + p * part_stride + row * d + ch * 8, t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yv[j][i] += t[i];
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss += yv[j][i] * yv[j][i];
     }
@@ -145,6 +155,36 @@ __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __
   }
 }
 
+// SwiGLU of split-K partial sums: y = [u | v] per row (2F columns, n_parts
+// partials part_stride apart); m = u * SiLU(v) as bf16 [rows, F].
+// grid = (ceil(F / 1024), rows), 128 threads x 8 columns.
+__global__ void __launch_bounds__(kRowThreads) swiglu_parts_kernel(const float* y, int F,
+                                                                   int n_parts,
+                                                                   long long part_stride,
+                                                                   __nv_bfloat16* m) {
+  pdl_wait();
+  pdl_trigger();
+  const long long row = blockIdx.y;
+  const int c0 = (blockIdx.x * kRowThreads + threadIdx.x) * 8;
+  if (c0 >= F) return;
+  float u[8], v[8];
+  load8(y + row * 2 * F + c0, u);
+  load8(y + row * 2 * F + F + c0, v);
+  for (int p = 1; p < n_parts; ++p) {
+    float tu[8], tv[8];
+    load8(y + p * part_stride + row * 2 * F + c0, tu);
+    load8(y + p * part_stride + row * 2 * F + F + c0, tv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      u[i] += tu[i];
+      v[i] += tv[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] *= v[i] / (1.0f + __expf(-v[i]));
+  store8_bf16(m + row * F + c0, u);
+}
+
 // Loop-boundary transforms ("Dory1.0-4B: A Looped Normalized-GPT", Training
 // with Loops): the state starts as x; before each pass of the shared block
 // the block input is N(s + x); the state after a pass is the normalised block
@@ -154,43 +194,105 @@ enum BoundaryMode : int {
   BND_ENTER_FIRST = 1, // h = N(s_0 + x) with s_0 = x held in h
   BND_ENTER_NEXT = 2,  // s = N(h); h = N(s + x)
   BND_EXIT = 3,        // h = N(h)  (final state s_k)
+  BND_SAVE_ENTER = 4,  // x = h; h = N(x + x)  (BND_SAVE_X then BND_ENTER_FIRST)
 };
 
+// With y != null the row is first moved by the pending nGPT step of the last
+// sublayer, h <- N(h + alpha * (N(y) - h)), y being that sublayer's
+// projection output (n_parts partial sums part_stride apart).
 __global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_bfloat16* hb,
-                                                               float* x32, int d, int mode) {
+                                                               float* x32, int d, int mode,
+                                                               const float* y, int n_parts,
+                                                               long long part_stride,
+                                                               const float* alpha) {
   __shared__ float red[4];
   pdl_wait();
   pdl_trigger();
   const long long row = blockIdx.x;
   const int nch = d / 8;
-  if (mode == BND_SAVE_X) {
-    for (int ch = threadIdx.x; ch < nch; ch += kRowThreads) {
-      float v[8];
-      load8(h32 + row * d + ch * 8, v);
-      store8(x32 + row * d + ch * 8, v);
-    }
-    return;
-  }
   float hv[kRowMaxChunks][8];
-  float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kRowMaxChunks; ++j) {
     const int ch = threadIdx.x + j * kRowThreads;
-    if (ch < nch) {
-      load8(h32 + row * d + ch * 8, hv[j]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss += hv[j][i] * hv[j][i];
-    }
+    if (ch < nch) load8(h32 + row * d + ch * 8, hv[j]);
   }
-  if (mode != BND_ENTER_FIRST) {
+  if (y != nullptr) {
+    float yv[kRowMaxChunks][8];
+    float sy = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j) {
+      const int ch = threadIdx.x + j * kRowThreads;
+      if (ch < nch) {
+        load8(y + row * d + ch * 8, yv[j]);
+        for (int p = 1; p < n_parts; ++p) {
+          float t[8];
+          load8(y + p * part_stride + row * d + ch * 8, t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) yv[j][i] += t[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sy += yv[j][i] * yv[j][i];
+      }
+    }
+    const float inv_y = 1.0f / sqrtf(fmaxf(block_sum128(sy, red), 1e-12f));
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j) {
+      const int ch = threadIdx.x + j * kRowThreads;
+      if (ch < nch) {
+        float av[8];
+        load8(alpha + ch * 8, av);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          hv[j][i] += av[i] * (yv[j][i] * inv_y - hv[j][i]);
+          ss += hv[j][i] * hv[j][i];
+        }
+      }
+    }
     const float inv = 1.0f / sqrtf(fmaxf(block_sum128(ss, red), 1e-12f));
 #pragma unroll
     for (int j = 0; j < kRowMaxChunks; ++j)
 #pragma unroll
       for (int i = 0; i < 8; ++i) hv[j][i] *= inv;
   }
+  if (mode == BND_SAVE_X || mode == BND_SAVE_ENTER) {
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j) {
+      const int ch = threadIdx.x + j * kRowThreads;
+      if (ch < nch) store8(x32 + row * d + ch * 8, hv[j]);
+    }
+    if (mode == BND_SAVE_X) {
+      if (y != nullptr) {
+#pragma unroll
+        for (int j = 0; j < kRowMaxChunks; ++j) {
+          const int ch = threadIdx.x + j * kRowThreads;
+          if (ch < nch) {
+            store8(h32 + row * d + ch * 8, hv[j]);
+            store8_bf16(hb + row * d + ch * 8, hv[j]);
+          }
+        }
+      }
+      return;
+    }
+  }
+  if (mode == BND_ENTER_NEXT || mode == BND_EXIT) {
+    float s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j) {
+      const int ch = threadIdx.x + j * kRowThreads;
+      if (ch < nch) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s2 += hv[j][i] * hv[j][i];
+      }
+    }
+    const float inv = 1.0f / sqrtf(fmaxf(block_sum128(s2, red), 1e-12f));
+#pragma unroll
+    for (int j = 0; j < kRowMaxChunks; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hv[j][i] *= inv;
+  }
   if (mode != BND_EXIT) {
-    ss = 0.f;
+    float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kRowMaxChunks; ++j) {
       const int ch = threadIdx.x + j * kRowThreads;
@@ -240,24 +342,28 @@ __global__ void kv_write_kernel(const __nv_bfloat16* k_cur, const __nv_bfloat16*
   }
 }
 
-// RoPE table for the positions of one call: tab[t][i] = (cos, sin) of
-// (P0 + t) * base^(-2i/dh); the angle is formed and reduced mod 2 pi in fp64
-// so long contexts keep full fp32 accuracy.
-__global__ void rope_table_kernel(float2* tab, int C, int P0, int dh, double base) {
+// RoPE tables for the positions of one call: tab_b[t][i] = (cos, sin) of
+// (P0 + t) * base_b^(-2i/dh) for the two bases (b = 0: sliding-window
+// layers, b = 1: full layers); the angle is formed and reduced mod 2 pi in
+// fp64 so long contexts keep full fp32 accuracy.
+__global__ void rope_table_kernel(float2* tab0, float2* tab1, int C, int P0, int dh, double base0,
+                                  double base1) {
   pdl_wait();
   pdl_trigger();
   const int half = dh / 2;
   const long long n = (long long)C * half;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < 2 * n;
        idx += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(idx / half), i = (int)(idx % half);
-    const double inv_freq = pow(base, -2.0 * i / dh);
+    const int which = idx >= n;
+    const long long e = idx - which * n;
+    const int t = (int)(e / half), i = (int)(e % half);
+    const double inv_freq = pow(which ? base1 : base0, -2.0 * i / dh);
     double ang = (double)(P0 + t) * inv_freq;
     const double two_pi = 6.283185307179586476925286766559;
     ang -= floor(ang / two_pi) * two_pi;
     double s, c;
     sincos(ang, &s, &c);
-    tab[idx] = make_float2((float)c, (float)s);
+    (which ? tab1 : tab0)[e] = make_float2((float)c, (float)s);
   }
 }
 

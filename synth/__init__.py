@@ -78,8 +78,13 @@ SMALL = Shape("small", d=1024, n_in=4, n_rec=10, n_out=4, n_q=8, n_kv=2, head_di
 DORY4B = Shape("dory4b", d=2048, n_in=16, n_rec=40, n_out=16, n_q=16, n_kv=4, head_dim=128,
                ffn=6144, vocab=131072, window=4096)
 
-SHAPES = {s.name: s for s in (TINY, TINY_LOOPFULL, SMALL, DORY4B)}
-SHAPE_ID = {"tiny": 0, "small": 1, "dory4b": 2, "tiny_loopfull": 100}
+# Test-only variant of the 4B-class shape with 2 / 4 / 2 layers: every matrix
+# and head has its full width (so every tile and the full vocabulary are
+# exercised) while the CPU oracle stays fast.  Layers 3 and 7 are full.
+DORY4B_SLIM = DORY4B.replace(name="dory4b_slim", n_in=2, n_rec=4, n_out=2)
+
+SHAPES = {s.name: s for s in (TINY, TINY_LOOPFULL, SMALL, DORY4B, DORY4B_SLIM)}
+SHAPE_ID = {"tiny": 0, "small": 1, "dory4b": 2, "tiny_loopfull": 100, "dory4b_slim": 102}
 
 # Tensor ids used to derive one independent seed per weight tensor.
 _TID = {"embed_in": 0, "embed_out": 1, "w_q": 2, "w_k": 3, "w_v": 4, "w_g": 5,
@@ -140,6 +145,14 @@ def make_weights(shape: Shape, shape_id: int | None = None) -> dict:
     """All weights of a model: {'embed_in', 'embed_out', 's_z', 'layers': [...]}"""
     w = embeddings(shape, shape_id)
     w["layers"] = [layer_weights(shape, l, shape_id) for l in range(shape.n_layers)]
+    return w
+
+
+def make_weights_lazy(shape: Shape, shape_id: int | None = None) -> dict:
+    """Like make_weights, but 'layers' is a generator that draws one layer at
+    a time (for shapes whose weights do not fit in host memory at once)."""
+    w = embeddings(shape, shape_id)
+    w["layers"] = (layer_weights(shape, l, shape_id) for l in range(shape.n_layers))
     return w
 
 
