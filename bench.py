@@ -393,6 +393,178 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------ 4B-class workloads
+def decode_step_bytes(sh, B, k, P0):
+    """Algorithmic HBM bytes of one decode step at position P0: every weight
+    matrix of the applied layers once, the LM head once, and the cached K/V
+    of the visible keys (the new token's own K/V is not read from HBM)."""
+    lp = layer_params(sh)
+    per_layer = 2 * sum(lp.values())
+    apps = [l for l in range(sh.n_in)] + [l for _ in range(k)
+                                          for l in range(sh.n_in, sh.n_in + sh.n_rec)] + \
+        [l for l in range(sh.n_in + sh.n_rec, sh.n_layers)]
+    w = per_layer * len(apps) + 2 * sh.vocab * sh.d
+    kv = 0
+    for l in apps:
+        keys = P0 if sh.is_full(l) else min(P0, sh.window - 1)
+        kv += B * 2 * sh.n_kv * sh.head_dim * 2 * keys
+    return {"weights": w, "kv": kv}
+
+
+def fill_cache_synthetic(m, sh, seed=0):
+    """Synthetic cache contents (unit K rows per head, N(0, 0.3^2) V) for
+    timing decode at long contexts without the prefill; every slot of every
+    (layer, slice) block is written."""
+    import torch
+    g = torch.Generator(device=m.device).manual_seed(seed)
+    for l in range(sh.n_layers):
+        n_sl = m.k_max if (m.cache_mode == 1 and sh.is_recurrent(l)) else 1
+        for sl in range(n_sl):
+            for which in (0, 1):
+                blk = m.kv_block(l, sl, which)
+                flat = blk.view(-1, sh.head_dim)
+                step = 1 << 20
+                for r0 in range(0, flat.shape[0], step):
+                    x = torch.randn(min(step, flat.shape[0] - r0), sh.head_dim, device=m.device,
+                                    generator=g)
+                    x = x / x.norm(dim=1, keepdim=True) if which == 0 else 0.3 * x
+                    flat[r0:r0 + x.shape[0]].copy_(x.to(torch.bfloat16))
+
+
+def _graph_time(fn, stream, warm=2, reps=5):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    del g
+    return e0.elapsed_time(e1) / reps
+
+
+def run_workload_4b(args):
+    """The 4B-class workloads (d 2048, 16/40/16 layers, 16 q / 4 kv heads,
+    SwiGLU 6144, vocab 131072, window 4096), timed on one GPU:
+      prefill4b  prefill of 1 x 8192 tokens at k = 1, 2, 4;
+      decode4b   64 sequences with a 32768-position last-loop cache, decode
+                 steps at k = 1..4 (cache contents synthetic);
+      longctx4b  1 sequence at 262144 positions, decode at k = 1, 4 with the
+                 last-loop cache and at k = 4 with the per-loop cache (cache
+                 contents synthetic), plus the KV bytes of both modes."""
+    import torch
+    import synth
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    sh = synth.DORY4B
+    peaks, peak_src = load_peaks()
+    st = torch.cuda.Stream()
+    out = {"workload": args.workload, "shape": "4B-class (d 2048, 16/40/16 layers, 16/4 heads, "
+                                                 "ffn 6144, vocab 131072, window 4096)",
+           "dtype": "bf16", "data": "synthetic (torch-seeded unit-norm bf16 weights, seeded tokens)"}
+    with ClockSampler(0) as clk:
+        if args.workload == "prefill4b":
+            T = 8192
+            m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,
+                           k_max=4)
+            tok = torch.tensor(synth.tokens(sh, 1, T, seed=3), device="cuda")
+            lg = torch.empty((1, sh.vocab), device="cuda")
+            res = {}
+            for k in (1, 2, 4):
+                def fn(k=k):
+                    m.reset()
+                    m.prefill(tok, k, logits=lg, stream=st)
+                ms = _graph_time(fn, st)
+                fl = step_flops(sh, 1, T, k)
+                res[str(k)] = {"prefill_tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3),
+                               "tflops": round(sum(fl.values()) / (ms / 1e3) / 1e12, 1)}
+            m.profile_begin(1 << 15)
+            with torch.cuda.stream(st):
+                m.reset()
+                m.prefill(tok, 4, logits=lg, stream=st)
+            prof = m.profile_end()
+            fl = step_flops(sh, 1, T, 4)
+            bd = {n: {"ms": round(t, 3), "launches": c,
+                      "tflops": round(fl[n] / (t / 1e3) / 1e12, 1) if n in fl and t > 0 else None}
+                  for n, (t, c) in prof.items() if c}
+            gemm = [n for n in ("qkvg_gemm", "o_gemm", "upgate_gemm", "down_gemm")]
+            g_ms = sum(prof[n][0] for n in gemm)
+            g_tf = sum(fl[n] for n in gemm) / (g_ms / 1e3) / 1e12
+            out.update({"per_k": res, "breakdown_k4": bd,
+                        "gemm_roofline_k4": {"achieved": round(g_tf, 1),
+                                             "peak": peaks["bf16_tflops_sustained"],
+                                             "unit": "TFLOP/s",
+                                             "frac": round(g_tf / peaks["bf16_tflops_sustained"], 4),
+                                             "peak_source": peak_src + " (bf16 sustained)"}})
+        else:
+            if args.workload == "decode4b":
+                B, ctx, D, modes = 64, 32768, 4, [(dory.LAST_LOOP, (1, 2, 3, 4))]
+            else:
+                B, ctx, D, modes = 1, 262144, 8, [(dory.LAST_LOOP, (1, 4)), (dory.PER_LOOP, (4,))]
+            weights = synth.make_weights_torch(sh)
+            res, kvb = {}, {}
+            m = None
+            for mode, ks in modes:
+                if m is None:
+                    m = dory.Model(sh, weights, max_batch=B, max_ctx=ctx, max_chunk=1,
+                                   k_max=4, cache_mode=mode)
+                else:
+                    m.bind(B, ctx, 1, 4, mode)
+                kvb["last_loop" if mode == dory.LAST_LOOP else "per_loop_k4"] = int(m.kv.numel())
+                fill_cache_synthetic(m, sh)
+                tok = torch.tensor(synth.tokens(sh, B, 1, seed=4)[:, 0], device="cuda")
+                lg = torch.empty((B, sh.vocab), device="cuda")
+                nxt = torch.empty((B,), dtype=torch.int32, device="cuda")
+                for k in ks:
+                    P0 = ctx - D
+
+                    def fn(k=k):
+                        m.set_length(B, P0)
+                        for _ in range(D):
+                            m.decode(tok, k, logits=lg, next_tokens=nxt, stream=st)
+                    ms = _graph_time(fn, st, warm=1, reps=3) / D
+                    by = decode_step_bytes(sh, B, k, P0 + D // 2)
+                    gbs = (by["weights"] + by["kv"]) / (ms / 1e3) / 1e9
+                    key = ("per_loop" if mode == dory.PER_LOOP else "last_loop") + f"_k{k}"
+                    res[key] = {"decode_tok_s": round(B / (ms / 1e3), 1),
+                                "ms_per_step": round(ms, 3),
+                                "bytes_per_step_GB": round((by["weights"] + by["kv"]) / 1e9, 2),
+                                "achieved_GBs": round(gbs, 1),
+                                "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+                if mode == dory.LAST_LOOP:
+                    m.set_length(B, ctx - D)
+                    m.profile_begin(1 << 15)
+                    with torch.cuda.stream(st):
+                        m.decode(tok, ks[-1], logits=lg, next_tokens=nxt, stream=st)
+                    prof = m.profile_end()
+                    by = decode_step_bytes(sh, B, ks[-1], ctx - D)
+                    at = prof["attention"][0]
+                    out["attention_k%d" % ks[-1]] = {
+                        "ms": round(at, 3), "kv_GB": round(by["kv"] / 1e9, 2),
+                        "achieved_GBs": round(by["kv"] / (at / 1e3) / 1e9, 1),
+                        "hbm_frac": round(by["kv"] / (at / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+                    out["breakdown_eager_k%d" % ks[-1]] = {
+                        n: {"ms": round(t, 3), "launches": c} for n, (t, c) in prof.items() if c}
+            out.update({"batch": B, "context": ctx, "per_mode_k": res, "kv_bytes": kvb,
+                        "hbm_peak_GBs": peaks["hbm_gbs"], "peak_source": peak_src,
+                        "cache": "synthetic contents (unit K rows, N(0, 0.3^2) V); decode cost "
+                                 "does not depend on them"})
+    out["clocks"] = clk.summary()
+    print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ CPU oracle
 def _blas_threads():
     try:
@@ -505,10 +677,15 @@ def main(argv=None):
                     default=[1, 2, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--workload", choices=["small", "prefill4b", "decode4b", "longctx4b"],
+                    default="small", help="small: the default benchmark line; the others time "
+                                          "the 4B-class workloads (one JSON line, not the contract)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "small":
+        run_workload_4b(args)
     elif args.mode == "profile":
         run_profile_target(args)
     else:

@@ -150,12 +150,22 @@ DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k,
 /* Decode: appends one token to each of B sequences at the current length and
  * runs the forward at loop count k.  tokens: device int32 [B].  logits:
  * device fp32 [B, vocab] or NULL; next: device int32 [B] greedy tokens or
- * NULL. */
+ * NULL (requires logits).
+ * Decode steps of up to 16 sequences run five kernels per layer application
+ * (see dory_set_persistent_decode for the single-kernel alternative); larger
+ * batches run the tensor-core projections with K split over the SMs. */
 DORY_API int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                      float* logits, int32_t* next, void* stream);
 
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
+
+/* Declares that the bound KV region already holds positions 0 .. len-1 of B
+ * sequences (for instance a cache saved earlier and copied back, in the
+ * layout dory_kv_bytes describes); later calls continue at position len.
+ * Host state only: the caller is responsible for the cache contents.
+ * Requires B <= max_batch and len <= max_ctx (else DORY_ECAPACITY). */
+DORY_API int dory_set_length(dory_t* m, int B, int len);
 
 /* Resets every sequence to length 0 (host state only; cache contents are
  * simply overwritten by later calls). */
@@ -171,6 +181,15 @@ DORY_API const char* dory_strerror(int status);
  * workspace: *out = 0 if every bounded device wait completed, else a code
  * naming the kernel and wait that expired.  The word is cleared. */
 DORY_API int dory_device_status(dory_t* m, int* out, void* stream);
+
+/* enable = 1: decode steps of up to 16 sequences (d <= 2048) run as ONE
+ * persistent kernel after the RoPE table, launched cooperatively (one CTA
+ * per SM, grid barriers between the dependent steps; every barrier wait is
+ * bounded: an expired wait sets the device status word and abandons the
+ * step, and dory_bind must be called again before further use).
+ * enable = 0 (the default): five kernels per layer application.  Both give
+ * the same results up to rounding order.  Host state only. */
+DORY_API int dory_set_persistent_decode(dory_t* m, int enable);
 
 /* Number of kernels the last dory_prefill / dory_decode_step launched. */
 DORY_API int dory_last_launch_count(const dory_t* m, int* out);
@@ -191,7 +210,8 @@ typedef enum {
     DORY_K_BOUNDARY = 9,    /* loop-boundary re-injection / normalisation */
     DORY_K_LM_HEAD = 10,    /* logits */
     DORY_K_ARGMAX = 11,     /* greedy token */
-    DORY_K_COUNT = 12
+    DORY_K_DECODE_STEP = 12,/* whole decode step as one persistent kernel */
+    DORY_K_COUNT = 13
 } dory_kernel_class;
 
 /* Starts recording a CUDA-event pair around each of the next max_launches
@@ -236,6 +256,13 @@ DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* 
                                   void* out, int B, int C, int P0, int S, int n_q, int n_kv,
                                   int head_dim, int window, float scale, void* scratch,
                                   size_t scratch_bytes, void* stream);
+
+/* Multi-token (prefill) attention runs on the tcgen05 tensor cores when
+ * head_dim is 128 and the key tiles of 128 positions line up (P0 a multiple
+ * of 128, window and ring size multiples of 128), else on the mma.sync
+ * kernel.  enable = 0 forces the mma.sync kernel (for comparison): for the
+ * handle m, or, with m = NULL, for dory_debug_attention.  Host state only. */
+DORY_API int dory_set_tc_attention(dory_t* m, int enable);
 
 /* Scratch bytes dory_debug_attention needs for one-token (decode) calls. */
 DORY_API size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim);

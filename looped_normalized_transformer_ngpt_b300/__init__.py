@@ -32,7 +32,7 @@ LAST_LOOP = 0
 PER_LOOP = 1
 
 KERNEL_CLASSES = ("embed", "rope", "qkvg_gemm", "attention", "kv_write", "o_gemm", "ngpt_update",
-                  "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax")
+                  "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax", "decode_step")
 
 
 class DoryConfig(ctypes.Structure):
@@ -73,10 +73,13 @@ _SIGS = {
     "dory_decode_step": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "dory_length": (_I, [_P, ctypes.POINTER(_I)]),
     "dory_reset": (_I, [_P]),
+    "dory_set_length": (_I, [_P, _I, _I]),
     "dory_destroy": (_I, [_P]),
     "dory_strerror": (ctypes.c_char_p, [_I]),
     "dory_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "dory_last_launch_count": (_I, [_P, ctypes.POINTER(_I)]),
+    "dory_set_persistent_decode": (_I, [_P, _I]),
+    "dory_set_tc_attention": (_I, [_P, _I]),
     "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
     "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
     "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
@@ -256,6 +259,11 @@ class Model:
         _check("dory_length", lib().dory_length(self.handle, ctypes.byref(v)))
         return v.value
 
+    def set_length(self, batch, length):
+        """Declare that the KV cache already holds `length` positions of
+        `batch` sequences (contents are the caller's)."""
+        _check("dory_set_length", lib().dory_set_length(self.handle, batch, length))
+
     def reset(self):
         _check("dory_reset", lib().dory_reset(self.handle))
 
@@ -264,6 +272,17 @@ class Model:
         _check("dory_device_status", lib().dory_device_status(self.handle, ctypes.byref(v),
                                                               _stream_ptr(stream)))
         return v.value
+
+    def set_persistent_decode(self, enable: bool):
+        """Decode steps of <= 16 sequences as one persistent kernel (default)
+        or one kernel per step of the layer."""
+        _check("dory_set_persistent_decode",
+               lib().dory_set_persistent_decode(self.handle, 1 if enable else 0))
+
+    def set_tc_attention(self, enable: bool):
+        """Prefill attention on tcgen05 where its tile rules hold (default)
+        or always on the mma.sync kernel."""
+        _check("dory_set_tc_attention", lib().dory_set_tc_attention(self.handle, 1 if enable else 0))
 
     def launch_count(self):
         v = ctypes.c_int()
@@ -292,6 +311,12 @@ class Model:
             self.close()
         except Exception:
             pass
+
+
+def set_debug_tc_attention(enable: bool):
+    """dory_debug_attention: tensor-core prefill kernel where it applies
+    (default) or always the mma.sync kernel."""
+    _check("dory_set_tc_attention", lib().dory_set_tc_attention(None, 1 if enable else 0))
 
 
 def debug_gemm(A, B, C=None, stream=None):

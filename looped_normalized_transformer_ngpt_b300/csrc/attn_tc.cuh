@@ -1,0 +1,350 @@
+// attn_tc.cuh - prefill attention on the 5th-generation tensor cores
+// (tcgen05, operands fed by TMA, accumulators in TMEM), head_dim 128.
+//
+// Same operation as attn_prefill_kernel ("Dory1.0-4B: A Looped
+// Normalized-GPT", Architecture; Last-Loop KV Caching): for every query
+// position t of the call and query head h,
+//   o_h(t) = sum_j softmax_j(scale * q_h(t) . k_{h/G}(j)) v_{h/G}(j),
+//   j visible iff j <= t and (full layer or t - j < W),
+// keys of positions < P0 from the cache slice, the others from this call's
+// projections; out = o * sigmoid(g) (bf16).
+//
+// One CTA = (block of 128 / G query positions, kv head, sequence): its 128
+// rows are (position, head-in-group) pairs, so one K/V tile serves all G
+// heads.  Warp roles (192 threads):
+//   warp 0    TMA producer: the Q tile once (3-D box: 64 dims x G heads x
+//             128/G positions, two boxes for the 128 dims), then 128-key K and
+//             V tiles into a 2-stage ring (128-byte swizzle);
+//   warp 1    TMEM owner and MMA issuer: S_j = Q K_j^T (M = N = 128, K = 128)
+//             into one of two TMEM S buffers, and O += P_j V_j (V as an MN-major
+//             operand) into the TMEM O accumulator;
+//   warps 2-5 softmax, one row per thread: S row from TMEM, mask, running max,
+//             P = exp2(S - max) written to shared memory as the bf16 K-major
+//             A operand of the PV MMA; O is rescaled in TMEM only when the
+//             running max rises by more than 8 (log2 units) - otherwise the
+//             stale max stays exact, since the same max scales P and the row
+//             sum; final O / sum * gate from TMEM to global.
+// Key tiles are aligned to 128 positions and never mix cached and current
+// keys (the launcher requires P0 % 128 == 0 and 128-aligned ring sizes).
+// Every wait is bounded (status word + orderly exit).
+#pragma once
+#include "ptx.cuh"
+
+namespace dory {
+
+struct AttnTcArgs {
+  int C, P0, S;               // tokens per sequence in the call, first position, cache slots
+  int n_kv, G;                // kv heads, query heads per kv head
+  int window;                 // 0 = full causal
+  float scale_log2;
+  const __nv_bfloat16* gate;  // [B*C, n_q*128] sigmoid(g)
+  __nv_bfloat16* out;         // [B*C, n_q*128]
+  int n_q;
+  int* status;
+};
+
+struct AttnTcCfg {
+  static constexpr int BK = 128;                 // keys per tile
+  static constexpr int HALF = 128 * 128;         // one 64-dim half of a 128-row tile (bytes)
+  static constexpr int TILE = 2 * HALF;          // 128 rows x 128 dims bf16
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = TILE;             // 2 stages
+  static constexpr int V_OFF = K_OFF + 2 * TILE; // 2 stages
+  static constexpr int P_OFF = V_OFF + 2 * TILE;
+  static constexpr int BAR_OFF = P_OFF + TILE;
+  static constexpr size_t SMEM = BAR_OFF + 256 + 1024;   // + barriers + alignment slack
+};
+
+// tensor maps: q (3-D: dim, head, token), k/v current (3-D: dim, kv head,
+// token), k/v cache (2-D: dim, slot row).
+template <bool FROM_CACHE>
+__device__ __forceinline__ void attn_tc_load_kv(uint8_t* dst_k, uint8_t* dst_v,
+                                                const CUtensorMap* tk, const CUtensorMap* tv,
+                                                uint64_t* bar, int j0, int b, int kvh,
+                                                const AttnTcArgs& a) {
+  if (FROM_CACHE) {
+    const int row = (b * a.n_kv + kvh) * a.S + (j0 % a.S);
+    tma_load_2d(dst_k, tk, bar, 0, row);
+    tma_load_2d(dst_k + AttnTcCfg::HALF, tk, bar, 64, row);
+    tma_load_2d(dst_v, tv, bar, 0, row);
+    tma_load_2d(dst_v + AttnTcCfg::HALF, tv, bar, 64, row);
+  } else {
+    const int tok = b * a.C + (j0 - a.P0);
+    tma_load_3d(dst_k, tk, bar, 0, kvh, tok);
+    tma_load_3d(dst_k + AttnTcCfg::HALF, tk, bar, 64, kvh, tok);
+    tma_load_3d(dst_v, tv, bar, 0, kvh, tok);
+    tma_load_3d(dst_v + AttnTcCfg::HALF, tv, bar, 64, kvh, tok);
+  }
+}
+
+__global__ void __launch_bounds__(192, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_kc,
+                   const __grid_constant__ CUtensorMap tm_vc, const AttnTcArgs a) {
+  using Cf = AttnTcCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;    // [2]
+  uint64_t* kv_empty = bars + 3;   // [2]
+  uint64_t* s_full = bars + 5;     // [2]
+  uint64_t* s_free = bars + 7;     // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int QP = 128 / a.G;                             // query positions per CTA
+  const int qb = gridDim.x - 1 - blockIdx.x;            // longest rows first
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int q0 = qb * QP;
+  const int nqv = min(QP, a.C - q0);
+  const int p_lo = a.P0 + q0, p_hi = a.P0 + q0 + nqv - 1;
+  const int k_lo = a.window > 0 ? max(0, p_lo - a.window + 1) : 0;
+  const int t_first = k_lo / Cf::BK, t_last = p_hi / Cf::BK;
+  const int ntiles = t_last - t_first + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, O: 256..383
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, Cf::TILE);
+      const int tok = b * a.C + q0;
+      tma_load_3d(smem + Cf::Q_OFF, &tm_q, q_full, 0, kvh * a.G, tok);
+      tma_load_3d(smem + Cf::Q_OFF + Cf::HALF, &tm_q, q_full, 64, kvh * a.G, tok);
+      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait_bounded(&kv_empty[st], ((j >> 1) - 1) & 1, a.status,
+                                         DEV_ATTN_PRODUCER)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int j0 = (t_first + j) * Cf::BK;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::TILE);
+        uint8_t* dk = smem + Cf::K_OFF + st * Cf::TILE;
+        uint8_t* dv = smem + Cf::V_OFF + st * Cf::TILE;
+        if (j0 < a.P0)
+          attn_tc_load_kv<true>(dk, dv, &tm_kc, &tm_vc, &kv_full[st], j0, b, kvh, a);
+        else
+          attn_tc_load_kv<false>(dk, dv, &tm_k, &tm_v, &kv_full[st], j0, b, kvh, a);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc_idesc_bf16(128, 128);
+      constexpr uint32_t idesc_o = tc_idesc_bf16(128, 128) | (1u << 16);   // B (V) MN-major
+      const uint32_t q_addr = smem_u32(smem + Cf::Q_OFF);
+      const uint32_t p_addr = smem_u32(smem + Cf::P_OFF);
+      bool ok = mbar_wait_bounded(q_full, 0, a.status, DEV_ATTN_MMA);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait_bounded(&kv_full[st], (j >> 1) & 1, a.status, DEV_ATTN_MMA)) return false;
+        if (j >= 2 && !mbar_wait_bounded(&s_free[st], ((j >> 1) - 1) & 1, a.status, DEV_ATTN_MMA))
+          return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + Cf::K_OFF + st * Cf::TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * Cf::HALF + (kk & 3) * 32;
+          tc_mma_bf16(tmem + st * 128, tc_sdesc_sw128(q_addr + off), tc_sdesc_sw128(k_addr + off),
+                      idesc_s, kk);
+        }
+        tc_commit(&s_full[st]);
+        return true;
+      };
+      if (ok && ntiles > 0) ok = issue_s(0);
+      for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
+        if (j + 1 < ntiles && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(p_full, j & 1, a.status, DEV_ATTN_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = j & 1;
+        const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major)
+          const uint32_t pa = p_addr + (kk >> 2) * Cf::HALF + (kk & 3) * 32;
+          tc_mma_bf16(tmem + 256, tc_sdesc_sw128(pa),
+                      tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::HALF, 1024), idesc_o,
+                      (j | kk) != 0);
+        }
+        tc_commit(&kv_empty[st]);
+        tc_commit(o_done);
+      }
+      if (!ok) *abort_flag = 1;
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0, a.status, DEV_ATTN_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps 2..5
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                  // tile row = TMEM lane
+    const int i = r / a.G, hg = r % a.G;
+    const bool row_ok = i < nqv;
+    const int qpos = a.P0 + q0 + i;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint8_t* prow = smem + Cf::P_OFF + r * 128;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (*abort_flag || !mbar_wait_bounded(&s_full[st], (j >> 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tmem + st * 128 + lane_off + c * 32, sv + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      // mask + scale; whole-tile visibility is uniform for the CTA
+      const int j0 = (t_first + j) * Cf::BK;
+      const bool all_vis = j0 + Cf::BK - 1 <= p_lo && (a.window <= 0 || p_hi - j0 < a.window);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = __uint_as_float(sv[c]) * a.scale_log2;
+        if (!all_vis) {
+          const int rel = qpos - (j0 + c);
+          const bool vis = row_ok && rel >= 0 && (a.window <= 0 || rel < a.window);
+          v = vis ? v : -INFINITY;
+        } else if (!row_ok) {
+          v = -INFINITY;
+        }
+        sv[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      float scale_o = 1.f;
+      bool rescale = false;
+      if (mx > m_run + 8.0f) {                     // stale max kept unless it grows by > 2^8
+        scale_o = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+        rescale = j > 0;
+        l_run *= scale_o;
+        m_run = mx;
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      // P buffer and O are free once the previous PV MMA completed
+      if (j > 0 && !mbar_wait_bounded(o_done, (j - 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32_nowait(tmem + 256 + lane_off + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * scale_o);
+          tmem_st32(tmem + 256 + lane_off + c * 32, ov);
+        }
+        tmem_wait_st();
+      }
+      float ls = 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {                // 16 chunks of 8 keys
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(__uint_as_float(sv[q * 8 + e]) - m_use);
+          ls += p[e];
+        }
+        uint4 pk;
+        pk.x = pack_bf16x2(p[0], p[1]);
+        pk.y = pack_bf16x2(p[2], p[3]);
+        pk.z = pack_bf16x2(p[4], p[5]);
+        pk.w = pack_bf16x2(p[6], p[7]);
+        const int region = q >> 3, chunk = q & 7;
+        *reinterpret_cast<uint4*>(prow + region * Cf::HALF + ((chunk ^ (r & 7)) << 4)) = pk;
+      }
+      l_run += ls;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // final: O / l * gate
+    if (ok && ntiles > 0 && !*abort_flag &&
+        mbar_wait_bounded(o_done, (ntiles - 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      const long long row = (long long)b * a.C + q0 + i;
+      const long long base = row * a.n_q * 128 + (long long)(kvh * a.G + hg) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32_nowait(tmem + 256 + lane_off + c * 32, ov);
+        tmem_wait_ld();
+        if (!row_ok) continue;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const uint4 gr = *reinterpret_cast<const uint4*>(a.gate + base + c * 32 + e);
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
+          uint4 o;
+          uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 gf = __bfloat1622float2(g2[u]);
+            op[u] = pack_bf16x2(__uint_as_float(ov[e + 2 * u]) * inv * gf.x,
+                                __uint_as_float(ov[e + 2 * u + 1]) * inv * gf.y);
+          }
+          *reinterpret_cast<uint4*>(a.out + base + c * 32 + e) = o;
+        }
+      }
+    } else if (!ok) {
+      *abort_flag = 1;
+    }
+  }
+
+  if (*abort_flag) {
+    for (int k = 0; k < 64; ++k) __nanosleep(1000);   // let in-flight copies land
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace dory

@@ -27,9 +27,11 @@
 
 #include "dory.h"
 #include "attn.cuh"
+#include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
 #include "rowops.cuh"
+#include "decode_mk.cuh"
 
 using namespace dory;
 
@@ -42,7 +44,7 @@ constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 
 struct WsLayout {
   size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, gy, dec_o,
-      dec_ml, dec_cnt, parts, total;
+      dec_ml, dec_cnt, parts, mk_tab, mk_bar, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -79,6 +81,9 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.dec_o = take((size_t)max_batch * c.n_q * kDecMaxSplits * c.head_dim * 4);
   L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
   L.dec_cnt = take((size_t)max_batch * c.n_kv * 4);   // split tickets, zero between launches
+  // persistent decode kernel: per-layer table, grid-barrier words + abort flag
+  L.mk_tab = take((size_t)(c.n_in + c.n_rec + c.n_out) * sizeof(MkLayer));
+  L.mk_bar = take(4 * sizeof(unsigned));
   // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
   if (max_batch > kGemvMaxM) {
     const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
@@ -160,6 +165,22 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 tensor [d2][d1][d0] (d0 contiguous, strides s1 / s2 elements), loaded
+// as boxes {64, box1, box2} with the 128-byte swizzle.
+bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t s1, uint64_t s2, uint32_t box1, uint32_t box2) {
+  if (!get_encoder()) return false;
+  if (((uintptr_t)base & 15) || (s1 * 2) % 16 || (s2 * 2) % 16) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1 * 2, s2 * 2};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launch with programmatic stream serialisation (see pdl_wait in ptx.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -178,6 +199,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 int g_num_sms = 0;
+bool g_debug_tc_attn = true;   // dory_debug_attention: tensor-core prefill kernel where it applies
 int num_sms() {
   if (g_num_sms == 0) {
     int dev = 0;
@@ -226,6 +248,55 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
   const int G = a.n_q / a.n_kv, BQ = AttnCfg<DH>::BR / G;
   dim3 grid((a.C + BQ - 1) / BQ, a.n_kv, B);
   return launch_k(attn_prefill_kernel<DH>, grid, dim3(128), AttnCfg<DH>::SMEM, st, a) ==
+                 cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
+// Prefill attention on tcgen05 (attn_tc.cuh) when its tile rules hold:
+// head_dim 128, 128 / G query positions per CTA, key tiles of 128 aligned
+// positions that never mix cached and current keys (P0 % 128 == 0) and never
+// wrap the ring (window and ring size multiples of 128, or a ring that is
+// not full).  Returns DORY_EUNSUPPORTED otherwise (the caller then runs the
+// mma.sync kernel).  cache_rows = rows of the cache block ([batch][n_kv][S]).
+int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows, int* status,
+                   cudaStream_t st) {
+  const int G = aa.n_q / aa.n_kv;
+  if (head_dim != 128 || G < 1 || 128 % G || aa.C < 2 || aa.P0 % 128) return DORY_EUNSUPPORTED;
+  if (aa.window > 0 && aa.window % 128) return DORY_EUNSUPPORTED;
+  if (aa.P0 > 0 && aa.window > 0 && aa.S % 128 && aa.S < aa.P0) return DORY_EUNSUPPORTED;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)AttnTcCfg::SMEM) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  const long long tok = (long long)B * aa.C;
+  CUtensorMap tq, tk, tv, tkc, tvc;
+  const __nv_bfloat16* kc = aa.k_cache ? aa.k_cache : aa.k_cur;
+  const __nv_bfloat16* vc = aa.v_cache ? aa.v_cache : aa.v_cur;
+  const uint64_t crow = aa.k_cache ? (uint64_t)cache_rows : (uint64_t)tok * aa.n_kv;
+  if (!encode_bf16_3d(&tq, aa.q, 128, aa.n_q, tok, 128, (uint64_t)aa.n_q * 128, G, 128 / G) ||
+      !encode_bf16_3d(&tk, aa.k_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, 128) ||
+      !encode_bf16_3d(&tv, aa.v_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, 128) ||
+      !encode_bf16(&tkc, kc, crow, 128, 128, 128) || !encode_bf16(&tvc, vc, crow, 128, 128, 128))
+    return DORY_ECUDA;
+  AttnTcArgs a{};
+  a.C = aa.C;
+  a.P0 = aa.P0;
+  a.S = aa.S;
+  a.n_kv = aa.n_kv;
+  a.G = G;
+  a.window = aa.window;
+  a.scale_log2 = aa.scale_log2;
+  a.gate = aa.gate;
+  a.out = aa.out;
+  a.n_q = aa.n_q;
+  a.status = status;
+  const int QP = 128 / G;
+  dim3 grid((aa.C + QP - 1) / QP, aa.n_kv, B);
+  return launch_k(attn_tc_kernel, grid, dim3(192), AttnTcCfg::SMEM, st, tq, tk, tv, tkc, tvc, a) ==
                  cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
@@ -320,6 +391,39 @@ int dec_attn(const DecAttnArgs& a, int B, int head_dim, cudaStream_t st) {
   return DORY_EUNSUPPORTED;
 }
 
+// Persistent decode-step kernel (see decode_mk.cuh): cooperative launch of
+// one CTA per SM.  Returns DORY_EUNSUPPORTED when the kernel cannot be
+// co-resident on every SM (the caller then runs the per-kernel path).
+template <int MM, int DH>
+int launch_mk(const MkArgs& a, cudaStream_t st) {
+  constexpr int smem = MkAttnCfg<DH>::SMEM > kGemvMaxM * kMkMaxD * 2 ? MkAttnCfg<DH>::SMEM
+                                                                      : kGemvMaxM * kMkMaxD * 2;
+  static int ok = -1;
+  if (ok < 0) {
+    int per_sm = 0;
+    ok = cudaFuncSetAttribute(decode_step_kernel<MM, DH>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<MM, DH>,
+                                                               kMkThreads, smem) == cudaSuccess &&
+                 per_sm >= 1
+             ? 1
+             : 0;
+  }
+  if (!ok) return DORY_EUNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kMkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<MM, DH>, a) == cudaSuccess ? DORY_OK
+                                                                                : DORY_ECUDA;
+}
+
 // Split-KV decode attention: partial kernel + combine.
 template <int DH>
 int launch_decode_attn(DecodeArgs a, int B, const __nv_bfloat16* gate, __nv_bfloat16* out,
@@ -365,6 +469,9 @@ struct dory_model {
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
   int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
+  bool use_mk = false; // decode steps of <= kGemvMaxM sequences as one persistent kernel
+  bool use_tc_attn = true;  // prefill attention on tcgen05 where its tile rules hold
+  bool next_done = false;  // the last step also wrote the greedy tokens
   int launches = 0;
   // optional per-launch event timing
   bool prof_on = false;
@@ -753,10 +860,14 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     aa.n_kv = c.n_kv;
     aa.window = full ? 0 : c.window;
     aa.scale_log2 = attn_scale_log2(c);
-    int arc = DORY_EUNSUPPORTED;
-    if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
-    if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
-    if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
+    int arc = m->use_tc_attn ? launch_attn_tc(aa, B, c.head_dim,
+                                              (long long)m->max_batch * c.n_kv * S, status, st)
+                             : DORY_EUNSUPPORTED;
+    if (arc == DORY_EUNSUPPORTED) {
+      if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
+      if (c.head_dim == 64) arc = launch_attn<64>(aa, B, st);
+      if (c.head_dim == 128) arc = launch_attn<128>(aa, B, st);
+    }
     DORY_TRY(pe(m, st, arc));
     // KV write: the last min(C, S) positions of the call
     if (store) {
@@ -866,7 +977,9 @@ int boundary(dory_model* m, int M, int mode, StepState& s, cudaStream_t st) {
 // Logit rows: if logits != null, rows (b, t) for t >= C - n_logit_rows are
 // written to logits + (b * ld_seq + t_out0 + t - (C - n_logit_rows)) * V.
 int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int k,
-             float* logits, long long ld_seq, int t_out0, int n_logit_rows, cudaStream_t st) {
+             float* logits, long long ld_seq, int t_out0, int n_logit_rows, cudaStream_t st,
+             int32_t* next_tok = nullptr) {
+  m->next_done = false;
   const dory_config& c = m->cfg;
   const int M = B * C;
   const int P0 = m->len;
@@ -893,6 +1006,62 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
                         cudaSuccess
                     ? DORY_OK
                     : DORY_ECUDA));
+  }
+  if (decode && m->use_mk && c.d <= kMkMaxD) {
+    // one persistent kernel for the whole step (embedding .. greedy token)
+    MkArgs a{};
+    a.layers = wsp<MkLayer>(m, m->L.mk_tab);
+    a.n_in = c.n_in;
+    a.n_rec = c.n_rec;
+    a.n_out = c.n_out;
+    a.d = c.d;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.ffn = c.ffn;
+    a.vocab = c.vocab;
+    a.window = c.window;
+    a.B = B;
+    a.P0 = P0;
+    a.k = k;
+    a.per_loop = m->cache_mode == DORY_CACHE_PER_LOOP ? 1 : 0;
+    a.scale_log2 = attn_scale_log2(c);
+    a.tokens = tokens;
+    a.embed_in = static_cast<const __nv_bfloat16*>(m->embed_in);
+    a.embed_out = static_cast<const __nv_bfloat16*>(m->embed_out);
+    a.s_z = m->s_z;
+    a.logits = n_logit_rows > 0 ? logits : nullptr;
+    a.next = a.logits ? next_tok : nullptr;
+    a.h0 = wsp<float>(m, m->L.h32);
+    a.h1 = wsp<float>(m, m->L.h32b);
+    a.x32 = wsp<float>(m, m->L.x32);
+    a.hb = wsp<__nv_bfloat16>(m, m->L.hb);
+    a.y32 = wsp<float>(m, m->L.y32);
+    a.gy = wsp<float>(m, m->L.gy);
+    a.att = wsp<__nv_bfloat16>(m, m->L.att);
+    a.mo = wsp<__nv_bfloat16>(m, m->L.m);
+    a.rope_swa = c.rope ? wsp<float2>(m, m->L.rope_swa) : nullptr;
+    a.rope_full = c.rope ? wsp<float2>(m, m->L.rope_full) : nullptr;
+    a.part_o = wsp<float>(m, m->L.dec_o);
+    a.part_ml = wsp<float>(m, m->L.dec_ml);
+    a.counter = wsp<int>(m, m->L.dec_cnt);
+    unsigned* bar = wsp<unsigned>(m, m->L.mk_bar);
+    a.bar = bar;
+    a.abort_flag = reinterpret_cast<int*>(bar + 2);
+    a.status = status;
+    int rc = DORY_EUNSUPPORTED;
+    pb(m, DORY_K_DECODE_STEP, st);
+    if (c.head_dim == 128) rc = M <= 4 ? launch_mk<4, 128>(a, st) : launch_mk<16, 128>(a, st);
+    if (c.head_dim == 64) rc = M <= 4 ? launch_mk<4, 64>(a, st) : launch_mk<16, 64>(a, st);
+    if (c.head_dim == 32) rc = M <= 4 ? launch_mk<4, 32>(a, st) : launch_mk<16, 32>(a, st);
+    if (rc != DORY_EUNSUPPORTED) {
+      DORY_TRY(pe(m, st, rc));
+      m->len += C;
+      m->last_rows = M;
+      m->hsel_last = 0;
+      m->next_done = a.next != nullptr;
+      return DORY_OK;
+    }
+    m->use_mk = false;                     // not co-resident here: per-kernel path
   }
   StepState s;
   pb(m, DORY_K_EMBED, st);
@@ -1068,10 +1237,31 @@ int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes, i
   m->batch = 0;
   m->last_rows = 0;
   m->hsel_last = 0;
-  // status word and split tickets start at zero (the tickets return to zero
-  // after every launch that uses them)
-  if (cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
+  // per-layer table of the persistent decode kernel
+  std::vector<MkLayer> tab(L);
+  for (int l = 0; l < L; ++l) {
+    const dory_layer_weights& w = m->layers[l];
+    MkLayer& t = tab[l];
+    t.w_qkvg = static_cast<const __nv_bfloat16*>(w.w_qkvg);
+    t.w_o = static_cast<const __nv_bfloat16*>(w.w_o);
+    t.w_upgate = static_cast<const __nv_bfloat16*>(w.w_upgate);
+    t.w_down = static_cast<const __nv_bfloat16*>(w.w_down);
+    t.alpha_attn = w.alpha_attn;
+    t.alpha_mlp = w.alpha_mlp;
+    t.s_qk = w.s_qk;
+    t.kv = reinterpret_cast<__nv_bfloat16*>(
+        m->kv + kv_offset(c, max_batch, max_ctx, k_max, cache_mode, l, 0, 0));
+    t.S = slots_of(c, l, max_ctx);
+    t.blk = (long long)t.S * c.n_kv * c.head_dim * max_batch;
+    t.full = layer_full(c, l) ? 1 : 0;
+  }
+  // status word, split tickets and barrier words start at zero (tickets and
+  // barrier arrivals return to zero after every launch that uses them)
+  if (cudaMemcpy(m->ws + m->L.mk_tab, tab.data(), tab.size() * sizeof(MkLayer),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
       cudaMemsetAsync(m->ws + m->L.dec_cnt, 0, (size_t)max_batch * c.n_kv * 4, 0) != cudaSuccess ||
+      cudaMemsetAsync(m->ws + m->L.mk_bar, 0, 4 * sizeof(unsigned), 0) != cudaSuccess ||
       cudaStreamSynchronize(0) != cudaSuccess)
     return DORY_ECUDA;
   return DORY_OK;
@@ -1118,9 +1308,9 @@ int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_m
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   m->launches = 0;
   m->batch = B;
-  const int r = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st);
+  const int r = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st, next);
   if (r != DORY_OK) return r;
-  if (next) {
+  if (next && !m->next_done) {
     pb(m, DORY_K_ARGMAX, st);
     return pe(m, st,
               launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits,
@@ -1134,6 +1324,16 @@ int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_m
 int dory_length(const dory_t* m, int* out) {
   if (!m || !out) return DORY_EINVAL;
   *out = m->len;
+  return DORY_OK;
+}
+
+int dory_set_length(dory_t* m, int B, int len) {
+  if (!m) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (B <= 0 || len < 0) return DORY_EINVAL;
+  if (B > m->max_batch || len > m->max_ctx) return DORY_ECAPACITY;
+  m->len = len;
+  m->batch = len > 0 ? B : 0;
   return DORY_OK;
 }
 
@@ -1213,6 +1413,12 @@ int dory_device_status(dory_t* m, int* out, void* stream) {
     return DORY_ECUDA;
   if (cudaMemsetAsync(m->ws + m->L.status, 0, sizeof(int), st) != cudaSuccess) return DORY_ECUDA;
   *out = v;
+  return DORY_OK;
+}
+
+int dory_set_persistent_decode(dory_t* m, int enable) {
+  if (!m || (enable != 0 && enable != 1)) return DORY_EINVAL;
+  m->use_mk = enable != 0;
   return DORY_OK;
 }
 
@@ -1320,10 +1526,23 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
     if (cudaMemsetAsync(da.counter, 0, (size_t)B * n_kv * 4, st) != cudaSuccess) return DORY_ECUDA;
     return dec_attn<false>(da, B, head_dim, st);
   }
+  if (g_debug_tc_attn) {
+    const int rc = launch_attn_tc(a, B, head_dim, (long long)B * n_kv * a.S, nullptr, st);
+    if (rc != DORY_EUNSUPPORTED) return rc;
+  }
   if (head_dim == 32) return launch_attn<32>(a, B, st);
   if (head_dim == 64) return launch_attn<64>(a, B, st);
   if (head_dim == 128) return launch_attn<128>(a, B, st);
   return DORY_EUNSUPPORTED;
+}
+
+int dory_set_tc_attention(dory_t* m, int enable) {
+  if (enable != 0 && enable != 1) return DORY_EINVAL;
+  if (m)
+    m->use_tc_attn = enable != 0;
+  else
+    g_debug_tc_attn = enable != 0;
+  return DORY_OK;
 }
 
 }  // extern "C"

@@ -156,6 +156,36 @@ def make_weights_lazy(shape: Shape, shape_id: int | None = None) -> dict:
     return w
 
 
+def make_weights_torch(shape: Shape, device="cuda", seed: int = 0) -> dict:
+    """Weights with the same distribution as make_weights (Gaussian
+    N(0, 0.02^2), unit vectors along d, bf16), drawn on the GPU by torch's
+    seeded generator: a fast stand-in for timing shapes too large to draw on
+    the host.  Values differ from make_weights'; no parity check uses them."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    d, hq, hk, F = shape.d, shape.n_q * shape.head_dim, shape.n_kv * shape.head_dim, shape.ffn
+
+    def unit_rows(rows, cols):
+        w = torch.randn(rows, cols, device=device, generator=g, dtype=torch.float32) * 0.02
+        return (w / w.norm(dim=1, keepdim=True)).to(torch.bfloat16)
+
+    out = {"embed_in": unit_rows(shape.vocab, d), "embed_out": unit_rows(shape.vocab, d),
+           "s_z": torch.ones(shape.vocab, device=device)}
+
+    def layer(l):
+        lw = {n: unit_rows(r, d) for n, r in (("w_q", hq), ("w_k", hk), ("w_v", hk), ("w_g", hq),
+                                                ("w_up", F), ("w_sl", F))}
+        lw["w_o"] = unit_rows(hq, d).t().contiguous()
+        lw["w_down"] = unit_rows(F, d).t().contiguous()
+        lw["alpha_attn"] = torch.full((d,), shape.alpha_attn, device=device)
+        lw["alpha_mlp"] = torch.full((d,), shape.alpha_mlp, device=device)
+        lw["s_qk"] = torch.full((shape.head_dim,), shape.s_qk, device=device)
+        return lw
+
+    out["layers"] = (layer(l) for l in range(shape.n_layers))
+    return out
+
+
 def tokens(shape: Shape, batch: int, length: int, seed: int = 0) -> np.ndarray:
     """Token ids uniform over the vocabulary, int32 [batch, length]."""
     rng = np.random.default_rng(seed)

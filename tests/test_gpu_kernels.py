@@ -132,3 +132,52 @@ def test_attention_matches_oracle(dev, dh, nq, nkv, W, P0, C):
                                  np.arange(L), W, W <= 0, math.sqrt(dh))
             want = o * gate[b].reshape(C, nq, dh)[:, h]
             np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
+
+
+# Shapes on the tcgen05 prefill attention (head_dim 128, key tiles of 128
+# aligned positions): ragged query blocks, cached + current keys, windows.
+TC_CASES = [(0, 0, 200), (128, 0, 300), (0, 256, 130), (256, 384, 200), (512, 128, 77),
+            (128, 128, 2), (0, 0, 2)]
+
+
+@pytest.mark.parametrize("nq,nkv", [(4, 2), (8, 2), (16, 4)])
+@pytest.mark.parametrize("W,P0,C", TC_CASES)
+def test_tc_attention_mask_is_exact(dev, nq, nkv, W, P0, C):
+    """The equal-score / one-hot-value probe on the tensor-core kernel."""
+    import torch
+    B, dh = 2, 128
+    out, *_ = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 0, uniform=True)
+    for t in range(C):
+        p = P0 + t
+        lo = 0 if W <= 0 else max(0, p - W + 1)
+        n = p - lo + 1
+        cnt = np.zeros(dh)
+        for j in range(lo, p + 1):
+            cnt[j % dh] += 1
+        want = (cnt.astype(np.float32) * (np.float32(1.0) / np.float32(n))).astype(np.float32)
+        want_bf = torch.tensor(want).to(torch.bfloat16).float().numpy()
+        for b in range(B):
+            for h in range(nq):
+                assert np.array_equal(out[b, t, h], want_bf), (t, b, h)
+
+
+@pytest.mark.parametrize("nq,nkv", [(8, 2), (16, 4)])
+@pytest.mark.parametrize("W,P0,C", TC_CASES)
+def test_tc_attention_matches_oracle_and_mma_sync(dev, nq, nkv, W, P0, C):
+    B, dh = 2, 128
+    out, q, k_all, v_all, gate = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 2)
+    G = nq // nkv
+    L = P0 + C
+    qpos = np.arange(P0, L)
+    for b in range(B):
+        for h in range(nq):
+            o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G], qpos,
+                                 np.arange(L), W, W <= 0, math.sqrt(dh))
+            want = o * gate[b].reshape(C, nq, dh)[:, h]
+            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
+    dev.set_debug_tc_attention(False)
+    try:
+        ref, *_ = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 2)
+    finally:
+        dev.set_debug_tc_attention(True)
+    np.testing.assert_allclose(out, ref, atol=2e-2, rtol=2e-2)

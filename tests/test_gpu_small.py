@@ -5,7 +5,8 @@
   (4 x 2048 tokens, one chunk, last-loop cache): the GPU processes the whole
   batch; sequences are independent, so two sampled sequences are checked
   against the float32 oracle run on those sequences alone, at every position.
-* Decode steps after a short prefill: the few-row GEMV path with split K
+* Decode steps after a short prefill, through the persistent decode-step
+  kernel and through the per-kernel path: few-row GEMVs with split K
   segments and the fused SwiGLU pair, and the split-key decode attention.
 Tolerances as in test_gpu_parity."""
 import numpy as np
@@ -54,13 +55,15 @@ def test_full_size_prefill_sampled_sequences(dev, weights, k):
 
 
 @pytest.mark.parametrize("k,mode", [(2, oracle.LAST_LOOP), (3, oracle.PER_LOOP)])
-def test_decode_steps(dev, weights, k, mode):
+@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "perkernel"])
+def test_decode_steps(dev, weights, k, mode, persistent):
     sh = synth.SMALL
     B, T, D = 3, 96, 3
     prompt = synth.tokens(sh, B, T, seed=7)
     dec = synth.tokens(sh, B, D, seed=8)
     o = oracle.Oracle(sh, weights, dtype=np.float32)
     m = dev.Model(sh, weights, max_batch=B, max_ctx=T + D, max_chunk=T, k_max=k, cache_mode=mode)
+    m.set_persistent_decode(persistent)
     r = o.prefill(prompt, k, mode)
     lg = m.prefill(_tok(prompt), k, mode)
     check_logits(lg.cpu().numpy(), r["logits"][:, -1])
