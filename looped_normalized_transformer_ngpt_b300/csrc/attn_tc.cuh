@@ -224,9 +224,13 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* prow = smem + Cf::P_OFF + r * 128;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    // tcgen05.ld / tcgen05.st are warp-collective: every decision that guards
+    // them (abort, rescale) is made uniform across the warp.
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
-      if (*abort_flag || !mbar_wait_bounded(&s_full[st], (j >> 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+      bool w_ok = !*abort_flag &&
+                  mbar_wait_bounded(&s_full[st], (j >> 1) & 1, a.status, DEV_ATTN_SOFTMAX);
+      if (!__all_sync(0xffffffffu, w_ok)) {
         ok = false;
         break;
       }
@@ -264,12 +268,14 @@ __global__ void __launch_bounds__(192, 1)
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       // P buffer and O are free once the previous PV MMA completed
-      if (j > 0 && !mbar_wait_bounded(o_done, (j - 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+      w_ok = j == 0 || mbar_wait_bounded(o_done, (j - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
+      if (!__all_sync(0xffffffffu, w_ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (rescale) {
+      if (__any_sync(0xffffffffu, rescale)) {      // lanes without a rescale scale by 1
+        if (!rescale) scale_o = 1.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -304,8 +310,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(p_full);
     }
     // final: O / l * gate
-    if (ok && ntiles > 0 && !*abort_flag &&
-        mbar_wait_bounded(o_done, (ntiles - 1) & 1, a.status, DEV_ATTN_SOFTMAX)) {
+    bool fin = ok && ntiles > 0 && !*abort_flag &&
+               mbar_wait_bounded(o_done, (ntiles - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
+    fin = __all_sync(0xffffffffu, fin);
+    if (fin) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
       const long long row = (long long)b * a.C + q0 + i;
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(192, 1)
           *reinterpret_cast<uint4*>(a.out + base + c * 32 + e) = o;
         }
       }
-    } else if (!ok) {
+    } else {
       *abort_flag = 1;
     }
   }

@@ -371,7 +371,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI)) {
+      // tcgen05.ld is warp-collective: the warp proceeds or leaves as a whole
+      const bool ready = mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI);
+      if (!__all_sync(0xffffffffu, ready)) {
         *abort_flag = 1;
         break;
       }
