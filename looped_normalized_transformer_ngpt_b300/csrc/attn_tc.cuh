@@ -11,21 +11,23 @@
 //
 // One CTA = (block of 128 / G query positions, kv head, sequence): its 128
 // rows are (position, head-in-group) pairs, so one K/V tile serves all G
-// heads.  Warp roles (192 threads):
+// heads.  112 KB of shared memory and 256 TMEM columns, so two CTAs share an
+// SM and the tensor core works for one while the other runs its softmax.
+// Warp roles (192 threads):
 //   warp 0    TMA producer: the Q tile once (3-D box: 64 dims x G heads x
-//             128/G positions, two boxes for the 128 dims), then 128-key K and
+//             128/G positions, two boxes for the 128 dims), then 64-key K and
 //             V tiles into a 2-stage ring (128-byte swizzle);
-//   warp 1    TMEM owner and MMA issuer: S_j = Q K_j^T (M = N = 128, K = 128)
-//             into one of two TMEM S buffers, and O += P_j V_j (V as an MN-major
-//             operand) into the TMEM O accumulator;
+//   warp 1    TMEM owner and MMA issuer: S_j = Q K_j^T (M = 128, N = 64,
+//             K = 128) into one of two TMEM S buffers, and O += P_j V_j (V as an
+//             MN-major operand) into the TMEM O accumulator;
 //   warps 2-5 softmax, one row per thread: S row from TMEM, mask, running max,
 //             P = exp2(S - max) written to shared memory as the bf16 K-major
 //             A operand of the PV MMA; O is rescaled in TMEM only when the
 //             running max rises by more than 8 (log2 units) - otherwise the
 //             stale max stays exact, since the same max scales P and the row
 //             sum; final O / sum * gate from TMEM to global.
-// Key tiles are aligned to 128 positions and never mix cached and current
-// keys (the launcher requires P0 % 128 == 0 and 128-aligned ring sizes).
+// Key tiles are aligned to 64 positions and never mix cached and current
+// keys (the launcher requires P0 % 64 == 0 and 64-aligned ring sizes).
 // Every wait is bounded (status word + orderly exit).
 #pragma once
 #include "ptx.cuh"
@@ -44,15 +46,17 @@ struct AttnTcArgs {
 };
 
 struct AttnTcCfg {
-  static constexpr int BK = 128;                 // keys per tile
-  static constexpr int HALF = 128 * 128;         // one 64-dim half of a 128-row tile (bytes)
-  static constexpr int TILE = 2 * HALF;          // 128 rows x 128 dims bf16
+  static constexpr int BK = 64;                  // keys per tile
+  static constexpr int QHALF = 128 * 128;        // Q: one 64-dim half of the 128 rows (bytes)
+  static constexpr int KVHALF = BK * 128;        // K or V: one 64-dim half of the BK rows
+  static constexpr int KVTILE = 2 * KVHALF;
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = TILE;             // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * TILE; // 2 stages
-  static constexpr int P_OFF = V_OFF + 2 * TILE;
-  static constexpr int BAR_OFF = P_OFF + TILE;
-  static constexpr size_t SMEM = BAR_OFF + 256 + 1024;   // + barriers + alignment slack
+  static constexpr int K_OFF = 2 * QHALF;          // 2 stages
+  static constexpr int V_OFF = K_OFF + 2 * KVTILE; // 2 stages
+  static constexpr int P_OFF = V_OFF + 2 * KVTILE; // 128 rows x 64 keys bf16
+  static constexpr int BAR_OFF = P_OFF + 128 * BK * 2;
+  static constexpr size_t SMEM = BAR_OFF + 256;    // two CTAs fit on one SM
+  static constexpr uint32_t TMEM_COLS = 256;       // S0 | S1 (64 each) | O (128)
 };
 
 // tensor maps: q (3-D: dim, head, token), k/v current (3-D: dim, kv head,
@@ -65,27 +69,32 @@ __device__ __forceinline__ void attn_tc_load_kv(uint8_t* dst_k, uint8_t* dst_v,
   if (FROM_CACHE) {
     const int row = (b * a.n_kv + kvh) * a.S + (j0 % a.S);
     tma_load_2d(dst_k, tk, bar, 0, row);
-    tma_load_2d(dst_k + AttnTcCfg::HALF, tk, bar, 64, row);
+    tma_load_2d(dst_k + AttnTcCfg::KVHALF, tk, bar, 64, row);
     tma_load_2d(dst_v, tv, bar, 0, row);
-    tma_load_2d(dst_v + AttnTcCfg::HALF, tv, bar, 64, row);
+    tma_load_2d(dst_v + AttnTcCfg::KVHALF, tv, bar, 64, row);
   } else {
     const int tok = b * a.C + (j0 - a.P0);
     tma_load_3d(dst_k, tk, bar, 0, kvh, tok);
-    tma_load_3d(dst_k + AttnTcCfg::HALF, tk, bar, 64, kvh, tok);
+    tma_load_3d(dst_k + AttnTcCfg::KVHALF, tk, bar, 64, kvh, tok);
     tma_load_3d(dst_v, tv, bar, 0, kvh, tok);
-    tma_load_3d(dst_v + AttnTcCfg::HALF, tv, bar, 64, kvh, tok);
+    tma_load_3d(dst_v + AttnTcCfg::KVHALF, tv, bar, 64, kvh, tok);
   }
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_kc,
                    const __grid_constant__ CUtensorMap tm_vc, const AttnTcArgs a) {
   using Cf = AttnTcCfg;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  // the 128-byte swizzle atoms need 1024-byte alignment; the dynamic segment
+  // of this kernel (no static shared memory) starts there
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0 && a.status) atomicCAS(a.status, 0, DEV_ATTN_ALIGN);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;    // [2]
@@ -128,21 +137,21 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tm_kc);
     tma_prefetch_desc(&tm_vc);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc(tmem_slot, Cf::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, O: 256..383
+  const uint32_t tmem = *tmem_slot;   // S0: cols 0..63, S1: 64..127, O: 128..255
   pdl_wait();
   pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, Cf::TILE);
+      mbar_arrive_expect_tx(q_full, 2 * Cf::QHALF);
       const int tok = b * a.C + q0;
       tma_load_3d(smem + Cf::Q_OFF, &tm_q, q_full, 0, kvh * a.G, tok);
-      tma_load_3d(smem + Cf::Q_OFF + Cf::HALF, &tm_q, q_full, 64, kvh * a.G, tok);
+      tma_load_3d(smem + Cf::Q_OFF + Cf::QHALF, &tm_q, q_full, 64, kvh * a.G, tok);
       for (int j = 0; j < ntiles && !*abort_flag; ++j) {
         const int st = j & 1;
         if (j >= 2 && !mbar_wait_bounded(&kv_empty[st], ((j >> 1) - 1) & 1, a.status,
@@ -151,9 +160,9 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         const int j0 = (t_first + j) * Cf::BK;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::TILE);
-        uint8_t* dk = smem + Cf::K_OFF + st * Cf::TILE;
-        uint8_t* dv = smem + Cf::V_OFF + st * Cf::TILE;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::KVTILE);
+        uint8_t* dk = smem + Cf::K_OFF + st * Cf::KVTILE;
+        uint8_t* dv = smem + Cf::V_OFF + st * Cf::KVTILE;
         if (j0 < a.P0)
           attn_tc_load_kv<true>(dk, dv, &tm_kc, &tm_vc, &kv_full[st], j0, b, kvh, a);
         else
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = tc_idesc_bf16(128, 128);
+      constexpr uint32_t idesc_s = tc_idesc_bf16(128, Cf::BK);
       constexpr uint32_t idesc_o = tc_idesc_bf16(128, 128) | (1u << 16);   // B (V) MN-major
       const uint32_t q_addr = smem_u32(smem + Cf::Q_OFF);
       const uint32_t p_addr = smem_u32(smem + Cf::P_OFF);
@@ -174,11 +183,12 @@ __global__ void __launch_bounds__(192, 1)
         if (j >= 2 && !mbar_wait_bounded(&s_free[st], ((j >> 1) - 1) & 1, a.status, DEV_ATTN_MMA))
           return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + Cf::K_OFF + st * Cf::TILE);
+        const uint32_t k_addr = smem_u32(smem + Cf::K_OFF + st * Cf::KVTILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * Cf::HALF + (kk & 3) * 32;
-          tc_mma_bf16(tmem + st * 128, tc_sdesc_sw128(q_addr + off), tc_sdesc_sw128(k_addr + off),
+          const uint32_t qo = (kk >> 2) * Cf::QHALF + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * Cf::KVHALF + (kk & 3) * 32;
+          tc_mma_bf16(tmem + st * Cf::BK, tc_sdesc_sw128(q_addr + qo), tc_sdesc_sw128(k_addr + ko),
                       idesc_s, kk);
         }
         tc_commit(&s_full[st]);
@@ -196,13 +206,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const int st = j & 1;
-        const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::TILE);
+        const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::KVTILE);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major)
-          const uint32_t pa = p_addr + (kk >> 2) * Cf::HALF + (kk & 3) * 32;
-          tc_mma_bf16(tmem + 256, tc_sdesc_sw128(pa),
-                      tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::HALF, 1024), idesc_o,
+        for (int kk = 0; kk < Cf::BK / 16; ++kk) {
+          // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major:
+          // the two 64-dim halves KVHALF apart, 8-key groups 1024 B apart)
+          tc_mma_bf16(tmem + 2 * Cf::BK, tc_sdesc_sw128(p_addr + kk * 32),
+                      tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::KVHALF, 1024), idesc_o,
                       (j | kk) != 0);
         }
         tc_commit(&kv_empty[st]);
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool row_ok = i < nqv;
     const int qpos = a.P0 + q0 + i;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint8_t* prow = smem + Cf::P_OFF + r * 128;
+    uint8_t* prow = smem + Cf::P_OFF + r * (Cf::BK * 2);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     // tcgen05.ld / tcgen05.st are warp-collective: every decision that guards
@@ -235,19 +245,21 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sv[128];
+      uint32_t sv[Cf::BK];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tmem + st * 128 + lane_off + c * 32, sv + c * 32);
+      for (int c = 0; c < Cf::BK / 32; ++c)
+        tmem_ld32_nowait(tmem + st * Cf::BK + lane_off + c * 32, sv + c * 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_free[st]);
-      // mask + scale; whole-tile visibility is uniform for the CTA
+      // mask (raw scores; scale > 0 keeps the order); whole-tile visibility is
+      // uniform for the CTA.  Four partial maxima break the dependency chain.
       const int j0 = (t_first + j) * Cf::BK;
       const bool all_vis = j0 + Cf::BK - 1 <= p_lo && (a.window <= 0 || p_hi - j0 < a.window);
-      float mx = -INFINITY;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = __uint_as_float(sv[c]) * a.scale_log2;
+      for (int c = 0; c < Cf::BK; ++c) {
+        float v = __uint_as_float(sv[c]);
         if (!all_vis) {
           const int rel = qpos - (j0 + c);
           const bool vis = row_ok && rel >= 0 && (a.window <= 0 || rel < a.window);
@@ -256,8 +268,9 @@ __global__ void __launch_bounds__(192, 1)
           v = -INFINITY;
         }
         sv[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        mx4[c & 3] = fmaxf(mx4[c & 3], v);
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
       float scale_o = 1.f;
       bool rescale = false;
       if (mx > m_run + 8.0f) {                     // stale max kept unless it grows by > 2^8
@@ -279,31 +292,31 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
-          tmem_ld32_nowait(tmem + 256 + lane_off + c * 32, ov);
+          tmem_ld32_nowait(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * scale_o);
-          tmem_st32(tmem + 256 + lane_off + c * 32, ov);
+          tmem_st32(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
         }
         tmem_wait_st();
       }
-      float ls = 0.f;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {                // 16 chunks of 8 keys
+      for (int q = 0; q < Cf::BK / 8; ++q) {        // chunks of 8 keys
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(__uint_as_float(sv[q * 8 + e]) - m_use);
-          ls += p[e];
+          p[e] = exp2f(fmaf(__uint_as_float(sv[q * 8 + e]), a.scale_log2, -m_use));
+          ls4[e & 3] += p[e];
         }
         uint4 pk;
         pk.x = pack_bf16x2(p[0], p[1]);
         pk.y = pack_bf16x2(p[2], p[3]);
         pk.z = pack_bf16x2(p[4], p[5]);
         pk.w = pack_bf16x2(p[6], p[7]);
-        const int region = q >> 3, chunk = q & 7;
-        *reinterpret_cast<uint4*>(prow + region * Cf::HALF + ((chunk ^ (r & 7)) << 4)) = pk;
+        *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) = pk;
       }
+      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l_run += ls;
       fence_proxy_async_smem();
       tc_fence_before();
@@ -321,7 +334,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
-        tmem_ld32_nowait(tmem + 256 + lane_off + c * 32, ov);
+        tmem_ld32_nowait(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
         tmem_wait_ld();
         if (!row_ok) continue;
 #pragma unroll
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, Cf::TMEM_COLS);
   }
 }
 

@@ -254,17 +254,18 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
 }
 
 // Prefill attention on tcgen05 (attn_tc.cuh) when its tile rules hold:
-// head_dim 128, 128 / G query positions per CTA, key tiles of 128 aligned
-// positions that never mix cached and current keys (P0 % 128 == 0) and never
-// wrap the ring (window and ring size multiples of 128, or a ring that is
-// not full).  Returns DORY_EUNSUPPORTED otherwise (the caller then runs the
+// head_dim 128, 128 / G query positions per CTA, key tiles of 64 aligned
+// positions that never mix cached and current keys (P0 % 64 == 0) and never
+// wrap the ring (window and ring size multiples of 64, or a ring that is not
+// full).  Returns DORY_EUNSUPPORTED otherwise (the caller then runs the
 // mma.sync kernel).  cache_rows = rows of the cache block ([batch][n_kv][S]).
 int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows, int* status,
                    cudaStream_t st) {
+  constexpr int BK = AttnTcCfg::BK;
   const int G = aa.n_q / aa.n_kv;
-  if (head_dim != 128 || G < 1 || 128 % G || aa.C < 2 || aa.P0 % 128) return DORY_EUNSUPPORTED;
-  if (aa.window > 0 && aa.window % 128) return DORY_EUNSUPPORTED;
-  if (aa.P0 > 0 && aa.window > 0 && aa.S % 128 && aa.S < aa.P0) return DORY_EUNSUPPORTED;
+  if (head_dim != 128 || G < 1 || 128 % G || aa.C < 2 || aa.P0 % BK) return DORY_EUNSUPPORTED;
+  if (aa.window > 0 && aa.window % BK) return DORY_EUNSUPPORTED;
+  if (aa.P0 > 0 && aa.window > 0 && aa.S % BK && aa.S < aa.P0) return DORY_EUNSUPPORTED;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -278,9 +279,9 @@ int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows
   const __nv_bfloat16* vc = aa.v_cache ? aa.v_cache : aa.v_cur;
   const uint64_t crow = aa.k_cache ? (uint64_t)cache_rows : (uint64_t)tok * aa.n_kv;
   if (!encode_bf16_3d(&tq, aa.q, 128, aa.n_q, tok, 128, (uint64_t)aa.n_q * 128, G, 128 / G) ||
-      !encode_bf16_3d(&tk, aa.k_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, 128) ||
-      !encode_bf16_3d(&tv, aa.v_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, 128) ||
-      !encode_bf16(&tkc, kc, crow, 128, 128, 128) || !encode_bf16(&tvc, vc, crow, 128, 128, 128))
+      !encode_bf16_3d(&tk, aa.k_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, BK) ||
+      !encode_bf16_3d(&tv, aa.v_cur, 128, aa.n_kv, tok, 128, (uint64_t)aa.n_kv * 128, 1, BK) ||
+      !encode_bf16(&tkc, kc, crow, 128, 128, BK) || !encode_bf16(&tvc, vc, crow, 128, 128, BK))
     return DORY_ECUDA;
   AttnTcArgs a{};
   a.C = aa.C;

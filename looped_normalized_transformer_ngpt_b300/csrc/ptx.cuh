@@ -20,6 +20,7 @@ enum : int {
   DEV_ATTN_MMA = 0x42,
   DEV_ATTN_SOFTMAX = 0x43,
   DEV_ATTN_DRAIN = 0x44,
+  DEV_ATTN_ALIGN = 0x45,
 };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
