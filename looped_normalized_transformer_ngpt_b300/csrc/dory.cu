@@ -308,16 +308,22 @@ int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows
 // K, M and either Y/ldy/col_scale or (SwiGLU) pair_off/m_out/ldm.
 template <int MM, int J, bool SW, bool PRE>
 cudaError_t gemv_go(const GemvArgs& a, int grid, cudaStream_t st) {
-  const size_t smem = PRE ? (size_t)a.M * a.K * 2 : 0;
-  static bool attr = false;
-  if (PRE && !attr) {
+  const size_t smem = (PRE || a.stage_x) ? (size_t)a.M * a.K * 2 : 0;
+  static int per_sm = 0;
+  if (per_sm == 0) {
     if (cudaFuncSetAttribute(gemv_kernel<MM, J, SW, PRE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kGemvMaxM * kGemvPreMaxD * 2) != cudaSuccess)
-      return cudaErrorInvalidValue;
-    attr = true;
+                             kGemvStageMax) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<MM, J, SW, PRE>,
+                                                      kGemvThreads, kGemvStageMax) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
   }
-  return launch_k(gemv_kernel<MM, J, SW, PRE>, dim3(grid), dim3(kGemvThreads), smem, st, a);
+  // no more CTAs than are resident at once: a partial second wave would
+  // double the time of these latency-bound kernels (CTAs stride instead)
+  const int cap = per_sm * num_sms();
+  return launch_k(gemv_kernel<MM, J, SW, PRE>, dim3(grid < cap ? grid : cap), dim3(kGemvThreads),
+                  smem, st, a);
 }
 
 template <int MM, bool SW, bool PRE>
@@ -342,7 +348,8 @@ int launch_gemv(GemvArgs a, cudaStream_t st) {
   a.S = S;
   const int fpi = kGemvWarps / S;
   a.n_iters = (a.N + fpi - 1) / fpi;
-  const int grid = a.n_iters < 3 * num_sms() ? a.n_iters : 3 * num_sms();
+  a.stage_x = (!pre && (size_t)a.M * a.K * 2 <= (size_t)kGemvStageMax) ? 1 : 0;
+  const int grid = a.n_iters;
   cudaError_t e;
   if (a.M <= 4)
     e = sw ? (pre ? gemv_j<4, true, true>(a, J, grid, st) : gemv_j<4, true, false>(a, J, grid, st))

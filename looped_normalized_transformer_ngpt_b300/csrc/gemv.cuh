@@ -35,6 +35,7 @@ constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kGemvMaxK = kGemvWarps * 8 * 256;     // S <= 8 segments of J <= 8 chunks
 constexpr int kGemvPreMaxD = 2048;                  // PRE: d <= 2048 (8 chunks per lane)
+constexpr int kGemvStageMax = kGemvMaxM * kGemvPreMaxD * 2;   // shared-memory rows, bytes
 
 struct GemvArgs {
   const __nv_bfloat16* X;   // activations [M, ldx] (not PRE)
@@ -53,6 +54,7 @@ struct GemvArgs {
   const float* y_in;
   const float* alpha;
   float* h_out;             // written by CTA 0 (a different buffer from h_in)
+  int stage_x;              // not PRE: copy X to shared memory first (M * K * 2 bytes)
 };
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -140,7 +142,7 @@ __device__ __forceinline__ void gemv_pre_rows(const GemvArgs& a, __nv_bfloat16* 
 }
 
 // K must be a multiple of 8; X rows are 16-byte aligned.  Dynamic shared
-// memory (PRE only): M * K bf16.
+// memory (PRE, or stage_x): M * K bf16.
 template <int MM, int J, bool SWIGLU, bool PRE>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
   constexpr int R = SWIGLU ? 2 : 1;
@@ -174,9 +176,22 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
 
   const __nv_bfloat16* X = a.X;
   int ldx = a.ldx;
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(gemv_smem);
   if (PRE) {
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(gemv_smem);
     gemv_pre_rows(a, xs);
+    __syncthreads();
+    X = xs;
+    ldx = a.K;
+  } else if (a.stage_x) {
+    // the activation rows (written by the previous kernel) staged once with
+    // coalesced 16-byte loads, instead of one dependent L2 round trip per
+    // weight chunk inside the loop below
+    const int cpr = a.K / 8;
+    for (int i = threadIdx.x; i < a.M * cpr; i += kGemvThreads) {
+      const int m = i / cpr, c = i % cpr;
+      *reinterpret_cast<uint4*>(xs + (long long)m * a.K + c * 8) =
+          *reinterpret_cast<const uint4*>(a.X + (long long)m * a.ldx + c * 8);
+    }
     __syncthreads();
     X = xs;
     ldx = a.K;
