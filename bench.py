@@ -468,9 +468,23 @@ def run_workload_4b(args):
     from looped_normalized_transformer_ngpt_b300 import _build
     _build.build()
     torch.cuda.set_device(0)
-    sh = synth.DORY4B
+    sh = synth.DORY4B_SLIM if args.slim else synth.DORY4B
     peaks, peak_src = load_peaks()
     st = torch.cuda.Stream()
+    if args.mode == "profile":
+        # one eager decode step (the ncu target): the chosen context, 1 sequence,
+        # last-loop cache, k = 1
+        ctx = args.ctx or 131072
+        m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=ctx, max_chunk=1,
+                       k_max=1)
+        fill_cache_synthetic(m, sh)
+        m.set_length(1, ctx - 1)
+        tok = torch.tensor(synth.tokens(sh, 1, 1, seed=4)[:, 0], device="cuda")
+        m.decode(tok, 1)
+        torch.cuda.synchronize()
+        assert m.device_status() == 0
+        print(json.dumps({"profile_target": "ok", "shape": sh.name, "context": ctx}))
+        return
     out = {"workload": args.workload, "shape": "4B-class (d 2048, 16/40/16 layers, 16/4 heads, "
                                                  "ffn 6144, vocab 131072, window 4096)",
            "dtype": "bf16", "data": "synthetic (torch-seeded unit-norm bf16 weights, seeded tokens)"}
@@ -512,7 +526,8 @@ def run_workload_4b(args):
             if args.workload == "decode4b":
                 B, ctx, D, modes = 64, 32768, 4, [(dory.LAST_LOOP, (1, 2, 3, 4))]
             else:
-                B, ctx, D, modes = 1, 262144, 8, [(dory.LAST_LOOP, (1, 4)), (dory.PER_LOOP, (4,))]
+                B, ctx, D, modes = 1, args.ctx or 262144, 8, [(dory.LAST_LOOP, (1, 4)),
+                                                               (dory.PER_LOOP, (4,))]
             weights = synth.make_weights_torch(sh)
             res, kvb = {}, {}
             m = None
@@ -677,6 +692,9 @@ def main(argv=None):
                     default=[1, 2, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--slim", action="store_true",
+                    help="4B-class width with 2/4/2 layers (profiling targets)")
+    ap.add_argument("--ctx", type=int, default=0, help="context of the decode workloads")
     ap.add_argument("--workload", choices=["small", "prefill4b", "decode4b", "longctx4b"],
                     default="small", help="small: the default benchmark line; the others time "
                                           "the 4B-class workloads (one JSON line, not the contract)")

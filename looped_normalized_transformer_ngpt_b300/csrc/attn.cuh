@@ -510,7 +510,7 @@ namespace dory {
 // and rounds k^ / v to bf16 (the cache precision).  Otherwise the inputs are
 // ready bf16 q^, k^, v and sigmoid(g).
 // ---------------------------------------------------------------------------
-constexpr int kDecStages = 3;
+constexpr int kDecStages = 2;
 constexpr int kDecMinTiles = 4;
 
 struct DecAttnArgs {
@@ -533,6 +533,7 @@ struct DecAttnArgs {
   float* part_ml;                 // [B, n_q, n_splits, 2]
   int* counter;                   // [B * n_kv], zero between launches
   __nv_bfloat16* out;             // [B, n_q * dh]
+  int B;                          // sequences
 };
 
 template <int DH>
@@ -561,319 +562,334 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
   const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = a.n_q / a.n_kv;
   const int P0 = a.P0;
   const int lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;
-  const int k0 = lo + split * a.chunk;
-  const int k1 = min(k0 + a.chunk, P0);                      // cached keys only
-  const int ntiles = k1 > k0 ? (k1 - k0 + kDecTile - 1) / kDecTile : 0;
+  const int NS = a.n_splits;
+  const int n_items = NS * a.n_kv * a.B;
 
-  // cached K / V tile t of this split into ring buffer `buf` (zero-filled
-  // beyond k1).  The cache was written by earlier launches, so these loads
-  // may start before the wait on the previous kernel.
-  auto load_tile = [&](int t, int buf) {
-    const int j0 = k0 + t * kDecTile;
-    const uint32_t kb = ringa + (uint32_t)(buf * Cf::STAGE), vb = kb + Cf::KVB;
-    for (int idx = tid; idx < kDecTile * CH; idx += 128) {
-      const int r = idx / CH, c = idx % CH;
-      const int j = j0 + r;
-      const bool ok = j < k1;
-      const long long off =
-          ok ? (((long long)b * a.n_kv + kvh) * a.S + (j % a.S)) * DH + c * 8 : 0;
-      cp_async16(kb + swz_off<DH>(r, c), a.k_cache + off, ok);
-      cp_async16(vb + swz_off<DH>(r, c), a.v_cache + off, ok);
-    }
-  };
-#pragma unroll
-  for (int s = 0; s < kDecStages - 1; ++s) {
-    if (s < ntiles) load_tile(s, s);
-    cp_async_commit();
-  }
-  pdl_wait();
-  pdl_trigger();
+  // Work items (split, kv head, sequence) of equal size; the CTAs of the grid
+  // (no more than are resident) stride over them.
+  bool first = true;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int split = item % NS, kvh = (item / NS) % a.n_kv, b = item / (NS * a.n_kv);
+    const int k0 = lo + split * a.chunk;
+    const int k1 = min(k0 + a.chunk, P0);                    // cached keys only
+    const int ntiles = k1 > k0 ? (k1 - k0 + kDecTile - 1) / kDecTile : 0;
 
-  // ---- prologue: q^ (rows of sQ), current k^ and v
-  for (int idx = tid; idx < 16 * CH; idx += 128) {   // zero rows >= G
-    const int r = idx / CH, c = idx % CH;
-    if (r >= G) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sQ) + swz_off<DH>(r, c)) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-  for (int hh = warp; hh < G + 2; hh += 4) {
-    // hh < G: query head kvh * G + hh; hh == G: key; hh == G + 1: value
-    if (RAW) {
-      const int col0 = hh < G ? (kvh * G + hh) * DH
-                              : (hh == G ? (a.n_q + kvh) * DH : (a.n_q + a.n_kv + kvh) * DH);
-      const float* yr = a.y + (long long)b * a.ldy + col0;
-      float x1[(HALF + 31) / 32], x2[(HALF + 31) / 32];
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < (HALF + 31) / 32; ++e) {
-        const int i = lane + 32 * e;
-        x1[e] = x2[e] = 0.f;
-        if (i < HALF) {
-          for (int p = 0; p < a.n_parts; ++p) {
-            x1[e] += yr[p * a.part_stride + i];
-            x2[e] += yr[p * a.part_stride + i + HALF];
-          }
-        }
-        ss += x1[e] * x1[e] + x2[e] * x2[e];
+    // cached K / V tile t into ring buffer `buf` (zero-filled beyond k1).
+    // The cache was written by earlier launches, so the first item's loads
+    // may start before the wait on the previous kernel.
+    auto load_tile = [&](int t, int buf) {
+      const int j0 = k0 + t * kDecTile;
+      const uint32_t kb = ringa + (uint32_t)(buf * Cf::STAGE), vb = kb + Cf::KVB;
+      for (int idx = tid; idx < kDecTile * CH; idx += 128) {
+        const int r = idx / CH, c = idx % CH;
+        const int j = j0 + r;
+        const bool ok = j < k1;
+        const long long off =
+            ok ? (((long long)b * a.n_kv + kvh) * a.S + (j % a.S)) * DH + c * 8 : 0;
+        cp_async16(kb + swz_off<DH>(r, c), a.k_cache + off, ok);
+        cp_async16(vb + swz_off<DH>(r, c), a.v_cache + off, ok);
       }
-      if (hh <= G) {
-        const float inv = 1.0f / sqrtf(fmaxf(warp_sum(ss), 1e-12f));
+    };
+    if (!first) __syncthreads();                           // smem of the previous item free
+#pragma unroll
+    for (int st = 0; st < kDecStages; ++st) {              // fill the whole ring
+      if (st < ntiles) load_tile(st, st);
+      cp_async_commit();
+    }
+    if (first) {
+      pdl_wait();
+      pdl_trigger();
+      first = false;
+    }
+
+    // ---- prologue: q^ (rows of sQ), current k^ and v
+    for (int idx = tid; idx < 16 * CH; idx += 128) {       // zero rows >= G
+      const int r = idx / CH, c = idx % CH;
+      if (r >= G) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sQ) + swz_off<DH>(r, c)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int hh = warp; hh < G + 2; hh += 4) {
+      // hh < G: query head kvh * G + hh; hh == G: key; hh == G + 1: value
+      if (RAW) {
+        const int col0 = hh < G ? (kvh * G + hh) * DH
+                                : (hh == G ? (a.n_q + kvh) * DH : (a.n_q + a.n_kv + kvh) * DH);
+        const float* yr = a.y + (long long)b * a.ldy + col0;
+        float x1[(HALF + 31) / 32], x2[(HALF + 31) / 32];
+        float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < (HALF + 31) / 32; ++e) {
           const int i = lane + 32 * e;
+          x1[e] = x2[e] = 0.f;
           if (i < HALF) {
-            float c1 = x1[e], c2 = x2[e];
-            if (a.rope) {
-              const float2 cs = a.rope[i];
-              c1 = x1[e] * cs.x - x2[e] * cs.y;
-              c2 = x2[e] * cs.x + x1[e] * cs.y;
+            for (int p = 0; p < a.n_parts; ++p) {
+              x1[e] += yr[p * a.part_stride + i];
+              x2[e] += yr[p * a.part_stride + i + HALF];
             }
-            x1[e] = c1 * inv * a.s_qk[i];
-            x2[e] = c2 * inv * a.s_qk[i + HALF];
           }
+          ss += x1[e] * x1[e] + x2[e] * x2[e];
         }
-      }
+        if (hh <= G) {
+          const float inv = 1.0f / sqrtf(fmaxf(warp_sum(ss), 1e-12f));
 #pragma unroll
-      for (int e = 0; e < (HALF + 31) / 32; ++e) {
-        const int i = lane + 32 * e;
-        if (i >= HALF) continue;
-        const __nv_bfloat16 b1 = __float2bfloat16_rn(x1[e]), b2 = __float2bfloat16_rn(x2[e]);
-        if (hh < G) {
-          sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] = b1;
-          sQ[(swz_off<DH>(hh, (i + HALF) / 8) >> 1) + (i & 7)] = b2;
-        } else {
-          float* dst = hh == G ? sKc : sVc;
-          dst[i] = __bfloat162float(b1);
-          dst[i + HALF] = __bfloat162float(b2);
-          if (a.store && split == 0) {
-            __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
-            const long long off = (((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH;
-            cache[off + i] = b1;
-            cache[off + i + HALF] = b2;
+          for (int e = 0; e < (HALF + 31) / 32; ++e) {
+            const int i = lane + 32 * e;
+            if (i < HALF) {
+              float c1 = x1[e], c2 = x2[e];
+              if (a.rope) {
+                const float2 cs = a.rope[i];
+                c1 = x1[e] * cs.x - x2[e] * cs.y;
+                c2 = x2[e] * cs.x + x1[e] * cs.y;
+              }
+              x1[e] = c1 * inv * a.s_qk[i];
+              x2[e] = c2 * inv * a.s_qk[i + HALF];
+            }
           }
         }
-      }
-    } else {
-      for (int i = lane; i < DH; i += 32) {
-        if (hh < G) {
-          sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] =
-              a.q[((long long)b * a.n_q + kvh * G + hh) * DH + i];
-        } else {
-          const __nv_bfloat16* src = hh == G ? a.k_cur : a.v_cur;
-          const __nv_bfloat16 v = src[((long long)b * a.n_kv + kvh) * DH + i];
-          (hh == G ? sKc : sVc)[i] = __bfloat162float(v);
-          if (a.store && split == 0) {
-            __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
-            cache[(((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH + i] = v;
+#pragma unroll
+        for (int e = 0; e < (HALF + 31) / 32; ++e) {
+          const int i = lane + 32 * e;
+          if (i >= HALF) continue;
+          const __nv_bfloat16 b1 = __float2bfloat16_rn(x1[e]), b2 = __float2bfloat16_rn(x2[e]);
+          if (hh < G) {
+            sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] = b1;
+            sQ[(swz_off<DH>(hh, (i + HALF) / 8) >> 1) + (i & 7)] = b2;
+          } else {
+            float* dst = hh == G ? sKc : sVc;
+            dst[i] = __bfloat162float(b1);
+            dst[i + HALF] = __bfloat162float(b2);
+            if (a.store && split == 0) {
+              __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
+              const long long off = (((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH;
+              cache[off + i] = b1;
+              cache[off + i + HALF] = b2;
+            }
+          }
+        }
+      } else {
+        for (int i = lane; i < DH; i += 32) {
+          if (hh < G) {
+            sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] =
+                a.q[((long long)b * a.n_q + kvh * G + hh) * DH + i];
+          } else {
+            const __nv_bfloat16* src = hh == G ? a.k_cur : a.v_cur;
+            const __nv_bfloat16 v = src[((long long)b * a.n_kv + kvh) * DH + i];
+            (hh == G ? sKc : sVc)[i] = __bfloat162float(v);
+            if (a.store && split == 0) {
+              __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
+              cache[(((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH + i] = v;
+            }
           }
         }
       }
     }
-  }
-  __syncthreads();
-
-  // ---- cached keys: S = Q K^T, online softmax, O += P V (warp: 16 keys / tile)
-  const int g = lane >> 2, t4 = lane & 3;
-  uint32_t qf[DH / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < DH / 16; ++kk) {
-    const int r = lane & 15;
-    const int c = 2 * kk + (lane >> 4);
-    ldsm_x4(sQa + swz_off<DH>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
-  float o[DH / 8][4];
-#pragma unroll
-  for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-  for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<kDecStages - 2>();
     __syncthreads();
-    if (t + kDecStages - 1 < ntiles) load_tile(t + kDecStages - 1, (t + kDecStages - 1) % kDecStages);
-    cp_async_commit();
-    const uint32_t kbase = ringa + (uint32_t)((t % kDecStages) * Cf::STAGE);
-    const uint32_t vbase = kbase + Cf::KVB;
-    float s[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+
+    // ---- cached keys: S = Q K^T, online softmax, O += P V (warp: 16 keys / tile)
+    const int g = lane >> 2, t4 = lane & 3;
+    uint32_t qf[DH / 16][4];
 #pragma unroll
     for (int kk = 0; kk < DH / 16; ++kk) {
-      const int key = 16 * warp + (lane & 7) + ((lane >> 4) & 1) * 8;
-      const int c = 2 * kk + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kbase + swz_off<DH>(key, c), b0, b1, b2, b3);
-      mma_bf16_16816(s[0], qf[kk], b0, b1);
-      mma_bf16_16816(s[1], qf[kk], b2, b3);
+      const int r = lane & 15;
+      const int c = 2 * kk + (lane >> 4);
+      ldsm_x4(sQa + swz_off<DH>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
     }
-    const int j0 = k0 + t * kDecTile + 16 * warp;
-    float corr[2];
+    float o[DH / 8][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    for (int t = 0; t < ntiles; ++t) {
+      // tile t landed (tile t + 1 may still be in flight)
+      if (t + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+      __syncthreads();
+      const uint32_t kbase = ringa + (uint32_t)((t % kDecStages) * Cf::STAGE);
+      const uint32_t vbase = kbase + Cf::KVB;
+      float s[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        const int key = 16 * warp + (lane & 7) + ((lane >> 4) & 1) * 8;
+        const int c = 2 * kk + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz_off<DH>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qf[kk], b0, b1);
+        mma_bf16_16816(s[1], qf[kk], b2, b3);
+      }
+      // Only mma rows g < 8 can hold a head (G <= 8): the second row half
+      // (g + 8) gets P = 0 and no softmax work.  The running max is raised
+      // only when it grows by more than 2^8 (exact: the same stale max scales
+      // P and the row sum), so the accumulators are rarely rescaled.
+      const int j0 = k0 + t * kDecTile + 16 * warp;
       float mx = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int j = j0 + 8 * nt + 2 * t4 + e;
-          float v = s[nt][2 * h + e] * a.scale_log2;
+          float v = s[nt][e] * a.scale_log2;
           v = j < k1 ? v : -INFINITY;
-          s[nt][2 * h + e] = v;
+          s[nt][e] = v;
           mx = fmaxf(mx, v);
         }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run[h], mx);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      corr[h] = exp2f(m_run[h] - m_use);
-      m_run[h] = m_new;
+      if (mx > m_run + 8.0f) {
+        const float corr = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+        m_run = mx;
+        l_run *= corr;
+#pragma unroll
+        for (int i = 0; i < DH / 8; ++i) {
+          o[i][0] *= corr;
+          o[i][1] *= corr;
+        }
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float ls = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p = exp2f(s[nt][2 * h + e] - m_use);
-          s[nt][2 * h + e] = p;
+          const float p = exp2f(s[nt][e] - m_use);
+          s[nt][e] = p;
           ls += p;
         }
-      l_run[h] = l_run[h] * corr[h] + ls;
-    }
+      l_run += ls;
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+      pa[1] = 0u;
+      pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+      pa[3] = 0u;
 #pragma unroll
-    for (int i = 0; i < DH / 8; ++i) {
-      o[i][0] *= corr[0];
-      o[i][1] *= corr[0];
-      o[i][2] *= corr[1];
-      o[i][3] *= corr[1];
+      for (int dp = 0; dp < DH / 16; ++dp) {
+        const int key = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = 2 * dp + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + swz_off<DH>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      }
+      __syncthreads();                                     // buffer t % 2 free
+      if (t + kDecStages < ntiles) load_tile(t + kDecStages, t % kDecStages);
+      cp_async_commit();
     }
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-    pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-    pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-    pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-#pragma unroll
-    for (int dp = 0; dp < DH / 16; ++dp) {
-      const int key = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int c = 2 * dp + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vbase + swz_off<DH>(key, c), b0, b1, b2, b3);
-      mma_bf16_16816(o[2 * dp], pa, b0, b1);
-      mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();                                 // ring free: reuse for the merge
+    cp_async_wait<0>();
+    __syncthreads();                                       // ring free: reuse for the merge
 
-  // ---- merge the 4 warps: row r = head, per warp (m, l, o[r][:])
-  float* sO = reinterpret_cast<float*>(ring);       // [4][16][DH]
+    // ---- merge the 4 warps: row r = head, per warp (m, l, o[r][:])
+    float* sO = reinterpret_cast<float*>(ring);             // [4][16][DH]
+    {
+      float l = l_run;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (t4 == 0) {
+        sM[warp * 16 + g] = m_run;
+        sL[warp * 16 + g] = l;
+      }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float l = l_run[h];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int r = g + 8 * h;
-    if (t4 == 0) {
-      sM[warp * 16 + r] = m_run[h];
-      sL[warp * 16 + r] = l;
+      for (int nt = 0; nt < DH / 8; ++nt) {
+        const int dim = 8 * nt + 2 * t4;
+        *reinterpret_cast<float2*>(sO + (warp * 16 + g) * DH + dim) =
+            make_float2(o[nt][0], o[nt][1]);
+      }
     }
+    __syncthreads();
+    for (int idx = tid; idx < G * DH; idx += 128) {
+      const int r = idx / DH, dd = idx % DH;
+      float M = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < DH / 8; ++nt) {
-      const int dim = 8 * nt + 2 * t4;
-      *reinterpret_cast<float2*>(sO + (warp * 16 + r) * DH + dim) =
-          make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < G * DH; idx += 128) {
-    const int r = idx / DH, dd = idx % DH;
-    float M = -INFINITY;
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, sM[w * 16 + r]);
+      float L = 0.f, acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, sM[w * 16 + r]);
-    float L = 0.f, acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float wt = sM[w * 16 + r] == -INFINITY ? 0.f : exp2f(sM[w * 16 + r] - M);
-      L += sL[w * 16 + r] * wt;
-      acc += sO[(w * 16 + r) * DH + dd] * wt;
+      for (int w = 0; w < 4; ++w) {
+        const float wt = sM[w * 16 + r] == -INFINITY ? 0.f : exp2f(sM[w * 16 + r] - M);
+        L += sL[w * 16 + r] * wt;
+        acc += sO[(w * 16 + r) * DH + dd] * wt;
+      }
+      const long long base = ((long long)b * a.n_q + kvh * G + r) * a.n_splits + split;
+      a.part_o[base * DH + dd] = acc;
+      if (dd == 0) {
+        a.part_ml[base * 2] = M;
+        a.part_ml[base * 2 + 1] = L;
+      }
     }
-    const long long base = ((long long)b * a.n_q + kvh * G + r) * a.n_splits + split;
-    a.part_o[base * DH + dd] = acc;
-    if (dd == 0) {
-      a.part_ml[base * 2] = M;
-      a.part_ml[base * 2 + 1] = L;
-    }
-  }
 
-  // ---- ticket: the last CTA of (b, kvh) merges all splits + the new token
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counter[b * a.n_kv + kvh], 1);
-    *sFlag = prev == a.n_splits - 1;
-  }
-  __syncthreads();
-  if (!*sFlag) return;
-  __threadfence();
-  // new token's own score per head: q^ . k^_cur (bf16 operands, fp32 sum)
-  for (int r = warp; r < G; r += 4) {
-    float acc = 0.f;
-    for (int i = lane; i < DH; i += 32)
-      acc += __bfloat162float(sQ[(swz_off<DH>(r, i / 8) >> 1) + (i & 7)]) * sKc[i];
-    acc = warp_sum(acc);
-    if (lane == 0) sCur[r] = acc * a.scale_log2;
-  }
-  __syncthreads();
-  // per head: global max and split weights, one lane per split (warp = head)
-  float* sW = reinterpret_cast<float*>(ring);                  // [G][n_splits + 1]
-  const int NS = a.n_splits;
-  for (int r = warp; r < G; r += 4) {
-    const long long bh = (long long)b * a.n_q + kvh * G + r;
-    float mx = sCur[r];
-    for (int sp = lane; sp < NS; sp += 32) mx = fmaxf(mx, __ldcg(a.part_ml + (bh * NS + sp) * 2));
+    // ---- ticket: the last CTA of (b, kvh) merges all splits + the new token
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const int prev = atomicAdd(&a.counter[b * a.n_kv + kvh], 1);
+      *sFlag = prev == a.n_splits - 1;
+    }
+    __syncthreads();
+    if (!*sFlag) continue;
+    __threadfence();
+    // new token's own score per head: q^ . k^_cur (bf16 operands, fp32 sum)
+    for (int r = warp; r < G; r += 4) {
+      float acc = 0.f;
+      for (int i = lane; i < DH; i += 32)
+        acc += __bfloat162float(sQ[(swz_off<DH>(r, i / 8) >> 1) + (i & 7)]) * sKc[i];
+      acc = warp_sum(acc);
+      if (lane == 0) sCur[r] = acc * a.scale_log2;
+    }
+    __syncthreads();
+    // per head: global max and split weights, one lane per split (warp = head)
+    float* sW = reinterpret_cast<float*>(ring);                // [G][NS + 1]
+    for (int r = warp; r < G; r += 4) {
+      const long long bh = (long long)b * a.n_q + kvh * G + r;
+      float mx = sCur[r];
+      for (int sp = lane; sp < NS; sp += 32) mx = fmaxf(mx, __ldcg(a.part_ml + (bh * NS + sp) * 2));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float L = 0.f;
-    for (int sp = lane; sp < NS; sp += 32) {
-      const float ms = __ldcg(a.part_ml + (bh * NS + sp) * 2);
-      const float wt = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-      sW[r * (NS + 1) + sp] = wt;
-      L += __ldcg(a.part_ml + (bh * NS + sp) * 2 + 1) * wt;
+      for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      float L = 0.f;
+      for (int sp = lane; sp < NS; sp += 32) {
+        const float ms = __ldcg(a.part_ml + (bh * NS + sp) * 2);
+        const float wt = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+        sW[r * (NS + 1) + sp] = wt;
+        L += __ldcg(a.part_ml + (bh * NS + sp) * 2 + 1) * wt;
+      }
+      L = warp_sum(L);
+      if (lane == 0) {
+        const float wc = exp2f(sCur[r] - mx);
+        sW[r * (NS + 1) + NS] = wc;                              // new token's weight
+        sM[r] = 1.0f / (L + wc);
+      }
     }
-    L = warp_sum(L);
-    if (lane == 0) {
-      const float wc = exp2f(sCur[r] - mx);
-      sW[r * (NS + 1) + NS] = wc;                              // new token's weight
-      sM[r] = 1.0f / (L + wc);
+    __syncthreads();
+    for (int idx = tid; idx < G * DH; idx += 128) {
+      const int r = idx / DH, dd = idx % DH;
+      const long long bh = (long long)b * a.n_q + kvh * G + r;
+      const float* wr = sW + r * (NS + 1);
+      float acc = wr[NS] * sVc[dd];
+      const float* po = a.part_o + bh * NS * DH + dd;
+      int sp = 0;
+      for (; sp + 4 <= NS; sp += 4) {
+        const float o0 = __ldcg(po + (sp + 0) * DH), o1 = __ldcg(po + (sp + 1) * DH);
+        const float o2 = __ldcg(po + (sp + 2) * DH), o3 = __ldcg(po + (sp + 3) * DH);
+        acc += wr[sp] * o0 + wr[sp + 1] * o1 + wr[sp + 2] * o2 + wr[sp + 3] * o3;
+      }
+      for (; sp < NS; ++sp) acc += wr[sp] * __ldcg(po + sp * DH);
+      float gt;
+      if (RAW) {
+        float gr = 0.f;
+        const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
+                          (kvh * G + r) * DH + dd;
+        for (int p = 0; p < a.n_parts; ++p) gr += yg[p * a.part_stride];
+        gt = 1.0f / (1.0f + __expf(-gr));
+      } else {
+        gt = __bfloat162float(a.gate[bh * DH + dd]);
+      }
+      a.out[bh * DH + dd] = __float2bfloat16_rn(acc * sM[r] * gt);
     }
+    if (tid == 0) a.counter[b * a.n_kv + kvh] = 0;
   }
-  __syncthreads();
-  for (int idx = tid; idx < G * DH; idx += 128) {
-    const int r = idx / DH, dd = idx % DH;
-    const long long bh = (long long)b * a.n_q + kvh * G + r;
-    const float* wr = sW + r * (NS + 1);
-    float acc = wr[NS] * sVc[dd];
-    const float* po = a.part_o + bh * NS * DH + dd;
-    int sp = 0;
-    for (; sp + 4 <= NS; sp += 4) {
-      const float o0 = __ldcg(po + (sp + 0) * DH), o1 = __ldcg(po + (sp + 1) * DH);
-      const float o2 = __ldcg(po + (sp + 2) * DH), o3 = __ldcg(po + (sp + 3) * DH);
-      acc += wr[sp] * o0 + wr[sp + 1] * o1 + wr[sp + 2] * o2 + wr[sp + 3] * o3;
-    }
-    for (; sp < NS; ++sp) acc += wr[sp] * __ldcg(po + sp * DH);
-    float gt;
-    if (RAW) {
-      float gr = 0.f;
-      const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
-                        (kvh * G + r) * DH + dd;
-      for (int p = 0; p < a.n_parts; ++p) gr += yg[p * a.part_stride];
-      gt = 1.0f / (1.0f + __expf(-gr));
-    } else {
-      gt = __bfloat162float(a.gate[bh * DH + dd]);
-    }
-    a.out[bh * DH + dd] = __float2bfloat16_rn(acc * sM[r] * gt);
+  if (first) {                                                // no item: still order the grid
+    pdl_wait();
+    pdl_trigger();
   }
-  if (tid == 0) a.counter[b * a.n_kv + kvh] = 0;
 }
 
 }  // namespace dory

@@ -375,18 +375,34 @@ int launch_dec_attn(DecAttnArgs a, int B, cudaStream_t st) {
   }
   const int lo = a.window > 0 ? (a.P0 - a.window + 1 > 0 ? a.P0 - a.window + 1 : 0) : 0;
   const int n_cache = a.P0 - lo;                      // cached keys (the new token is extra)
-  // enough CTAs to fill the SMs twice, but at least kDecMinTiles tiles per
-  // split so that the prologue and merge of a CTA stay small against its keys
-  int splits = (2 * num_sms() + B * a.n_kv - 1) / (B * a.n_kv);
-  if (splits > kDecMaxSplits) splits = kDecMaxSplits;
-  if (splits < 1) splits = 1;
-  int chunk = (n_cache + splits - 1) / splits;
+  // Work items of equal size; the grid (no more CTAs than are resident: three
+  // per SM) strides over them.  The split count gives every (sequence, kv
+  // head) at least kDecMinTiles tiles per split and keeps the last round of
+  // items nearly full.
+  const int groups = B * a.n_kv;
+  const int cap = 3 * num_sms();
+  const int max_sp = (n_cache + kDecMinTiles * kDecTile - 1) / (kDecMinTiles * kDecTile);
+  int best_sp = 1;
+  double best = -1.0;
+  for (int sp = 1; sp <= kDecMaxSplits && sp <= (max_sp > 0 ? max_sp : 1); ++sp) {
+    const long long items = (long long)groups * sp;
+    const long long rounds = (items + cap - 1) / cap;
+    // time ~ rounds x keys per split; prefer fewer, fuller rounds
+    const double per = (double)rounds * (double)((n_cache + sp - 1) / sp + 1);
+    if (best < 0 || per < best * 0.98) {
+      best = per;
+      best_sp = sp;
+    }
+  }
+  int chunk = n_cache > 0 ? (n_cache + best_sp - 1) / best_sp : kDecTile;
   chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
-  if (chunk < kDecMinTiles * kDecTile) chunk = kDecMinTiles * kDecTile;
   a.chunk = chunk;
   a.n_splits = n_cache > 0 ? (n_cache + chunk - 1) / chunk : 1;
-  return launch_k(attn_decode_kernel<DH, RAW>, dim3(a.n_splits, a.n_kv, B), dim3(128),
-                  DecCfg<DH>::SMEM, st, a) == cudaSuccess
+  const long long items = (long long)groups * a.n_splits;
+  const int grid = items < cap ? (int)items : cap;
+  a.B = B;
+  return launch_k(attn_decode_kernel<DH, RAW>, dim3(grid), dim3(128), DecCfg<DH>::SMEM, st, a) ==
+                 cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
 }
