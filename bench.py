@@ -82,11 +82,16 @@ def layer_params(sh):
 
 
 def visible_keys(sh, layer, P0, C):
-    """Sum over the C query positions P0..P0+C-1 of the number of visible keys."""
-    tot = 0
-    for t in range(P0, P0 + C):
-        tot += t + 1 if sh.is_full(layer) else min(t + 1, sh.window)
-    return tot
+    """Sum over the C query positions P0..P0+C-1 of the number of visible
+    keys (closed form: t + 1 keys at position t, at most the window)."""
+    lo, hi = P0, P0 + C - 1
+
+    def tri(a, b):                       # sum of (t + 1) for t = a..b
+        return 0 if b < a else (b - a + 1) * (a + b + 2) // 2
+    if sh.is_full(layer):
+        return tri(lo, hi)
+    W = sh.window
+    return tri(lo, min(hi, W - 1)) + max(0, hi - max(lo, W) + 1) * W
 
 
 def step_flops(sh, B, C, k, P0=0, logit_rows=None):
@@ -489,7 +494,93 @@ def run_workload_4b(args):
                                                  "ffn 6144, vocab 131072, window 4096)",
            "dtype": "bf16", "data": "synthetic (torch-seeded unit-norm bf16 weights, seeded tokens)"}
     with ClockSampler(0) as clk:
-        if args.workload == "prefill4b":
+        if args.workload == "longprefill4b":
+            # 262144-token context prefilled in 16384-token chunks at k = 4
+            # (last-loop cache), then decode steps at that context
+            T, CH, K, D = args.ctx or 262144, 16384, 4, 8
+            m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T + D,
+                           max_chunk=CH, k_max=K)
+            tok = torch.tensor(synth.tokens(sh, 1, T, seed=5), device="cuda")
+            lg = torch.empty((1, sh.vocab), device="cuda")
+            with torch.cuda.stream(st):
+                m.reset()
+                m.prefill(tok[:, :CH], K, logits=lg, stream=st)      # warm-up chunk
+            st.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st):
+                m.reset()
+                e0.record(st)
+                m.prefill(tok, K, logits=lg, stream=st)
+                e1.record(st)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            fl = 0.0
+            for c0 in range(0, T, CH):
+                fl += sum(step_flops(sh, 1, CH, K, P0=c0, logit_rows=1).values())
+            nxt = torch.empty((1,), dtype=torch.int32, device="cuda")
+            first = torch.argmax(lg, dim=-1).to(torch.int32)
+            assert m.device_status() == 0
+
+            def fn():
+                m.set_length(1, T)
+                for _ in range(D):
+                    m.decode(first, K, logits=lg, next_tokens=nxt, stream=st)
+            dms = _graph_time(fn, st, warm=1, reps=3) / D
+            by = decode_step_bytes(sh, 1, K, T + D // 2)
+            out.update({"prefill": {"tokens": T, "chunk": CH, "k": K, "ms": round(ms, 1),
+                                    "tokens_s": round(T / (ms / 1e3), 1),
+                                    "algorithmic_pflop": round(fl / 1e15, 2),
+                                    "tflops": round(fl / (ms / 1e3) / 1e12, 1)},
+                        "decode_after_prefill": {"k": K, "ms_per_step": round(dms, 3),
+                                                 "tokens_s": round(1 / (dms / 1e3), 1),
+                                                 "GBs": round((by["weights"] + by["kv"]) /
+                                                              (dms / 1e3) / 1e9, 1)},
+                        "kv_bytes_last_loop": int(m.kv.numel())})
+        elif args.workload == "divergence4b":
+            # real chunked prefill in both cache modes, then teacher-forced decode:
+            # how far last-loop caching moves the outputs from per-loop caching
+            T, CH, K, D = args.ctx or 16384, 4096, 4, 16
+            weights = synth.make_weights_torch(sh)
+            tok = torch.tensor(synth.tokens(sh, 1, T, seed=6), device="cuda")
+            runs = {}
+            m = None
+            for mode in (dory.PER_LOOP, dory.LAST_LOOP):
+                if m is None:
+                    m = dory.Model(sh, weights, max_batch=1, max_ctx=T + D, max_chunk=CH,
+                                   k_max=K, cache_mode=mode)
+                else:
+                    m.bind(1, T + D, CH, K, mode)
+                lg = m.prefill(tok, K, mode).clone()
+                c_last = T - ((T - 1) // CH) * CH
+                hs, lgs = [m.hidden(c_last)[-1:].clone()], [lg]
+                forced = runs.get(dory.PER_LOOP, {}).get("next")
+                nxts = []
+                cur = torch.argmax(lg, dim=-1).to(torch.int32) if forced is None else forced[0]
+                for s_ in range(D):
+                    l2, n2 = m.decode(cur, K, mode)
+                    lgs.append(l2.clone())
+                    hs.append(m.hidden(1).clone())
+                    nxts.append(n2.clone())
+                    cur = n2 if forced is None else forced[min(s_ + 1, D - 1)]
+                if forced is None:
+                    forced = [torch.argmax(lg, dim=-1).to(torch.int32)] + nxts
+                runs[mode] = {"logits": lgs, "hidden": hs, "next": forced}
+                assert m.device_status() == 0
+            steps = []
+            for i in range(D + 1):
+                a_, b_ = runs[dory.PER_LOOP]["logits"][i], runs[dory.LAST_LOOP]["logits"][i]
+                ha, hb = runs[dory.PER_LOOP]["hidden"][i], runs[dory.LAST_LOOP]["hidden"][i]
+                steps.append({"step": i, "logits_maxabs": round(float((a_ - b_).abs().max()), 4),
+                              "hidden_maxabs": round(float((ha - hb).abs().max()), 4),
+                              "hidden_cos": round(float(torch.nn.functional.cosine_similarity(
+                                  ha, hb, dim=-1).min()), 5),
+                              "greedy_agree": bool(torch.equal(torch.argmax(a_, -1),
+                                                               torch.argmax(b_, -1)))})
+            out.update({"context": T, "chunk": CH, "k": K, "decode_steps": D,
+                        "teacher_forcing": "both modes decode the per-loop run's greedy tokens",
+                        "per_step": steps,
+                        "greedy_agreement": sum(x["greedy_agree"] for x in steps[1:]) / D})
+        elif args.workload == "prefill4b":
             T = 8192
             m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,
                            k_max=4)
@@ -695,7 +786,8 @@ def main(argv=None):
     ap.add_argument("--slim", action="store_true",
                     help="4B-class width with 2/4/2 layers (profiling targets)")
     ap.add_argument("--ctx", type=int, default=0, help="context of the decode workloads")
-    ap.add_argument("--workload", choices=["small", "prefill4b", "decode4b", "longctx4b"],
+    ap.add_argument("--workload", choices=["small", "prefill4b", "decode4b", "longctx4b",
+                                           "longprefill4b", "divergence4b"],
                     default="small", help="small: the default benchmark line; the others time "
                                           "the 4B-class workloads (one JSON line, not the contract)")
     args = ap.parse_args(argv)

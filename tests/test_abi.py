@@ -128,3 +128,16 @@ def test_debug_gemm_rejects_bad_shapes(L):
     assert L.dory_debug_gemm(None, None, None, 1, 1, 8, 1, None) == dory.DORY_EINVAL
     assert L.dory_debug_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
                              4, 4, 12, 4, None) == dory.DORY_EINVAL
+
+
+def test_bench_visible_key_count_matches_brute_force():
+    """bench.py's algorithmic work model: the closed-form count of visible
+    (query, key) pairs equals direct counting."""
+    import bench
+    import synth
+    for sh in (synth.SMALL, synth.TINY):
+        for l in range(4):
+            for P0, C in ((0, 2048), (300, 700), (1000, 5), (0, 1), (511, 2), (512, 1), (15, 40)):
+                brute = sum(t + 1 if sh.is_full(l) else min(t + 1, sh.window)
+                            for t in range(P0, P0 + C))
+                assert bench.visible_keys(sh, l, P0, C) == brute
