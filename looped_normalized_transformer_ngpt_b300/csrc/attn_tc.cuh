@@ -42,6 +42,7 @@ struct AttnTcArgs {
   const __nv_bfloat16* gate;  // [B*C, n_q*128] sigmoid(g)
   __nv_bfloat16* out;         // [B*C, n_q*128]
   int n_q;
+  int B;                      // sequences
   int* status;
 };
 
@@ -81,6 +82,30 @@ __device__ __forceinline__ void attn_tc_load_kv(uint8_t* dst_k, uint8_t* dst_v,
   }
 }
 
+// Geometry of one work item (query block qb of one (kv head, sequence)).
+struct AttnTcItem {
+  int kvh, b, q0, nqv, p_lo, p_hi, t_first, ntiles;
+};
+
+__device__ __forceinline__ AttnTcItem attn_tc_item(const AttnTcArgs& a, int item) {
+  AttnTcItem it;
+  const int QP = 128 / a.G;
+  const int nqb = (a.C + QP - 1) / QP;
+  const int per_q = a.n_kv * a.B;
+  const int qb = nqb - 1 - item / per_q;                 // longest query blocks first
+  const int rem = item % per_q;
+  it.kvh = rem % a.n_kv;
+  it.b = rem / a.n_kv;
+  it.q0 = qb * QP;
+  it.nqv = min(QP, a.C - it.q0);
+  it.p_lo = a.P0 + it.q0;
+  it.p_hi = a.P0 + it.q0 + it.nqv - 1;
+  const int k_lo = a.window > 0 ? max(0, it.p_lo - a.window + 1) : 0;
+  it.t_first = k_lo / AttnTcCfg::BK;
+  it.ntiles = it.p_hi / AttnTcCfg::BK - it.t_first + 1;
+  return it;
+}
+
 __global__ void __launch_bounds__(192, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
@@ -97,29 +122,25 @@ __global__ void __launch_bounds__(192, 2)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;    // [2]
-  uint64_t* kv_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;     // [2]
-  uint64_t* s_free = bars + 7;     // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;    // [2]
+  uint64_t* kv_empty = bars + 4;   // [2]
+  uint64_t* s_full = bars + 6;     // [2]
+  uint64_t* s_free = bars + 8;     // [2]
+  uint64_t* p_full = bars + 10;
+  uint64_t* o_done = bars + 11;
+  uint64_t* o_free = bars + 12;
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int QP = 128 / a.G;                             // query positions per CTA
-  const int qb = gridDim.x - 1 - blockIdx.x;            // longest rows first
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int q0 = qb * QP;
-  const int nqv = min(QP, a.C - q0);
-  const int p_lo = a.P0 + q0, p_hi = a.P0 + q0 + nqv - 1;
-  const int k_lo = a.window > 0 ? max(0, p_lo - a.window + 1) : 0;
-  const int t_first = k_lo / Cf::BK, t_last = p_hi / Cf::BK;
-  const int ntiles = t_last - t_first + 1;
+  const int QP = 128 / a.G;
+  const int n_items = ((a.C + QP - 1) / QP) * a.n_kv * a.B;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -128,6 +149,7 @@ __global__ void __launch_bounds__(192, 2)
     }
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
+    mbar_init(o_free, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -145,28 +167,40 @@ __global__ void __launch_bounds__(192, 2)
   pdl_wait();
   pdl_trigger();
 
+  // Work items are strided over the CTAs of the grid (no more than are
+  // resident); barrier phases run on across items: g counts key tiles, n
+  // counts this CTA's items.
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * Cf::QHALF);
-      const int tok = b * a.C + q0;
-      tma_load_3d(smem + Cf::Q_OFF, &tm_q, q_full, 0, kvh * a.G, tok);
-      tma_load_3d(smem + Cf::Q_OFF + Cf::QHALF, &tm_q, q_full, 64, kvh * a.G, tok);
-      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait_bounded(&kv_empty[st], ((j >> 1) - 1) & 1, a.status,
-                                         DEV_ATTN_PRODUCER)) {
+      int g = 0, n = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++n) {
+        const AttnTcItem it = attn_tc_item(a, item);
+        if (n >= 1 && !mbar_wait_bounded(q_empty, (n - 1) & 1, a.status, DEV_ATTN_PRODUCER)) {
           *abort_flag = 1;
           break;
         }
-        const int j0 = (t_first + j) * Cf::BK;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::KVTILE);
-        uint8_t* dk = smem + Cf::K_OFF + st * Cf::KVTILE;
-        uint8_t* dv = smem + Cf::V_OFF + st * Cf::KVTILE;
-        if (j0 < a.P0)
-          attn_tc_load_kv<true>(dk, dv, &tm_kc, &tm_vc, &kv_full[st], j0, b, kvh, a);
-        else
-          attn_tc_load_kv<false>(dk, dv, &tm_k, &tm_v, &kv_full[st], j0, b, kvh, a);
+        mbar_arrive_expect_tx(q_full, 2 * Cf::QHALF);
+        const int tok = it.b * a.C + it.q0;
+        tma_load_3d(smem + Cf::Q_OFF, &tm_q, q_full, 0, it.kvh * a.G, tok);
+        tma_load_3d(smem + Cf::Q_OFF + Cf::QHALF, &tm_q, q_full, 64, it.kvh * a.G, tok);
+        for (int j = 0; j < it.ntiles; ++j, ++g) {
+          const int st = g & 1;
+          if (g >= 2 && !mbar_wait_bounded(&kv_empty[st], ((g >> 1) - 1) & 1, a.status,
+                                           DEV_ATTN_PRODUCER)) {
+            *abort_flag = 1;
+            break;
+          }
+          const int j0 = (it.t_first + j) * Cf::BK;
+          mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::KVTILE);
+          uint8_t* dk = smem + Cf::K_OFF + st * Cf::KVTILE;
+          uint8_t* dv = smem + Cf::V_OFF + st * Cf::KVTILE;
+          if (j0 < a.P0)
+            attn_tc_load_kv<true>(dk, dv, &tm_kc, &tm_vc, &kv_full[st], j0, it.b, it.kvh, a);
+          else
+            attn_tc_load_kv<false>(dk, dv, &tm_k, &tm_v, &kv_full[st], j0, it.b, it.kvh, a);
+        }
+        if (*abort_flag) break;
       }
     }
   } else if (warp == 1) {
@@ -176,11 +210,10 @@ __global__ void __launch_bounds__(192, 2)
       constexpr uint32_t idesc_o = tc_idesc_bf16(128, 128) | (1u << 16);   // B (V) MN-major
       const uint32_t q_addr = smem_u32(smem + Cf::Q_OFF);
       const uint32_t p_addr = smem_u32(smem + Cf::P_OFF);
-      bool ok = mbar_wait_bounded(q_full, 0, a.status, DEV_ATTN_MMA);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&kv_full[st], (j >> 1) & 1, a.status, DEV_ATTN_MMA)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&s_free[st], ((j >> 1) - 1) & 1, a.status, DEV_ATTN_MMA))
+      auto issue_s = [&](int g) -> bool {
+        const int st = g & 1;
+        if (!mbar_wait_bounded(&kv_full[st], (g >> 1) & 1, a.status, DEV_ATTN_MMA)) return false;
+        if (g >= 2 && !mbar_wait_bounded(&s_free[st], ((g >> 1) - 1) & 1, a.status, DEV_ATTN_MMA))
           return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + Cf::K_OFF + st * Cf::KVTILE);
@@ -194,29 +227,41 @@ __global__ void __launch_bounds__(192, 2)
         tc_commit(&s_full[st]);
         return true;
       };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-        if (j + 1 < ntiles && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_bounded(p_full, j & 1, a.status, DEV_ATTN_MMA)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int st = j & 1;
-        const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::KVTILE);
+      bool ok = true;
+      int g = 0, n = 0;
+      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++n) {
+        const AttnTcItem it = attn_tc_item(a, item);
+        ok = mbar_wait_bounded(q_full, n & 1, a.status, DEV_ATTN_MMA) && issue_s(g);
+        for (int j = 0; ok && j < it.ntiles && !*abort_flag; ++j) {
+          const int gj = g + j;
+          if (j + 1 < it.ntiles) {
+            if (!issue_s(gj + 1)) {
+              ok = false;
+              break;
+            }
+          } else {
+            tc_commit(q_empty);                   // Q free once this item's S MMAs are done
+          }
+          if (!mbar_wait_bounded(p_full, gj & 1, a.status, DEV_ATTN_MMA) ||
+              (j == 0 && n >= 1 && !mbar_wait_bounded(o_free, (n - 1) & 1, a.status, DEV_ATTN_MMA))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int st = gj & 1;
+          const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::KVTILE);
 #pragma unroll
-        for (int kk = 0; kk < Cf::BK / 16; ++kk) {
-          // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major:
-          // the two 64-dim halves KVHALF apart, 8-key groups 1024 B apart)
-          tc_mma_bf16(tmem + 2 * Cf::BK, tc_sdesc_sw128(p_addr + kk * 32),
-                      tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::KVHALF, 1024), idesc_o,
-                      (j | kk) != 0);
+          for (int kk = 0; kk < Cf::BK / 16; ++kk) {
+            // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major:
+            // the two 64-dim halves KVHALF apart, 8-key groups 1024 B apart)
+            tc_mma_bf16(tmem + 2 * Cf::BK, tc_sdesc_sw128(p_addr + kk * 32),
+                        tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::KVHALF, 1024), idesc_o,
+                        (j | kk) != 0);
+          }
+          tc_commit(&kv_empty[st]);
+          tc_commit(o_done);
         }
-        tc_commit(&kv_empty[st]);
-        tc_commit(o_done);
+        g += it.ntiles;
       }
       if (!ok) *abort_flag = 1;
       tc_commit(drain);
@@ -227,110 +272,117 @@ __global__ void __launch_bounds__(192, 2)
     // ------------------------------------------------ softmax warps 2..5
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                  // tile row = TMEM lane
-    const int i = r / a.G, hg = r % a.G;
-    const bool row_ok = i < nqv;
-    const int qpos = a.P0 + q0 + i;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t* prow = smem + Cf::P_OFF + r * (Cf::BK * 2);
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    int g = 0, n = 0;
     // tcgen05.ld / tcgen05.st are warp-collective: every decision that guards
     // them (abort, rescale) is made uniform across the warp.
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      bool w_ok = !*abort_flag &&
-                  mbar_wait_bounded(&s_full[st], (j >> 1) & 1, a.status, DEV_ATTN_SOFTMAX);
-      if (!__all_sync(0xffffffffu, w_ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[Cf::BK];
-#pragma unroll
-      for (int c = 0; c < Cf::BK / 32; ++c)
-        tmem_ld32_nowait(tmem + st * Cf::BK + lane_off + c * 32, sv + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
-      // mask (raw scores; scale > 0 keeps the order); whole-tile visibility is
-      // uniform for the CTA.  Four partial maxima break the dependency chain.
-      const int j0 = (t_first + j) * Cf::BK;
-      const bool all_vis = j0 + Cf::BK - 1 <= p_lo && (a.window <= 0 || p_hi - j0 < a.window);
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < Cf::BK; ++c) {
-        float v = __uint_as_float(sv[c]);
-        if (!all_vis) {
-          const int rel = qpos - (j0 + c);
-          const bool vis = row_ok && rel >= 0 && (a.window <= 0 || rel < a.window);
-          v = vis ? v : -INFINITY;
-        } else if (!row_ok) {
-          v = -INFINITY;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++n) {
+      const AttnTcItem it = attn_tc_item(a, item);
+      const int i = r / a.G, hg = r % a.G;
+      const bool row_ok = i < it.nqv;
+      const int qpos = it.p_lo + i;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < it.ntiles; ++j) {
+        const int gj = g + j, st = gj & 1;
+        bool w_ok = !*abort_flag &&
+                    mbar_wait_bounded(&s_full[st], (gj >> 1) & 1, a.status, DEV_ATTN_SOFTMAX);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
         }
-        sv[c] = __float_as_uint(v);
-        mx4[c & 3] = fmaxf(mx4[c & 3], v);
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
-      float scale_o = 1.f;
-      bool rescale = false;
-      if (mx > m_run + 8.0f) {                     // stale max kept unless it grows by > 2^8
-        scale_o = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
-        rescale = j > 0;
-        l_run *= scale_o;
-        m_run = mx;
-      }
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      // P buffer and O are free once the previous PV MMA completed
-      w_ok = j == 0 || mbar_wait_bounded(o_done, (j - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
-      if (!__all_sync(0xffffffffu, w_ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale)) {      // lanes without a rescale scale by 1
-        if (!rescale) scale_o = 1.f;
+        tc_fence_after();
+        uint32_t sv[Cf::BK];
+#pragma unroll
+        for (int c = 0; c < Cf::BK / 32; ++c)
+          tmem_ld32_nowait(tmem + st * Cf::BK + lane_off + c * 32, sv + c * 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_free[st]);
+        // mask (raw scores; scale > 0 keeps the order); whole-tile visibility is
+        // uniform for the item.  Four partial maxima break the dependency chain.
+        const int j0 = (it.t_first + j) * Cf::BK;
+        const bool all_vis =
+            j0 + Cf::BK - 1 <= it.p_lo && (a.window <= 0 || it.p_hi - j0 < a.window);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < Cf::BK; ++c) {
+          float v = __uint_as_float(sv[c]);
+          if (!all_vis) {
+            const int rel = qpos - (j0 + c);
+            const bool vis = row_ok && rel >= 0 && (a.window <= 0 || rel < a.window);
+            v = vis ? v : -INFINITY;
+          } else if (!row_ok) {
+            v = -INFINITY;
+          }
+          sv[c] = __float_as_uint(v);
+          mx4[c & 3] = fmaxf(mx4[c & 3], v);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
+        float scale_o = 1.f;
+        bool rescale = false;
+        if (mx > m_run + 8.0f) {                     // stale max kept unless it grows by > 2^8
+          scale_o = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+          rescale = j > 0;
+          l_run *= scale_o;
+          m_run = mx;
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        // the P buffer (and, within the item, O) is free once the previous PV
+        // MMA completed
+        w_ok = gj == 0 || mbar_wait_bounded(o_done, (gj - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {      // lanes without a rescale scale by 1
+          if (!rescale) scale_o = 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32_nowait(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
-          tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32_nowait(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * scale_o);
-          tmem_st32(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * scale_o);
+            tmem_st32(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
-      }
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < Cf::BK / 8; ++q) {        // chunks of 8 keys
-        float p[8];
+        for (int q = 0; q < Cf::BK / 8; ++q) {        // chunks of 8 keys
+          float p[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(fmaf(__uint_as_float(sv[q * 8 + e]), a.scale_log2, -m_use));
-          ls4[e & 3] += p[e];
+          for (int e = 0; e < 8; ++e) {
+            p[e] = exp2f(fmaf(__uint_as_float(sv[q * 8 + e]), a.scale_log2, -m_use));
+            ls4[e & 3] += p[e];
+          }
+          uint4 pk;
+          pk.x = pack_bf16x2(p[0], p[1]);
+          pk.y = pack_bf16x2(p[2], p[3]);
+          pk.z = pack_bf16x2(p[4], p[5]);
+          pk.w = pack_bf16x2(p[6], p[7]);
+          *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) = pk;
         }
-        uint4 pk;
-        pk.x = pack_bf16x2(p[0], p[1]);
-        pk.y = pack_bf16x2(p[2], p[3]);
-        pk.z = pack_bf16x2(p[4], p[5]);
-        pk.w = pack_bf16x2(p[6], p[7]);
-        *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) = pk;
+        l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
-      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-      l_run += ls;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // final: O / l * gate
-    bool fin = ok && ntiles > 0 && !*abort_flag &&
-               mbar_wait_bounded(o_done, (ntiles - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
-    fin = __all_sync(0xffffffffu, fin);
-    if (fin) {
+      if (!ok) break;
+      // final: O / l * gate, then O is free for the next item
+      bool fin = !*abort_flag && mbar_wait_bounded(o_done, (g + it.ntiles - 1) & 1, a.status,
+                                                   DEV_ATTN_SOFTMAX);
+      if (!__all_sync(0xffffffffu, fin)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      const long long row = (long long)b * a.C + q0 + i;
-      const long long base = row * a.n_q * 128 + (long long)(kvh * a.G + hg) * 128;
+      const long long row = (long long)it.b * a.C + it.q0 + i;
+      const long long base = row * a.n_q * 128 + (long long)(it.kvh * a.G + hg) * 128;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
@@ -352,9 +404,11 @@ __global__ void __launch_bounds__(192, 2)
           *reinterpret_cast<uint4*>(a.out + base + c * 32 + e) = o;
         }
       }
-    } else {
-      *abort_flag = 1;
+      tc_fence_before();
+      mbar_arrive(o_free);
+      g += it.ntiles;
     }
+    if (!ok) *abort_flag = 1;
   }
 
   if (*abort_flag) {

@@ -295,10 +295,15 @@ int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows
   a.out = aa.out;
   a.n_q = aa.n_q;
   a.status = status;
+  a.B = B;
+  // persistent: no more CTAs than are resident (two per SM), striding over
+  // the work items (query block, kv head, sequence), longest first
   const int QP = 128 / G;
-  dim3 grid((aa.C + QP - 1) / QP, aa.n_kv, B);
-  return launch_k(attn_tc_kernel, grid, dim3(192), AttnTcCfg::SMEM, st, tq, tk, tv, tkc, tvc, a) ==
-                 cudaSuccess
+  const long long items = (long long)((aa.C + QP - 1) / QP) * aa.n_kv * B;
+  const int cap = 2 * num_sms();
+  const int grid = items < cap ? (int)items : cap;
+  return launch_k(attn_tc_kernel, dim3(grid), dim3(192), AttnTcCfg::SMEM, st, tq, tk, tv, tkc, tvc,
+                  a) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
 }

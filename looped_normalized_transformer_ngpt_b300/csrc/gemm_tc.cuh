@@ -85,6 +85,14 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
   reinterpret_cast<uint4*>(dst)[1] = b;
 }
 
+// 16 fp32 values given as their bit patterns -> 16 bf16.
+__device__ __forceinline__ void store_bf16x16_bits(__nv_bfloat16* dst, const uint32_t* r) {
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  store_bf16x16(dst, v);
+}
+
 // ------------------------------------------------------------- epilogues
 template <int BN>
 __device__ __forceinline__ void epi_f32(const GemmArgs& a, uint32_t tacc, int row, int n0,
@@ -144,10 +152,60 @@ __device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int r
     if (gcol >= a.N) break;
     const int head = gcol / dh;
     if (head < nq + nkv) {
-      // q or k head: RoPE, per-head L2 norm, s_qk
+      // q or k head: RoPE, per-head L2 norm, s_qk.  Latency matters here (the
+      // GEMM is epilogue-bound otherwise): TMEM is read 32 columns at a time
+      // with one wait per pair of loads, and the RoPE-table row of this
+      // position is fetched in two halves, each issued before the work that
+      // precedes its use.
       const bool is_q = head < nq;
       __nv_bfloat16* dst = is_q ? a.q + ((long long)row * nq + head) * dh
                                 : a.k + ((long long)row * nkv + (head - nq)) * dh;
+      if (dh == 128 && a.rope) {
+        const float2* cs_row = a.rope + (long long)t * 64;
+        float2 cs[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) cs[i] = row_ok ? cs_row[i] : make_float2(1.f, 0.f);
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_nowait(tacc + hc + c, r0);
+          tmem_ld32_nowait(tacc + hc + c + 32, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float u0 = __uint_as_float(r0[i]), u1 = __uint_as_float(r1[i]);
+            ss += u0 * u0 + u1 * u1;
+          }
+        }
+        const float inv = 1.0f / sqrtf(fmaxf(ss, 1e-12f));
+#pragma unroll 1
+        for (int hp = 0; hp < 2; ++hp) {              // pairs (i, i + 64), i in [32 hp, 32 hp + 32)
+          uint32_t r1[32], r2[32];
+          tmem_ld32_nowait(tacc + hc + 32 * hp, r1);
+          tmem_ld32_nowait(tacc + hc + 64 + 32 * hp, r2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float u1 = __uint_as_float(r1[i]), u2 = __uint_as_float(r2[i]);
+            const float y1 = u1 * cs[i].x - u2 * cs[i].y;
+            const float y2 = u2 * cs[i].x + u1 * cs[i].y;
+            r1[i] = __float_as_uint(y1 * inv * a.s_qk[32 * hp + i]);
+            r2[i] = __float_as_uint(y2 * inv * a.s_qk[64 + 32 * hp + i]);
+          }
+          if (hp == 0) {                              // second half's table entries
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cs[i] = row_ok ? cs_row[32 + i] : make_float2(1.f, 0.f);
+          }
+          if (row_ok) {
+            store_bf16x16_bits(dst + 32 * hp, r1);
+            store_bf16x16_bits(dst + 32 * hp + 16, r1 + 16);
+            store_bf16x16_bits(dst + 64 + 32 * hp, r2);
+            store_bf16x16_bits(dst + 64 + 32 * hp + 16, r2 + 16);
+          }
+        }
+        continue;
+      }
       float ss = 0.f;
 #pragma unroll 1
       for (int c = 0; c < dh; c += 16) {

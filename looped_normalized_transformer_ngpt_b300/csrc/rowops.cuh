@@ -377,11 +377,24 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V
   const float* z = logits + row * V;
   float best = -INFINITY;
   int idx = 0x7fffffff;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float v = z[i];
-    if (v > best) {           // strictly greater: keeps the lowest index per thread
-      best = v;
-      idx = i;
+  // 16-byte loads, four rows of them in flight per thread (V % 16 == 0);
+  // within a thread indices grow, so "strictly greater" keeps the lowest
+  const float4* z4 = reinterpret_cast<const float4*>(z);
+  const int n4 = V / 4;
+  for (int base = threadIdx.x; base < n4; base += 4 * blockDim.x) {
+    float4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i4 = base + u * blockDim.x;
+      q[u] = i4 < n4 ? z4[i4] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = 4 * (base + u * blockDim.x);
+      if (q[u].x > best) { best = q[u].x; idx = i; }
+      if (q[u].y > best) { best = q[u].y; idx = i + 1; }
+      if (q[u].z > best) { best = q[u].z; idx = i + 2; }
+      if (q[u].w > best) { best = q[u].w; idx = i + 3; }
     }
   }
 #pragma unroll
