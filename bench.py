@@ -345,6 +345,17 @@ def run_gpu(args):
     breakdown = {c[1]: {"ms": round(c[0], 3), "launches": c[2],
                         "achieved": None if c[4] is None else round(c[4], 1), "unit": c[5]}
                  for c in classes}
+    # one decode step, each launch event-timed (no overlap between kernels,
+    # so the classes add up to more than the graph-timed step)
+    with torch.cuda.stream(stream):
+        prefill_part(K)
+    stream.synchronize()
+    m.profile_begin(1 << 12)
+    with torch.cuda.stream(stream):
+        m.decode(first, K, logits=dlogits, next_tokens=nxt[0], stream=stream)
+    dprof = m.profile_end()
+    decode_breakdown = {n: {"ms": round(t, 4), "launches": c2, "us_per_launch": round(t / c2 * 1e3, 2)}
+                        for n, (t, c2) in dprof.items() if c2}
 
     # ---- end to end through the public API with host buffers
     host_prompt = torch.tensor(prompt_np).pin_memory()
@@ -391,7 +402,8 @@ def run_gpu(args):
                       "l2": "not flushed: each step streams 575 MB of weights and ~200 MB of "
                             "activations, > 126 MB L2"},
            "roofline": roofline, "gpu_launches": int(n_launch * args.steps),
-           "clocks": clk.summary(), "e2e": e2e, "per_k": per_k, "breakdown": breakdown}
+           "clocks": clk.summary(), "e2e": e2e, "per_k": per_k, "breakdown": breakdown,
+           "decode_breakdown_eager": decode_breakdown}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(K, budget_s=args.cpu_budget)
     if rank == 0:

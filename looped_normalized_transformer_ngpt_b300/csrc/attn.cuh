@@ -511,7 +511,7 @@ namespace dory {
 // ready bf16 q^, k^, v and sigmoid(g).
 // ---------------------------------------------------------------------------
 constexpr int kDecStages = 2;
-constexpr int kDecMinTiles = 4;
+constexpr int kDecMinTiles = 2;
 
 struct DecAttnArgs {
   const float* y;                 // RAW: [B, ldy] fp32 projection rows
@@ -543,7 +543,7 @@ struct DecCfg {
   static constexpr int STAGE = 2 * KVB;
   static constexpr int MERGE = 4 * 16 * DH * 4;             // per-warp o for the merge
   static constexpr int RING = kDecStages * STAGE > MERGE ? kDecStages * STAGE : MERGE;
-  static constexpr size_t SMEM = QB + RING + 2 * DH * 4 + 4 * 16 * 2 * 4 + 64;
+  static constexpr size_t SMEM = QB + RING + 2 * DH * 4 + 4 * 16 * 2 * 4 + 64 + kDecMaxG * DH * 4;
 };
 
 template <int DH, bool RAW>
@@ -559,6 +559,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
   float* sL = sM + 64;                                        // [4][16]
   int* sFlag = reinterpret_cast<int*>(sL + 64);
   float* sCur = reinterpret_cast<float*>(sFlag + 1);          // [8] new-token score per head
+  float* sGate = sCur + 8;                                    // [G][DH] sigmoid(g)
   const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -610,6 +611,23 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
       const int r = idx / CH, c = idx % CH;
       if (r >= G) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sQ) + swz_off<DH>(r, c)) =
           make_uint4(0u, 0u, 0u, 0u);
+    }
+    // gate of the G heads (needed only by the item that merges, but its
+    // load overlaps the rest of the prologue here instead of lengthening the
+    // merge at the end)
+    for (int idx = tid; idx < G * DH; idx += 128) {
+      const int r = idx / DH, dd = idx % DH;
+      float gt;
+      if (RAW) {
+        float gr = 0.f;
+        const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
+                          (kvh * G + r) * DH + dd;
+        for (int p = 0; p < a.n_parts; ++p) gr += yg[p * a.part_stride];
+        gt = 1.0f / (1.0f + __expf(-gr));
+      } else {
+        gt = __bfloat162float(a.gate[((long long)b * a.n_q + kvh * G + r) * DH + dd]);
+      }
+      sGate[idx] = gt;
     }
     for (int hh = warp; hh < G + 2; hh += 4) {
       // hh < G: query head kvh * G + hh; hh == G: key; hh == G + 1: value
@@ -872,17 +890,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
         acc += wr[sp] * o0 + wr[sp + 1] * o1 + wr[sp + 2] * o2 + wr[sp + 3] * o3;
       }
       for (; sp < NS; ++sp) acc += wr[sp] * __ldcg(po + sp * DH);
-      float gt;
-      if (RAW) {
-        float gr = 0.f;
-        const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
-                          (kvh * G + r) * DH + dd;
-        for (int p = 0; p < a.n_parts; ++p) gr += yg[p * a.part_stride];
-        gt = 1.0f / (1.0f + __expf(-gr));
-      } else {
-        gt = __bfloat162float(a.gate[bh * DH + dd]);
-      }
-      a.out[bh * DH + dd] = __float2bfloat16_rn(acc * sM[r] * gt);
+      a.out[bh * DH + dd] = __float2bfloat16_rn(acc * sM[r] * sGate[idx]);
     }
     if (tid == 0) a.counter[b * a.n_kv + kvh] = 0;
   }
