@@ -211,9 +211,10 @@ int num_sms() {
 }
 
 template <int BN, int EPI>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cudaStream_t st) {
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cudaStream_t st,
+                const EpiMaps* maps = nullptr) {
   static bool attr = false;
-  using Cf = GemmCfg<BN>;
+  using Cf = GemmCfg<BN, EPI>;
   if (!attr) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Cf::SMEM) != cudaSuccess)
@@ -229,8 +230,15 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
   const int tiles = args.tiles_m * args.tiles_n * args.k_splits;
   if (tiles == 0) return DORY_OK;
   const int grid = tiles < num_sms() ? tiles : num_sms();
+  EpiMaps em;
+  if (maps) {
+    em = *maps;
+  } else {
+    std::memset(&em, 0, sizeof(em));
+    if (Cf::STAGED) return DORY_EINVAL;            // the staged epilogue needs its maps
+  }
   return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM, st, ta, tb,
-                  args) ==
+                  args, em) ==
                  cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
@@ -791,7 +799,7 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
 // at once.
 int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
               const CUtensorMap& tm_hb, const CUtensorMap& tm_att, const CUtensorMap& tm_m,
-              StepState& s, cudaStream_t st) {
+              const EpiMaps& em, StepState& s, cudaStream_t st) {
   const dory_config& c = m->cfg;
   const dory_layer_weights& w = m->layers[l];
   const int M = B * C;
@@ -843,7 +851,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
                     : DORY_ECUDA));
   } else {
     pb(m, DORY_K_QKVG_GEMM, st);
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st)));
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_QKVG>(tm_hb, m->tm_qkvg[l], ga, st, &em)));
   }
 
   // attention over cached + current keys
@@ -1023,6 +1031,14 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       !encode_bf16(&tm_att, m->ws + m->L.att, M, hq, hq, box) ||
       !encode_bf16(&tm_m, m->ws + m->L.m, M, c.ffn, c.ffn, box))
     return DORY_ECUDA;
+  // destinations of the staged QKV+gate epilogue (q, k, v, sigmoid(g))
+  EpiMaps em;
+  const int hk = c.n_kv * c.head_dim;
+  if (!encode_bf16(&em.q, m->ws + m->L.q, M, hq, hq, 128) ||
+      !encode_bf16(&em.k, m->ws + m->L.k, M, hk, hk, 128) ||
+      !encode_bf16(&em.v, m->ws + m->L.v, M, hk, hk, 128) ||
+      !encode_bf16(&em.g, m->ws + m->L.g, M, hq, hq, 128))
+    return DORY_ECUDA;
 
   if (c.rope) {
     const int n = 2 * C * (c.head_dim / 2);
@@ -1104,7 +1120,7 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   auto layer = [&](int l, int slice, bool store) {
     if (decode) return run_layer_decode(m, l, slice, store, B, P0, s, st);
     if (batched) return run_layer_batched(m, l, slice, store, B, P0, tm_hb, tm_att, tm_m, s, st);
-    return run_layer(m, l, slice, store, B, C, P0, tm_hb, tm_att, tm_m, s, st);
+    return run_layer(m, l, slice, store, B, C, P0, tm_hb, tm_att, tm_m, em, s, st);
   };
   for (int l = 0; l < c.n_in; ++l) DORY_TRY(layer(l, 0, true));
   if (c.n_rec > 0) {

@@ -62,15 +62,25 @@ struct GemmArgs {
   long long part_stride;
 };
 
-template <int BN>
+template <int BN, int EPI = 0>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  // the QKV+gate epilogue stages its bf16 output tile (2 x 128 x 128) in
+  // shared memory for TMA stores, which costs one stage of the ring
+  static constexpr bool STAGED = EPI == 1 && BN == 256;
+  static constexpr int STAGES = STAGED ? 3 : (BN == 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t OUT_BYTES = STAGED ? 2 * 128 * 128 * 2 : 0;
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
+};
+
+// Destination maps of the staged QKV+gate epilogue: bf16 [M, heads x 128]
+// outputs loaded as {64 columns, 128 rows} boxes with the 128-byte swizzle.
+struct EpiMaps {
+  CUtensorMap q, k, v, g;
 };
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
@@ -281,19 +291,127 @@ __device__ __forceinline__ void epi_parts(const GemmArgs& a, uint32_t tacc, int 
   }
 }
 
+// QKV+gate epilogue for head_dim 128 through shared memory: this thread's
+// row of the head block (RoPE / q-k norm / s_qk, copy, or sigmoid applied)
+// goes into the 128 x 128 staging tile in the 128-byte swizzled layout; one
+// thread of the 4-warp half then writes the tile with two TMA stores (whole
+// 128-byte rows instead of 16-byte pieces of 128 different rows).
+__device__ __forceinline__ void epi_qkvg_staged(const GemmArgs& a, const EpiMaps& maps,
+                                                uint32_t tacc, int row, int rloc, int n0, int hc,
+                                                uint8_t* stage, int half, bool leader) {
+  if (n0 + hc >= a.N) return;                          // uniform for the half
+  const int head = (n0 + hc) / 128;
+  const int nq = a.n_q, nkv = a.n_kv;
+  const bool row_ok = row < a.M;
+  const int t = row_ok ? row % a.rows_per_seq : 0;
+  // staging tile free (its previous TMA store has read it)
+  if (leader) bulk_wait_read0();
+  named_bar(1 + half, 128);
+  auto put16 = [&](int col, const uint32_t* bits) {   // 16 values at tile column col
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(bits[i]);
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+      const int c = col + 8 * h8;                      // 8-element chunk start
+      uint4 u;
+      u.x = pack_bf16x2(v[8 * h8 + 0], v[8 * h8 + 1]);
+      u.y = pack_bf16x2(v[8 * h8 + 2], v[8 * h8 + 3]);
+      u.z = pack_bf16x2(v[8 * h8 + 4], v[8 * h8 + 5]);
+      u.w = pack_bf16x2(v[8 * h8 + 6], v[8 * h8 + 7]);
+      const int region = c >> 6, chunk = (c & 63) >> 3;
+      *reinterpret_cast<uint4*>(stage + region * 16384 + rloc * 128 +
+                                ((chunk ^ (rloc & 7)) << 4)) = u;
+    }
+  };
+  const CUtensorMap* map;
+  int x0;
+  if (head < nq + nkv) {
+    map = head < nq ? &maps.q : &maps.k;
+    x0 = (head < nq ? head : head - nq) * 128;
+    const float2* cs_row = a.rope ? a.rope + (long long)t * 64 : nullptr;
+    float2 cs[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) cs[i] = (cs_row && row_ok) ? cs_row[i] : make_float2(1.f, 0.f);
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 64) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_nowait(tacc + hc + c, r0);
+      tmem_ld32_nowait(tacc + hc + c + 32, r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float u0 = __uint_as_float(r0[i]), u1 = __uint_as_float(r1[i]);
+        ss += u0 * u0 + u1 * u1;
+      }
+    }
+    const float inv = 1.0f / sqrtf(fmaxf(ss, 1e-12f));
+#pragma unroll 1
+    for (int hp = 0; hp < 2; ++hp) {                   // pairs (i, i + 64)
+      uint32_t r1[32], r2[32];
+      tmem_ld32_nowait(tacc + hc + 32 * hp, r1);
+      tmem_ld32_nowait(tacc + hc + 64 + 32 * hp, r2);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float u1 = __uint_as_float(r1[i]), u2 = __uint_as_float(r2[i]);
+        const float y1 = u1 * cs[i].x - u2 * cs[i].y;
+        const float y2 = u2 * cs[i].x + u1 * cs[i].y;
+        r1[i] = __float_as_uint(y1 * inv * a.s_qk[32 * hp + i]);
+        r2[i] = __float_as_uint(y2 * inv * a.s_qk[64 + 32 * hp + i]);
+      }
+      if (hp == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          cs[i] = (cs_row && row_ok) ? cs_row[32 + i] : make_float2(1.f, 0.f);
+      }
+      put16(32 * hp, r1);
+      put16(32 * hp + 16, r1 + 16);
+      put16(64 + 32 * hp, r2);
+      put16(64 + 32 * hp + 16, r2 + 16);
+    }
+  } else {
+    const bool is_v = head < nq + 2 * nkv;
+    map = is_v ? &maps.v : &maps.g;
+    x0 = (is_v ? head - nq - nkv : head - nq - 2 * nkv) * 128;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t r0[32];
+      tmem_ld32_nowait(tacc + hc + c, r0);
+      tmem_wait_ld();
+      if (!is_v) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r0[i] = __float_as_uint(sigmoidf_(__uint_as_float(r0[i])));
+      }
+      put16(c, r0);
+      put16(c + 16, r0 + 16);
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar(1 + half, 128);
+  if (leader) {
+    const int m0 = row - rloc;                         // first row of the tile
+    tma_store_2d(map, stage, x0, m0);
+    tma_store_2d(map, stage + 16384, x0 + 64, m0);
+    bulk_commit();
+  }
+}
+
 // ------------------------------------------------------------- the kernel
 constexpr int kGemmThreads = 320;   // producer, MMA, 8 epilogue warps
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args) {
-  using C = GemmCfg<BN>;
+                   const GemmArgs args, const __grid_constant__ EpiMaps maps) {
+  using C = GemmCfg<BN, EPI>;
   constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* out_stage = smem + STAGES * C::STAGE_BYTES;          // STAGED: 2 x 32 KB
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;   // [2]
   uint64_t* tempty_bar = tfull_bar + 2;       // [2]
@@ -426,12 +544,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int chalf = (warp - 2) >> 2;            // which half of the columns
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+    // tcgen05.ld is warp-collective and the staged epilogue synchronises its
+    // 4-warp half on a hardware barrier, so the go / stop decision for a tile
+    // is made uniform across the warp (across the half when staged)
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      // tcgen05.ld is warp-collective: the warp proceeds or leaves as a whole
-      const bool ready = mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI);
-      if (!__all_sync(0xffffffffu, ready)) {
+      bool ready = !*abort_flag &&
+                   mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI);
+      ready = C::STAGED ? named_bar_and(1 + chalf, 128, ready) : __all_sync(0xffffffffu, ready);
+      if (!ready) {
         *abort_flag = 1;
         break;
       }
@@ -443,13 +565,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr int CW = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 2;   // columns per half
       const int c_lo = chalf * CW, c_hi = c_lo + CW;
       if (EPI == EPI_F32) epi_f32<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
-      if (EPI == EPI_QKVG) epi_qkvg<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      if (EPI == EPI_QKVG) {
+        if (C::STAGED && args.head_dim == 128)
+          epi_qkvg_staged(args, maps, tacc, row, quarter * 32 + lane, tn * BN, c_lo,
+                          out_stage + chalf * 32768, chalf, (warp & 3) == 2 && lane == 0);
+        else
+          epi_qkvg<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      }
       if (EPI == EPI_SWIGLU) epi_swiglu<BN>(args, tacc, row, tn, c_lo, c_hi);
       if (EPI == EPI_PARTS)
         epi_parts<BN>(args, tacc, row, tn * BN, tile / (args.tiles_m * args.tiles_n), c_lo, c_hi);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
+    // staged stores must have completed before the CTA (and its shared
+    // memory) goes away
+    if (C::STAGED && (warp & 3) == 2 && lane == 0) bulk_wait0();
   }
 
   if (*abort_flag) {
