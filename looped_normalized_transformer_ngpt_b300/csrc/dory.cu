@@ -43,7 +43,8 @@ constexpr int kSwapMaxM = 128;      // batched decode through the swapped GEMM u
 constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 
 struct WsLayout {
-  size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, gy, dec_o,
+  size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, ropet_swa,
+      ropet_full, gy, dec_o,
       dec_ml, dec_cnt, parts, mk_tab, mk_bar, total;
 };
 
@@ -73,6 +74,8 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.m = take(M * (size_t)c.ffn * 2);
   L.rope_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);
   L.rope_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
+  L.ropet_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);    // transposed copies
+  L.ropet_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
   // few-row projections (decode): fp32 output of the QKV+gate / up+gate GEMV
   const size_t nq = (size_t)(2 * c.n_q + 2 * c.n_kv) * c.head_dim;
   const size_t wide = nq > 2 * (size_t)c.ffn ? nq : 2 * (size_t)c.ffn;
@@ -151,6 +154,22 @@ bool get_encoder() {
 
 // Row-major bf16 matrix [rows, cols] with row stride ld (elements), loaded
 // as 64-column x box_rows boxes with the 128-byte swizzle.
+// fp32 matrix [rows][cols] (row stride ld elements) written as {32, 128}
+// boxes with the 128-byte swizzle (staged fp32 GEMM epilogue).
+bool encode_f32_out(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint64_t ld) {
+  if (!get_encoder()) return false;
+  if (((uintptr_t)base & 15) || (ld * 4) % 16) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                  uint32_t box_rows) {
   if (!get_encoder()) return false;
@@ -235,8 +254,11 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
     em = *maps;
   } else {
     std::memset(&em, 0, sizeof(em));
-    if (Cf::STAGED) return DORY_EINVAL;            // the staged epilogue needs its maps
+    // the head_dim-128 QKV+gate epilogue always writes through its maps
+    if (EPI == EPI_QKVG && Cf::STAGED && args.head_dim == 128) return DORY_EINVAL;
   }
+  // fp32 / SwiGLU: staged stores when the caller described the output
+  args.staged = maps ? 1 : 0;
   return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM, st, ta, tb,
                   args, em) ==
                  cudaSuccess
@@ -824,6 +846,9 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   ga.head_dim = c.head_dim;
   ga.s_qk = w.s_qk;
   ga.rope = c.rope ? wsp<float2>(m, full ? m->L.rope_full : m->L.rope_swa) : nullptr;
+  ga.rope_t = c.rope && c.head_dim == 128
+                  ? wsp<float4>(m, full ? m->L.ropet_full : m->L.ropet_swa)
+                  : nullptr;
   ga.rows_per_seq = C;
   const bool few = M <= kGemvMaxM;
   __nv_bfloat16* hb = wsp<__nv_bfloat16>(m, m->L.hb);
@@ -941,7 +966,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.ldy = c.d;
     DORY_TRY(pe(m, st, launch_gemv(g, st)));
   } else {
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st)));
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st, &em)));
   }
   DORY_TRY(ngpt_update(m, M, h, w.alpha_attn, st));
 
@@ -968,7 +993,9 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.ldm = c.ffn;
     DORY_TRY(pe(m, st, launch_gemv(g, st)));
   } else {
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st)));
+    EpiMaps emm = em;                              // m is written through its load map
+    emm.out = tm_m;
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st, &emm)));
   }
   GemmArgs gd{};
   gd.M = M;
@@ -990,7 +1017,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.ldy = c.d;
     DORY_TRY(pe(m, st, launch_gemv(g, st)));
   } else {
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st)));
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st, &em)));
   }
   return ngpt_update(m, M, h, w.alpha_mlp, st);
 }
@@ -1037,7 +1064,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   if (!encode_bf16(&em.q, m->ws + m->L.q, M, hq, hq, 128) ||
       !encode_bf16(&em.k, m->ws + m->L.k, M, hk, hk, 128) ||
       !encode_bf16(&em.v, m->ws + m->L.v, M, hk, hk, 128) ||
-      !encode_bf16(&em.g, m->ws + m->L.g, M, hq, hq, 128))
+      !encode_bf16(&em.g, m->ws + m->L.g, M, hq, hq, 128) ||
+      !encode_f32_out(&em.out, m->ws + m->L.y32, M, c.d, c.d))   // output / down projections
     return DORY_ECUDA;
 
   if (c.rope) {
@@ -1046,7 +1074,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     pb(m, DORY_K_ROPE, st);
     DORY_TRY(pe(m, st,
                 launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st,
-                         wsp<float2>(m, m->L.rope_swa), wsp<float2>(m, m->L.rope_full), C, P0,
+                         wsp<float2>(m, m->L.rope_swa), wsp<float2>(m, m->L.rope_full),
+                         wsp<float2>(m, m->L.ropet_swa), wsp<float2>(m, m->L.ropet_full), C, P0,
                          c.head_dim, (double)c.rope_base_swa, (double)c.rope_base_full) ==
                         cudaSuccess
                     ? DORY_OK
@@ -1168,8 +1197,11 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       gl.M = B;
       gl.ldo = ld_seq * c.vocab;
       gl.out = logits + (long long)t_out0 * c.vocab;
+      EpiMaps el;
+      const bool st_ok = encode_f32_out(&el.out, gl.out, B, c.vocab, gl.ldo);
       pb(m, DORY_K_LM_HEAD, st);
-      DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_last, m->tm_embed_out, gl, st)));
+      DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_last, m->tm_embed_out, gl, st,
+                                                        st_ok ? &el : nullptr)));
     } else {
       for (int b = 0; b < B; ++b) {
         CUtensorMap tm_rows;
@@ -1178,8 +1210,11 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
           return DORY_ECUDA;
         gl.M = n_logit_rows;
         gl.out = logits + ((long long)b * ld_seq + t_out0) * c.vocab;
+        EpiMaps el;
+        const bool st_ok = encode_f32_out(&el.out, gl.out, n_logit_rows, c.vocab, gl.ldo);
         pb(m, DORY_K_LM_HEAD, st);
-        DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_rows, m->tm_embed_out, gl, st)));
+        DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_rows, m->tm_embed_out, gl, st,
+                                                          st_ok ? &el : nullptr)));
       }
     }
   }
@@ -1509,7 +1544,11 @@ int dory_debug_gemm(const void* A, const void* B, float* C, int M, int N, int K,
   g.K = K;
   g.out = C;
   g.ldo = ldc;
-  return launch_gemm<kGemmBN, EPI_F32>(ta, tb, g, static_cast<cudaStream_t>(stream));
+  // output written through a TMA map where its alignment allows, else directly
+  EpiMaps eo;
+  const bool st_ok = encode_f32_out(&eo.out, C, M, N, ldc);
+  return launch_gemm<kGemmBN, EPI_F32>(ta, tb, g, static_cast<cudaStream_t>(stream),
+                                       st_ok ? &eo : nullptr);
 }
 
 size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim) {

@@ -25,6 +25,10 @@
 //               as bf16 in head-major rows.
 //   EPI_SWIGLU  B tile = 64/128 rows of W_up and the same rows of W_sl; the
 //               epilogue forms m = u * SiLU(v) and stores m as bf16.
+// With BN = 256 these three stage their output in shared memory in the
+// 128-byte swizzled layout and one thread of each 4-warp half writes it with
+// TMA tensor stores (whole 128-byte rows; a thread-per-row store pattern
+// touches 32 rows per instruction).
 //   EPI_PARTS   swapped operands for few activation rows (decode batches):
 //               A = 128 weight rows, B = BN activation rows, and K split into
 //               k_splits ranges so that even a 2048-wide projection spreads
@@ -52,6 +56,10 @@ struct GemmArgs {
   int n_q, n_kv, head_dim;
   const float* s_qk;
   const float2* rope;       // [rows_per_seq][head_dim / 2] (cos, sin), or null
+  // the same table transposed for the staged head_dim-128 epilogue, two
+  // frequencies per entry: rope_t[j * rows_per_seq + t] =
+  // (cos, sin of frequency 2j, cos, sin of frequency 2j + 1), or null
+  const float4* rope_t;
   int rows_per_seq;
   // EPI_SWIGLU
   __nv_bfloat16* m_out;
@@ -60,30 +68,46 @@ struct GemmArgs {
   // out[split * part_stride + n * ldo + m]
   int k_splits;
   long long part_stride;
+  // EPI_F32 / EPI_SWIGLU with BN = 256: 1 if EpiMaps::out describes the
+  // output (then it is written through shared memory), else direct stores
+  int staged;
 };
 
 template <int BN, int EPI = 0>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
-  // the QKV+gate epilogue stages its bf16 output tile (2 x 128 x 128) in
-  // shared memory for TMA stores, which costs one stage of the ring
-  static constexpr bool STAGED = EPI == 1 && BN == 256;
-  static constexpr int STAGES = STAGED ? 3 : (BN == 256 ? 4 : 6);
+  // Staged epilogues keep their output tile in shared memory for TMA stores:
+  // QKV+gate 2 halves x 128 x 128 bf16 (64 KB), fp32 2 halves x 2 buffers x
+  // {32 x 128} fp32 (64 KB), SwiGLU 2 halves x {64 x 128} bf16 (32 KB).
+  // The first two cost a stage of the operand ring.
+  static constexpr bool STAGED = BN == 256 && EPI != 3;
+  static constexpr uint32_t OUT_BYTES = !STAGED ? 0 : (EPI == 2 ? 2 * 16384 : 4 * 16384);
+  static constexpr int STAGES = STAGED ? (EPI == 2 ? 4 : 3) : (BN == 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t OUT_BYTES = STAGED ? 2 * 128 * 128 * 2 : 0;
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
+  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t SQK_BYTES = EPI == 1 ? 512 : 0;   // s_qk of a 128-wide head
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES + 1024;
 };
 
-// Destination maps of the staged QKV+gate epilogue: bf16 [M, heads x 128]
-// outputs loaded as {64 columns, 128 rows} boxes with the 128-byte swizzle.
+// Destination maps of the staged epilogues, all with the 128-byte swizzle:
+//   QKV+gate  q, k, v, g: bf16 [M, heads x 128], {64 columns, 128 rows} boxes;
+//   fp32      out: fp32 [M, N], {32 columns, 128 rows} boxes;
+//   SwiGLU    out: bf16 [M, ffn], {64 columns, 128 rows} boxes.
 struct EpiMaps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap q, k, v, g, out;
 };
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// epilogue form: reciprocal instead of a division
+__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+
+// 16-byte chunk `chunk` (0..7) of row `r` of a 128-byte swizzled box
+__device__ __forceinline__ uint4* sw128_chunk(uint8_t* box, int r, int chunk) {
+  return reinterpret_cast<uint4*>(box + r * 128 + ((chunk ^ (r & 7)) << 4));
+}
 
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
   uint4 a, b;
@@ -162,60 +186,11 @@ __device__ __forceinline__ void epi_qkvg(const GemmArgs& a, uint32_t tacc, int r
     if (gcol >= a.N) break;
     const int head = gcol / dh;
     if (head < nq + nkv) {
-      // q or k head: RoPE, per-head L2 norm, s_qk.  Latency matters here (the
-      // GEMM is epilogue-bound otherwise): TMEM is read 32 columns at a time
-      // with one wait per pair of loads, and the RoPE-table row of this
-      // position is fetched in two halves, each issued before the work that
-      // precedes its use.
+      // q or k head: RoPE, per-head L2 norm, s_qk (head_dim 128 takes the
+      // staged epilogue instead)
       const bool is_q = head < nq;
       __nv_bfloat16* dst = is_q ? a.q + ((long long)row * nq + head) * dh
                                 : a.k + ((long long)row * nkv + (head - nq)) * dh;
-      if (dh == 128 && a.rope) {
-        const float2* cs_row = a.rope + (long long)t * 64;
-        float2 cs[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) cs[i] = row_ok ? cs_row[i] : make_float2(1.f, 0.f);
-        float ss = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 64) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32_nowait(tacc + hc + c, r0);
-          tmem_ld32_nowait(tacc + hc + c + 32, r1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float u0 = __uint_as_float(r0[i]), u1 = __uint_as_float(r1[i]);
-            ss += u0 * u0 + u1 * u1;
-          }
-        }
-        const float inv = 1.0f / sqrtf(fmaxf(ss, 1e-12f));
-#pragma unroll 1
-        for (int hp = 0; hp < 2; ++hp) {              // pairs (i, i + 64), i in [32 hp, 32 hp + 32)
-          uint32_t r1[32], r2[32];
-          tmem_ld32_nowait(tacc + hc + 32 * hp, r1);
-          tmem_ld32_nowait(tacc + hc + 64 + 32 * hp, r2);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float u1 = __uint_as_float(r1[i]), u2 = __uint_as_float(r2[i]);
-            const float y1 = u1 * cs[i].x - u2 * cs[i].y;
-            const float y2 = u2 * cs[i].x + u1 * cs[i].y;
-            r1[i] = __float_as_uint(y1 * inv * a.s_qk[32 * hp + i]);
-            r2[i] = __float_as_uint(y2 * inv * a.s_qk[64 + 32 * hp + i]);
-          }
-          if (hp == 0) {                              // second half's table entries
-#pragma unroll
-            for (int i = 0; i < 32; ++i) cs[i] = row_ok ? cs_row[32 + i] : make_float2(1.f, 0.f);
-          }
-          if (row_ok) {
-            store_bf16x16_bits(dst + 32 * hp, r1);
-            store_bf16x16_bits(dst + 32 * hp + 16, r1 + 16);
-            store_bf16x16_bits(dst + 64 + 32 * hp, r2);
-            store_bf16x16_bits(dst + 64 + 32 * hp + 16, r2 + 16);
-          }
-        }
-        continue;
-      }
       float ss = 0.f;
 #pragma unroll 1
       for (int c = 0; c < dh; c += 16) {
@@ -294,34 +269,47 @@ __device__ __forceinline__ void epi_parts(const GemmArgs& a, uint32_t tacc, int 
 // QKV+gate epilogue for head_dim 128 through shared memory: this thread's
 // row of the head block (RoPE / q-k norm / s_qk, copy, or sigmoid applied)
 // goes into the 128 x 128 staging tile in the 128-byte swizzled layout; one
-// thread of the 4-warp half then writes the tile with two TMA stores (whole
-// 128-byte rows instead of 16-byte pieces of 128 different rows).
+// thread of the 4-warp half then writes the tile with two TMA stores.
+//
+// RoPE (cos, sin) pairs come from the transposed table, so the 32 lanes of
+// a warp (32 consecutive rows, i.e. positions) read 512 contiguous bytes per
+// load.  The rotation runs in four passes of 16 pairs; the first pass's
+// pairs are fetched before the accumulator wait, each later pass's during
+// the pass before it.  s_qk is read from shared memory.
+__device__ __forceinline__ bool qkvg_rope_head(const GemmArgs& a, int gcol) {
+  return a.rope_t != nullptr && gcol / 128 < a.n_q + a.n_kv && gcol < a.N;
+}
+
+// (cos, sin) of frequencies [16 part, 16 part + 16) at this row's position
+__device__ __forceinline__ void qkvg_rope_load(const GemmArgs& a, int row, bool use, int part,
+                                               float4 (&cs)[8]) {
+  const float4* p = a.rope_t + (use ? row % a.rows_per_seq : 0);
+  const long long stride = a.rows_per_seq;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    cs[j] = use ? __ldg(p + (8 * part + j) * stride) : make_float4(1.f, 0.f, 1.f, 0.f);
+}
+
 __device__ __forceinline__ void epi_qkvg_staged(const GemmArgs& a, const EpiMaps& maps,
-                                                uint32_t tacc, int row, int rloc, int n0, int hc,
-                                                uint8_t* stage, int half, bool leader) {
+                                                const float* sqk, uint32_t tacc, int row,
+                                                int rloc, int n0, int hc, uint8_t* stage, int half,
+                                                bool leader, float4 (&cs)[8]) {
   if (n0 + hc >= a.N) return;                          // uniform for the half
   const int head = (n0 + hc) / 128;
   const int nq = a.n_q, nkv = a.n_kv;
-  const bool row_ok = row < a.M;
-  const int t = row_ok ? row % a.rows_per_seq : 0;
   // staging tile free (its previous TMA store has read it)
   if (leader) bulk_wait_read0();
   named_bar(1 + half, 128);
   auto put16 = [&](int col, const uint32_t* bits) {   // 16 values at tile column col
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(bits[i]);
 #pragma unroll
     for (int h8 = 0; h8 < 2; ++h8) {
       const int c = col + 8 * h8;                      // 8-element chunk start
       uint4 u;
-      u.x = pack_bf16x2(v[8 * h8 + 0], v[8 * h8 + 1]);
-      u.y = pack_bf16x2(v[8 * h8 + 2], v[8 * h8 + 3]);
-      u.z = pack_bf16x2(v[8 * h8 + 4], v[8 * h8 + 5]);
-      u.w = pack_bf16x2(v[8 * h8 + 6], v[8 * h8 + 7]);
-      const int region = c >> 6, chunk = (c & 63) >> 3;
-      *reinterpret_cast<uint4*>(stage + region * 16384 + rloc * 128 +
-                                ((chunk ^ (rloc & 7)) << 4)) = u;
+      u.x = pack_bf16x2(__uint_as_float(bits[8 * h8 + 0]), __uint_as_float(bits[8 * h8 + 1]));
+      u.y = pack_bf16x2(__uint_as_float(bits[8 * h8 + 2]), __uint_as_float(bits[8 * h8 + 3]));
+      u.z = pack_bf16x2(__uint_as_float(bits[8 * h8 + 4]), __uint_as_float(bits[8 * h8 + 5]));
+      u.w = pack_bf16x2(__uint_as_float(bits[8 * h8 + 6]), __uint_as_float(bits[8 * h8 + 7]));
+      *sw128_chunk(stage + (c >> 6) * 16384, rloc, (c & 63) >> 3) = u;
     }
   };
   const CUtensorMap* map;
@@ -329,10 +317,7 @@ __device__ __forceinline__ void epi_qkvg_staged(const GemmArgs& a, const EpiMaps
   if (head < nq + nkv) {
     map = head < nq ? &maps.q : &maps.k;
     x0 = (head < nq ? head : head - nq) * 128;
-    const float2* cs_row = a.rope ? a.rope + (long long)t * 64 : nullptr;
-    float2 cs[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) cs[i] = (cs_row && row_ok) ? cs_row[i] : make_float2(1.f, 0.f);
+    const bool use = qkvg_rope_head(a, n0 + hc) && row < a.M;
     float ss = 0.f;
 #pragma unroll 1
     for (int c = 0; c < 128; c += 64) {
@@ -343,49 +328,59 @@ __device__ __forceinline__ void epi_qkvg_staged(const GemmArgs& a, const EpiMaps
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float u0 = __uint_as_float(r0[i]), u1 = __uint_as_float(r1[i]);
-        ss += u0 * u0 + u1 * u1;
+        ss = fmaf(u0, u0, ss);
+        ss = fmaf(u1, u1, ss);
       }
     }
     const float inv = 1.0f / sqrtf(fmaxf(ss, 1e-12f));
+    const float4* sq4 = reinterpret_cast<const float4*>(sqk);
 #pragma unroll 1
-    for (int hp = 0; hp < 2; ++hp) {                   // pairs (i, i + 64)
-      uint32_t r1[32], r2[32];
-      tmem_ld32_nowait(tacc + hc + 32 * hp, r1);
-      tmem_ld32_nowait(tacc + hc + 64 + 32 * hp, r2);
+    for (int qp = 0; qp < 4; ++qp) {                   // pairs (i, i + 64), i in [16 qp, 16 qp + 16)
+      uint32_t r1[16], r2[16];
+      tmem_ld16_nowait(tacc + hc + 16 * qp, r1);
+      tmem_ld16_nowait(tacc + hc + 64 + 16 * qp, r2);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float u1 = __uint_as_float(r1[i]), u2 = __uint_as_float(r2[i]);
-        const float y1 = u1 * cs[i].x - u2 * cs[i].y;
-        const float y2 = u2 * cs[i].x + u1 * cs[i].y;
-        r1[i] = __float_as_uint(y1 * inv * a.s_qk[32 * hp + i]);
-        r2[i] = __float_as_uint(y2 * inv * a.s_qk[64 + 32 * hp + i]);
-      }
-      if (hp == 0) {
+      for (int j = 0; j < 4; ++j) {                    // 4 pairs per step
+        const float4 s1 = sq4[4 * qp + j], s2 = sq4[16 + 4 * qp + j];
+        const float sa[4] = {s1.x, s1.y, s1.z, s1.w}, sb[4] = {s2.x, s2.y, s2.z, s2.w};
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          cs[i] = (cs_row && row_ok) ? cs_row[32 + i] : make_float2(1.f, 0.f);
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * j + e;
+          const float4 c4 = cs[i >> 1];
+          const float co = (i & 1) ? c4.z : c4.x, si = (i & 1) ? c4.w : c4.y;
+          const float u1 = __uint_as_float(r1[i]), u2 = __uint_as_float(r2[i]);
+          const float y1 = u1 * co - u2 * si;
+          const float y2 = u2 * co + u1 * si;
+          r1[i] = __float_as_uint(y1 * (inv * sa[e]));
+          r2[i] = __float_as_uint(y2 * (inv * sb[e]));
+        }
       }
-      put16(32 * hp, r1);
-      put16(32 * hp + 16, r1 + 16);
-      put16(64 + 32 * hp, r2);
-      put16(64 + 32 * hp + 16, r2 + 16);
+      if (qp < 3) qkvg_rope_load(a, row, use, qp + 1, cs);   // next pass's pairs
+      put16(16 * qp, r1);
+      put16(64 + 16 * qp, r2);
     }
   } else {
     const bool is_v = head < nq + 2 * nkv;
     map = is_v ? &maps.v : &maps.g;
     x0 = (is_v ? head - nq - nkv : head - nq - 2 * nkv) * 128;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-      uint32_t r0[32];
+    for (int c = 0; c < 128; c += 64) {
+      uint32_t r0[32], r1[32];
       tmem_ld32_nowait(tacc + hc + c, r0);
+      tmem_ld32_nowait(tacc + hc + c + 32, r1);
       tmem_wait_ld();
       if (!is_v) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r0[i] = __float_as_uint(sigmoidf_(__uint_as_float(r0[i])));
+        for (int i = 0; i < 32; ++i) {
+          r0[i] = __float_as_uint(sigmoid_fast(__uint_as_float(r0[i])));
+          r1[i] = __float_as_uint(sigmoid_fast(__uint_as_float(r1[i])));
+        }
       }
       put16(c, r0);
       put16(c + 16, r0 + 16);
+      put16(c + 32, r1);
+      put16(c + 48, r1 + 16);
     }
   }
   fence_proxy_async_smem();
@@ -394,6 +389,83 @@ __device__ __forceinline__ void epi_qkvg_staged(const GemmArgs& a, const EpiMaps
     const int m0 = row - rloc;                         // first row of the tile
     tma_store_2d(map, stage, x0, m0);
     tma_store_2d(map, stage + 16384, x0 + 64, m0);
+    bulk_commit();
+  }
+}
+
+// fp32 epilogue through shared memory, 32 columns at a time: each thread's
+// 32 values (one 128-byte row of a {32 x 128} fp32 box) go into one of the
+// half's two 16 KB buffers and the half's leader stores the box with TMA.
+// The buffers alternate (counter nst, kept across tiles); before the
+// barrier that publishes chunk j the leader waits until the store of chunk
+// j - 1 has read its buffer, which is the one chunk j + 1 writes.
+__device__ __forceinline__ void epi_f32_staged(const GemmArgs& a, const CUtensorMap* map,
+                                               uint32_t tacc, int rloc, int m0, int n0, int c_lo,
+                                               int c_hi, uint8_t* stage, int half, bool leader,
+                                               uint32_t& nst) {
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; c += 32) {
+    if (n0 + c >= a.N) break;                          // uniform for the half
+    uint32_t r[32];
+    tmem_ld32_nowait(tacc + c, r);
+    tmem_wait_ld();
+    if (a.col_scale) {
+      const int nvalid = min(32, a.N - n0 - c);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nvalid) r[i] = __float_as_uint(__uint_as_float(r[i]) * a.col_scale[n0 + c + i]);
+    }
+    uint8_t* buf = stage + (nst & 1) * 16384;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *sw128_chunk(buf, rloc, j) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();
+    if (leader) bulk_wait_read0();
+    named_bar(1 + half, 128);
+    if (leader) {
+      tma_store_2d(map, buf, n0 + c, m0);
+      bulk_commit();
+    }
+    ++nst;
+  }
+}
+
+// SwiGLU epilogue through shared memory: the half's 64 columns of m
+// (bf16, one 128-byte row per thread) go into its {64 x 128} box buffer,
+// stored by the half's leader with TMA.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_staged(const GemmArgs& a, const CUtensorMap* map,
+                                                  uint32_t tacc, int rloc, int m0, int tn,
+                                                  int c_lo, uint8_t* stage, int half,
+                                                  bool leader) {
+  constexpr int H = BN / 2;
+  const int col = tn * H + c_lo;                       // first column of m
+  if (col >= a.N / 2) return;                          // uniform for the half
+  if (leader) bulk_wait_read0();
+  named_bar(1 + half, 128);
+#pragma unroll 1
+  for (int c = 0; c < H / 2; c += 32) {
+    uint32_t u[32], v[32];
+    tmem_ld32_nowait(tacc + c_lo + c, u);
+    tmem_ld32_nowait(tacc + H + c_lo + c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float m[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float x = __uint_as_float(u[8 * q + i]), g = __uint_as_float(v[8 * q + i]);
+        m[i] = x * (g * sigmoid_fast(g));
+      }
+      *sw128_chunk(stage, rloc, (c >> 3) + q) =
+          make_uint4(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]), pack_bf16x2(m[4], m[5]),
+                     pack_bf16x2(m[6], m[7]));
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar(1 + half, 128);
+  if (leader) {
+    tma_store_2d(map, stage, col, m0);
     bulk_commit();
   }
 }
@@ -410,8 +482,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* out_stage = smem + STAGES * C::STAGE_BYTES;          // STAGED: 2 x 32 KB
+  uint8_t* out_stage = smem + STAGES * C::STAGE_BYTES;          // STAGED: OUT_BYTES
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES);
+  float* sqk = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES +
+                                        C::BAR_BYTES);               // EPI_QKVG: s_qk[128]
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;   // [2]
   uint64_t* tempty_bar = tfull_bar + 2;       // [2]
@@ -543,6 +617,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------ epilogue warps 2..9
     const int quarter = warp & 3;
     const int chalf = (warp - 2) >> 2;            // which half of the columns
+    const bool leader = (warp & 3) == 2 && lane == 0;   // one thread per half
+    constexpr int OUT_HALF = C::OUT_BYTES / 2;
+    uint8_t* my_stage = out_stage + chalf * OUT_HALF;
+    const bool staged = C::STAGED && (EPI == EPI_QKVG ? args.head_dim == 128 : args.staged != 0);
+    uint32_t nst = 0;                             // fp32: boxes this half has staged
+    if (EPI == EPI_QKVG && C::STAGED) {
+      const int e = threadIdx.x - 64;
+      if (e < 128) sqk[e] = args.s_qk && e < args.head_dim ? args.s_qk[e] : 1.0f;
+      named_bar(3, 256);
+    }
     int it = 0;
     // tcgen05.ld is warp-collective and the staged epilogue synchronises its
     // 4-warp half on a hardware barrier, so the go / stop decision for a tile
@@ -550,6 +634,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
+      const int tt = tile % (args.tiles_m * args.tiles_n);
+      const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
+      const int row = tm * BM + quarter * 32 + lane;
+      constexpr int CW = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 2;   // columns per half
+      const int c_lo = chalf * CW, c_hi = c_lo + CW;
+      // RoPE pairs of this row are fetched while the accumulator is computed
+      float4 cs[8];
+      if (EPI == EPI_QKVG && C::STAGED && staged)
+        qkvg_rope_load(args, row, qkvg_rope_head(args, tn * BN + c_lo) && row < args.M, 0, cs);
       bool ready = !*abort_flag &&
                    mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI);
       ready = C::STAGED ? named_bar_and(1 + chalf, 128, ready) : __all_sync(0xffffffffu, ready);
@@ -558,21 +651,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int tt = tile % (args.tiles_m * args.tiles_n);
-      const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
-      const int row = tm * BM + quarter * 32 + lane;
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
-      constexpr int CW = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 2;   // columns per half
-      const int c_lo = chalf * CW, c_hi = c_lo + CW;
-      if (EPI == EPI_F32) epi_f32<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      const int rloc = quarter * 32 + lane, m0 = tm * BM;
+      if (EPI == EPI_F32) {
+        if (C::STAGED && staged)
+          epi_f32_staged(args, &maps.out, tacc, rloc, m0, tn * BN, c_lo, c_hi, my_stage, chalf,
+                         leader, nst);
+        else
+          epi_f32<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
+      }
       if (EPI == EPI_QKVG) {
-        if (C::STAGED && args.head_dim == 128)
-          epi_qkvg_staged(args, maps, tacc, row, quarter * 32 + lane, tn * BN, c_lo,
-                          out_stage + chalf * 32768, chalf, (warp & 3) == 2 && lane == 0);
+        if (C::STAGED && staged)
+          epi_qkvg_staged(args, maps, sqk, tacc, row, rloc, tn * BN, c_lo, my_stage, chalf,
+                          leader, cs);
         else
           epi_qkvg<BN>(args, tacc, row, tn * BN, c_lo, c_hi);
       }
-      if (EPI == EPI_SWIGLU) epi_swiglu<BN>(args, tacc, row, tn, c_lo, c_hi);
+      if (EPI == EPI_SWIGLU) {
+        if (C::STAGED && staged)
+          epi_swiglu_staged<BN>(args, &maps.out, tacc, rloc, m0, tn, c_lo, my_stage, chalf,
+                                leader);
+        else
+          epi_swiglu<BN>(args, tacc, row, tn, c_lo, c_hi);
+      }
       if (EPI == EPI_PARTS)
         epi_parts<BN>(args, tacc, row, tn * BN, tile / (args.tiles_m * args.tiles_n), c_lo, c_hi);
       tc_fence_before();
@@ -580,7 +681,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     // staged stores must have completed before the CTA (and its shared
     // memory) goes away
-    if (C::STAGED && (warp & 3) == 2 && lane == 0) bulk_wait0();
+    if (C::STAGED && leader) bulk_wait0();
   }
 
   if (*abort_flag) {

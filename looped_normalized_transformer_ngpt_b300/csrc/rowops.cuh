@@ -345,9 +345,11 @@ __global__ void kv_write_kernel(const __nv_bfloat16* k_cur, const __nv_bfloat16*
 // RoPE tables for the positions of one call: tab_b[t][i] = (cos, sin) of
 // (P0 + t) * base_b^(-2i/dh) for the two bases (b = 0: sliding-window
 // layers, b = 1: full layers); the angle is formed and reduced mod 2 pi in
-// fp64 so long contexts keep full fp32 accuracy.
-__global__ void rope_table_kernel(float2* tab0, float2* tab1, int C, int P0, int dh, double base0,
-                                  double base1) {
+// fp64 so long contexts keep full fp32 accuracy.  tabt_b holds the same
+// pairs transposed, two frequencies per 16 bytes: tabt_b[(i / 2) C + t]
+// = pairs i & ~1 and i | 1 (coalesced reads across consecutive positions).
+__global__ void rope_table_kernel(float2* tab0, float2* tab1, float2* tabt0, float2* tabt1, int C,
+                                  int P0, int dh, double base0, double base1) {
   pdl_wait();
   pdl_trigger();
   const int half = dh / 2;
@@ -363,7 +365,9 @@ __global__ void rope_table_kernel(float2* tab0, float2* tab1, int C, int P0, int
     ang -= floor(ang / two_pi) * two_pi;
     double s, c;
     sincos(ang, &s, &c);
-    (which ? tab1 : tab0)[e] = make_float2((float)c, (float)s);
+    const float2 cs = make_float2((float)c, (float)s);
+    (which ? tab1 : tab0)[e] = cs;
+    (which ? tabt1 : tabt0)[((long long)(i >> 1) * C + t) * 2 + (i & 1)] = cs;
   }
 }
 
