@@ -11,21 +11,31 @@
 //
 // One CTA = (block of 128 / G query positions, kv head, sequence): its 128
 // rows are (position, head-in-group) pairs, so one K/V tile serves all G
-// heads.  112 KB of shared memory and 256 TMEM columns, so two CTAs share an
+// heads.  96 KB of shared memory and 256 TMEM columns, so two CTAs share an
 // SM and the tensor core works for one while the other runs its softmax.
-// Warp roles (192 threads):
-//   warp 0    TMA producer: the Q tile once (3-D box: 64 dims x G heads x
-//             128/G positions, two boxes for the 128 dims), then 64-key K and
-//             V tiles into a 2-stage ring (128-byte swizzle);
+// Warp roles (224 threads):
+//   warp 0    TMA producer of Q and K: the Q tile once per item (3-D box: 64
+//             dims x G heads x 128/G positions, two boxes for the 128 dims),
+//             then 64-key K tiles into a 2-stage ring (128-byte swizzle); a K
+//             stage is released when its S MMA completes, so K runs up to two
+//             tiles ahead of the softmax;
+//   warp 6    TMA producer of V: 64-key V tiles into their own 2-stage ring,
+//             a stage released when its PV MMA completes;
 //   warp 1    TMEM owner and MMA issuer: S_j = Q K_j^T (M = 128, N = 64,
-//             K = 128) into one of two TMEM S buffers, and O += P_j V_j (V as an
-//             MN-major operand) into the TMEM O accumulator;
-//   warps 2-5 softmax, one row per thread: S row from TMEM, mask, running max,
-//             P = exp2(S - max) written to shared memory as the bf16 K-major
-//             A operand of the PV MMA; O is rescaled in TMEM only when the
-//             running max rises by more than 8 (log2 units) - otherwise the
-//             stale max stays exact, since the same max scales P and the row
-//             sum; final O / sum * gate from TMEM to global.
+//             K = 128) into TMEM S buffer j % 2, and O += P_j V_j into the TMEM
+//             O accumulator with P_j read from TMEM (A operand) and V as an
+//             MN-major shared-memory operand;
+//   warps 2-5 softmax, one row per thread: S row from TMEM, mask (only on
+//             tiles that need one, decided once per tile), running max,
+//             P = exp2(S - max) packed to bf16 pairs and written back over the
+//             first 32 columns of the same S buffer (so P is double-buffered
+//             with S and the exponentials of tile j overlap the PV MMA of
+//             tile j - 1); O is rescaled in TMEM only when the running max
+//             rises by more than 8 (log2 units) - otherwise the stale max
+//             stays exact, since the same max scales P and the row sum; final
+//             O / sum * gate from TMEM to global.
+// One thread issues every MMA and the MMAs of one thread run in order, so
+// S_{j+2} (issued after PV_j) never overwrites P_j before PV_j has read it.
 // Key tiles are aligned to 64 positions and never mix cached and current
 // keys (the launcher requires P0 % 64 == 0 and 64-aligned ring sizes).
 // Every wait is bounded (status word + orderly exit).
@@ -54,31 +64,28 @@ struct AttnTcCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = 2 * QHALF;          // 2 stages
   static constexpr int V_OFF = K_OFF + 2 * KVTILE; // 2 stages
-  static constexpr int P_OFF = V_OFF + 2 * KVTILE; // 128 rows x 64 keys bf16
-  static constexpr int BAR_OFF = P_OFF + 128 * BK * 2;
+  static constexpr int BAR_OFF = V_OFF + 2 * KVTILE;
   static constexpr size_t SMEM = BAR_OFF + 256;    // two CTAs fit on one SM
-  static constexpr uint32_t TMEM_COLS = 256;       // S0 | S1 (64 each) | O (128)
+  // S0 | S1 (64 fp32 columns each; P_j as 32 columns of bf16 pairs over S_j)
+  // | O (128)
+  static constexpr uint32_t TMEM_COLS = 256;
 };
 
 // tensor maps: q (3-D: dim, head, token), k/v current (3-D: dim, kv head,
-// token), k/v cache (2-D: dim, slot row).
-template <bool FROM_CACHE>
-__device__ __forceinline__ void attn_tc_load_kv(uint8_t* dst_k, uint8_t* dst_v,
-                                                const CUtensorMap* tk, const CUtensorMap* tv,
-                                                uint64_t* bar, int j0, int b, int kvh,
-                                                const AttnTcArgs& a) {
-  if (FROM_CACHE) {
+// token), k/v cache (2-D: dim, slot row).  One 64-key K or V tile (both
+// 64-dim halves) starting at key position j0: from the cache slice below P0,
+// else from this call's projections.
+__device__ __forceinline__ void attn_tc_load_tile(uint8_t* dst, const CUtensorMap* t_cache,
+                                                  const CUtensorMap* t_cur, uint64_t* bar, int j0,
+                                                  int b, int kvh, const AttnTcArgs& a) {
+  if (j0 < a.P0) {
     const int row = (b * a.n_kv + kvh) * a.S + (j0 % a.S);
-    tma_load_2d(dst_k, tk, bar, 0, row);
-    tma_load_2d(dst_k + AttnTcCfg::KVHALF, tk, bar, 64, row);
-    tma_load_2d(dst_v, tv, bar, 0, row);
-    tma_load_2d(dst_v + AttnTcCfg::KVHALF, tv, bar, 64, row);
+    tma_load_2d(dst, t_cache, bar, 0, row);
+    tma_load_2d(dst + AttnTcCfg::KVHALF, t_cache, bar, 64, row);
   } else {
     const int tok = b * a.C + (j0 - a.P0);
-    tma_load_3d(dst_k, tk, bar, 0, kvh, tok);
-    tma_load_3d(dst_k + AttnTcCfg::KVHALF, tk, bar, 64, kvh, tok);
-    tma_load_3d(dst_v, tv, bar, 0, kvh, tok);
-    tma_load_3d(dst_v + AttnTcCfg::KVHALF, tv, bar, 64, kvh, tok);
+    tma_load_3d(dst, t_cur, bar, 0, kvh, tok);
+    tma_load_3d(dst + AttnTcCfg::KVHALF, t_cur, bar, 64, kvh, tok);
   }
 }
 
@@ -106,7 +113,9 @@ __device__ __forceinline__ AttnTcItem attn_tc_item(const AttnTcArgs& a, int item
   return it;
 }
 
-__global__ void __launch_bounds__(192, 2)
+constexpr int kAttnTcThreads = 224;
+
+__global__ void __launch_bounds__(kAttnTcThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_kc,
@@ -123,15 +132,16 @@ __global__ void __launch_bounds__(192, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;    // [2]
-  uint64_t* kv_empty = bars + 4;   // [2]
-  uint64_t* s_full = bars + 6;     // [2]
-  uint64_t* s_free = bars + 8;     // [2]
-  uint64_t* p_full = bars + 10;
-  uint64_t* o_done = bars + 11;
-  uint64_t* o_free = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* k_full = bars + 2;     // [2]
+  uint64_t* k_empty = bars + 4;    // [2]
+  uint64_t* v_full = bars + 6;     // [2]
+  uint64_t* v_empty = bars + 8;    // [2]
+  uint64_t* s_full = bars + 10;    // [2]
+  uint64_t* p_full = bars + 12;
+  uint64_t* o_done = bars + 13;
+  uint64_t* o_free = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,10 +152,11 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
     }
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(192, 2)
   // resident); barrier phases run on across items: g counts key tiles, n
   // counts this CTA's items.
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: Q and K
     if (lane == 0) {
       int g = 0, n = 0;
       for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++n) {
@@ -186,19 +197,34 @@ __global__ void __launch_bounds__(192, 2)
         tma_load_3d(smem + Cf::Q_OFF + Cf::QHALF, &tm_q, q_full, 64, it.kvh * a.G, tok);
         for (int j = 0; j < it.ntiles; ++j, ++g) {
           const int st = g & 1;
-          if (g >= 2 && !mbar_wait_bounded(&kv_empty[st], ((g >> 1) - 1) & 1, a.status,
+          if (g >= 2 && !mbar_wait_bounded(&k_empty[st], ((g >> 1) - 1) & 1, a.status,
                                            DEV_ATTN_PRODUCER)) {
             *abort_flag = 1;
             break;
           }
-          const int j0 = (it.t_first + j) * Cf::BK;
-          mbar_arrive_expect_tx(&kv_full[st], 2 * Cf::KVTILE);
-          uint8_t* dk = smem + Cf::K_OFF + st * Cf::KVTILE;
-          uint8_t* dv = smem + Cf::V_OFF + st * Cf::KVTILE;
-          if (j0 < a.P0)
-            attn_tc_load_kv<true>(dk, dv, &tm_kc, &tm_vc, &kv_full[st], j0, it.b, it.kvh, a);
-          else
-            attn_tc_load_kv<false>(dk, dv, &tm_k, &tm_v, &kv_full[st], j0, it.b, it.kvh, a);
+          mbar_arrive_expect_tx(&k_full[st], Cf::KVTILE);
+          attn_tc_load_tile(smem + Cf::K_OFF + st * Cf::KVTILE, &tm_kc, &tm_k, &k_full[st],
+                            (it.t_first + j) * Cf::BK, it.b, it.kvh, a);
+        }
+        if (*abort_flag) break;
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------ TMA producer: V
+    if (lane == 0) {
+      int g = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+        const AttnTcItem it = attn_tc_item(a, item);
+        for (int j = 0; j < it.ntiles; ++j, ++g) {
+          const int st = g & 1;
+          if (g >= 2 && !mbar_wait_bounded(&v_empty[st], ((g >> 1) - 1) & 1, a.status,
+                                           DEV_ATTN_PRODUCER)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], Cf::KVTILE);
+          attn_tc_load_tile(smem + Cf::V_OFF + st * Cf::KVTILE, &tm_vc, &tm_v, &v_full[st],
+                            (it.t_first + j) * Cf::BK, it.b, it.kvh, a);
         }
         if (*abort_flag) break;
       }
@@ -209,12 +235,11 @@ __global__ void __launch_bounds__(192, 2)
       constexpr uint32_t idesc_s = tc_idesc_bf16(128, Cf::BK);
       constexpr uint32_t idesc_o = tc_idesc_bf16(128, 128) | (1u << 16);   // B (V) MN-major
       const uint32_t q_addr = smem_u32(smem + Cf::Q_OFF);
-      const uint32_t p_addr = smem_u32(smem + Cf::P_OFF);
+      // S_g reuses the TMEM buffer of tile g - 2, whose softmax finished (its
+      // p_full was waited for) and whose PV MMA was issued before this one
       auto issue_s = [&](int g) -> bool {
         const int st = g & 1;
-        if (!mbar_wait_bounded(&kv_full[st], (g >> 1) & 1, a.status, DEV_ATTN_MMA)) return false;
-        if (g >= 2 && !mbar_wait_bounded(&s_free[st], ((g >> 1) - 1) & 1, a.status, DEV_ATTN_MMA))
-          return false;
+        if (!mbar_wait_bounded(&k_full[st], (g >> 1) & 1, a.status, DEV_ATTN_MMA)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + Cf::K_OFF + st * Cf::KVTILE);
 #pragma unroll
@@ -225,6 +250,7 @@ __global__ void __launch_bounds__(192, 2)
                       idesc_s, kk);
         }
         tc_commit(&s_full[st]);
+        tc_commit(&k_empty[st]);                  // K stage free once S_g is computed
         return true;
       };
       bool ok = true;
@@ -242,23 +268,25 @@ __global__ void __launch_bounds__(192, 2)
           } else {
             tc_commit(q_empty);                   // Q free once this item's S MMAs are done
           }
+          const int st = gj & 1;
           if (!mbar_wait_bounded(p_full, gj & 1, a.status, DEV_ATTN_MMA) ||
+              !mbar_wait_bounded(&v_full[st], (gj >> 1) & 1, a.status, DEV_ATTN_MMA) ||
               (j == 0 && n >= 1 && !mbar_wait_bounded(o_free, (n - 1) & 1, a.status, DEV_ATTN_MMA))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int st = gj & 1;
           const uint32_t v_addr = smem_u32(smem + Cf::V_OFF + st * Cf::KVTILE);
 #pragma unroll
           for (int kk = 0; kk < Cf::BK / 16; ++kk) {
-            // A = P (128 rows x 16 keys, K-major), B = V (16 keys x 128 dims, MN-major:
-            // the two 64-dim halves KVHALF apart, 8-key groups 1024 B apart)
-            tc_mma_bf16(tmem + 2 * Cf::BK, tc_sdesc_sw128(p_addr + kk * 32),
-                        tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::KVHALF, 1024), idesc_o,
-                        (j | kk) != 0);
+            // A = P (128 rows x 16 keys: 8 TMEM columns of bf16 pairs), B = V
+            // (16 keys x 128 dims, MN-major: the two 64-dim halves KVHALF
+            // apart, 8-key groups 1024 B apart)
+            tc_mma_bf16_ts(tmem + 2 * Cf::BK, tmem + st * Cf::BK + kk * 8,
+                           tc_sdesc_sw128_mn(v_addr + kk * 2048, Cf::KVHALF, 1024), idesc_o,
+                           (j | kk) != 0);
           }
-          tc_commit(&kv_empty[st]);
+          tc_commit(&v_empty[st]);
           tc_commit(o_done);
         }
         g += it.ntiles;
@@ -273,7 +301,6 @@ __global__ void __launch_bounds__(192, 2)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                  // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint8_t* prow = smem + Cf::P_OFF + r * (Cf::BK * 2);
     bool ok = true;
     int g = 0, n = 0;
     // tcgen05.ld / tcgen05.st are warp-collective: every decision that guards
@@ -298,39 +325,72 @@ __global__ void __launch_bounds__(192, 2)
         for (int c = 0; c < Cf::BK / 32; ++c)
           tmem_ld32_nowait(tmem + st * Cf::BK + lane_off + c * 32, sv + c * 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&s_free[st]);
-        // mask (raw scores; scale > 0 keeps the order); whole-tile visibility is
-        // uniform for the item.  Four partial maxima break the dependency chain.
+        // Mask (raw scores; scale > 0 keeps the order).  Whether the tile needs
+        // a mask at all is uniform for the item (all keys visible to all of
+        // its query positions, all 128 rows real), so the common case is a
+        // plain maximum; otherwise key j0 + c is visible to this row iff
+        // lo < c <= hi.
         const int j0 = (it.t_first + j) * Cf::BK;
-        const bool all_vis =
-            j0 + Cf::BK - 1 <= it.p_lo && (a.window <= 0 || it.p_hi - j0 < a.window);
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const bool plain = it.nqv * a.G == 128 && j0 + Cf::BK - 1 <= it.p_lo &&
+                           (a.window <= 0 || it.p_hi - j0 < a.window);
+        float mx;
+        if (plain) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < Cf::BK; ++c) {
-          float v = __uint_as_float(sv[c]);
-          if (!all_vis) {
-            const int rel = qpos - (j0 + c);
-            const bool vis = row_ok && rel >= 0 && (a.window <= 0 || rel < a.window);
-            v = vis ? v : -INFINITY;
-          } else if (!row_ok) {
-            v = -INFINITY;
+          for (int c = 0; c < Cf::BK; c += 8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              m4[u] = max3f(m4[u], __uint_as_float(sv[c + 2 * u]), __uint_as_float(sv[c + 2 * u + 1]));
           }
-          sv[c] = __float_as_uint(v);
-          mx4[c & 3] = fmaxf(mx4[c & 3], v);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        } else {
+          const int hi = row_ok ? qpos - j0 : -1;
+          const int lo = a.window > 0 ? qpos - j0 - a.window : -0x7fffffff;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < Cf::BK; ++c) {
+            const float v = (c <= hi && c > lo) ? __uint_as_float(sv[c]) : -INFINITY;
+            sv[c] = __float_as_uint(v);
+            m4[c & 3] = fmaxf(m4[c & 3], v);
+          }
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
+        mx *= a.scale_log2;
         float scale_o = 1.f;
         bool rescale = false;
         if (mx > m_run + 8.0f) {                     // stale max kept unless it grows by > 2^8
-          scale_o = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+          scale_o = m_run == -INFINITY ? 0.f : ex2_ftz(m_run - mx);
           rescale = j > 0;
           l_run *= scale_o;
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        // the P buffer (and, within the item, O) is free once the previous PV
-        // MMA completed
+        // P as bf16 pairs (key 2c in the low half of column c); the exponent
+        // arguments and the row sum are formed two keys per instruction
+        uint32_t pk[Cf::BK / 2];
+        const unsigned long long sc2 = f32x2_pack(a.scale_log2, a.scale_log2);
+        const unsigned long long nm2 = f32x2_pack(-m_use, -m_use);
+        unsigned long long sum_a = f32x2_pack(0.f, 0.f), sum_b = sum_a;
+#pragma unroll
+        for (int c = 0; c < Cf::BK / 2; ++c) {
+          float x0, x1;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[2 * c]),
+                                            __uint_as_float(sv[2 * c + 1])),
+                                 sc2, nm2),
+                       x0, x1);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          if (c & 1)
+            sum_b = f32x2_add(sum_b, f32x2_pack(p0, p1));
+          else
+            sum_a = f32x2_add(sum_a, f32x2_pack(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        float ls4[4];
+        f32x2_unpack(sum_a, ls4[0], ls4[1]);
+        f32x2_unpack(sum_b, ls4[2], ls4[3]);
+        l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        // O holds PV_{j-1} once o_done completed that phase (waited for every
+        // tile, after the exponentials, so they overlap that MMA)
         w_ok = gj == 0 || mbar_wait_bounded(o_done, (gj - 1) & 1, a.status, DEV_ATTN_SOFTMAX);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
@@ -348,26 +408,9 @@ __global__ void __launch_bounds__(192, 2)
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * scale_o);
             tmem_st32(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
           }
-          tmem_wait_st();
         }
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < Cf::BK / 8; ++q) {        // chunks of 8 keys
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = exp2f(fmaf(__uint_as_float(sv[q * 8 + e]), a.scale_log2, -m_use));
-            ls4[e & 3] += p[e];
-          }
-          uint4 pk;
-          pk.x = pack_bf16x2(p[0], p[1]);
-          pk.y = pack_bf16x2(p[2], p[3]);
-          pk.z = pack_bf16x2(p[4], p[5]);
-          pk.w = pack_bf16x2(p[6], p[7]);
-          *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) = pk;
-        }
-        l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-        fence_proxy_async_smem();
+        tmem_st32(tmem + st * Cf::BK + lane_off, pk);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
       }

@@ -332,7 +332,8 @@ int launch_attn_tc(const AttnArgs& aa, int B, int head_dim, long long cache_rows
   const long long items = (long long)((aa.C + QP - 1) / QP) * aa.n_kv * B;
   const int cap = 2 * num_sms();
   const int grid = items < cap ? (int)items : cap;
-  return launch_k(attn_tc_kernel, dim3(grid), dim3(192), AttnTcCfg::SMEM, st, tq, tk, tv, tkc, tvc,
+  return launch_k(attn_tc_kernel, dim3(grid), dim3(kAttnTcThreads), AttnTcCfg::SMEM, st, tq, tk,
+                  tv, tkc, tvc,
                   a) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
