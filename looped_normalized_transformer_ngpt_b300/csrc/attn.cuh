@@ -534,6 +534,8 @@ struct DecAttnArgs {
   int* counter;                   // [B * n_kv], zero between launches
   __nv_bfloat16* out;             // [B, n_q * dh]
   int B;                          // sequences
+  long long cache_rows;           // rows of the cache block ([batch][n_kv][S]); 0 = unknown
+  int* status;                    // device status word (bounded waits), or null
 };
 
 template <int DH>

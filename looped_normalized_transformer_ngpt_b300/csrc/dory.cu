@@ -28,6 +28,7 @@
 #include "dory.h"
 #include "attn.cuh"
 #include "attn_tc.cuh"
+#include "attn_dec.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
 #include "rowops.cuh"
@@ -443,8 +444,62 @@ int launch_dec_attn(DecAttnArgs a, int B, cudaStream_t st) {
              : DORY_ECUDA;
 }
 
+// TMA-fed decode attention (attn_dec.cuh): head_dim 128, cache given as a
+// block of 64-aligned rings ([batch][n_kv][S], S % 64 == 0).  One CTA per SM
+// strides over (split, kv head, sequence) items; the split ranges are
+// 64-aligned.  Returns DORY_EUNSUPPORTED when the cache does not qualify.
+template <bool RAW>
+int launch_dec_attn_tma(DecAttnArgs a, int B, cudaStream_t st) {
+  if (!a.k_cache || !a.v_cache || a.cache_rows <= 0 || a.S % kDecTile) return DORY_EUNSUPPORTED;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_decode_tma_kernel<RAW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DecTmaCfg::SMEM) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  const int lo = a.window > 0 ? (a.P0 - a.window + 1 > 0 ? a.P0 - a.window + 1 : 0) : 0;
+  const int lo_a = lo / kDecTile * kDecTile;
+  const int n_cache = a.P0 - lo_a;                    // cached keys from the aligned start
+  const int groups = B * a.n_kv;
+  const int cap = num_sms();
+  const int max_sp = (n_cache + kDecMinTiles * kDecTile - 1) / (kDecMinTiles * kDecTile);
+  int best_sp = 1;
+  double best = -1.0;
+  for (int sp = 1; sp <= kDecMaxSplits && sp <= (max_sp > 0 ? max_sp : 1); ++sp) {
+    const long long items = (long long)groups * sp;
+    const long long rounds = (items + cap - 1) / cap;
+    const int keys = ((n_cache + sp - 1) / sp + kDecTile - 1) / kDecTile * kDecTile;
+    const double per = (double)rounds * (double)(keys + kDecTile);
+    if (best < 0 || per < best * 0.98) {
+      best = per;
+      best_sp = sp;
+    }
+  }
+  int chunk = n_cache > 0 ? (n_cache + best_sp - 1) / best_sp : kDecTile;
+  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+  a.chunk = chunk;
+  a.n_splits = n_cache > 0 ? (n_cache + chunk - 1) / chunk : 1;
+  CUtensorMap tkc, tvc;
+  if (!encode_bf16(&tkc, a.k_cache, (uint64_t)a.cache_rows, 128, 128, kDecTile) ||
+      !encode_bf16(&tvc, a.v_cache, (uint64_t)a.cache_rows, 128, 128, kDecTile))
+    return DORY_EUNSUPPORTED;
+  const long long items = (long long)groups * a.n_splits;
+  const int grid = items < cap ? (int)items : cap;
+  a.B = B;
+  return launch_k(attn_decode_tma_kernel<RAW>, dim3(grid), dim3(kDecTmaThreads), DecTmaCfg::SMEM,
+                  st, tkc, tvc, a) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
 template <bool RAW>
 int dec_attn(const DecAttnArgs& a, int B, int head_dim, cudaStream_t st) {
+  if (head_dim == 128) {
+    const int rc = launch_dec_attn_tma<RAW>(a, B, st);
+    if (rc != DORY_EUNSUPPORTED) return rc;
+  }
   if (head_dim == 32) return launch_dec_attn<32, RAW>(a, B, st);
   if (head_dim == 64) return launch_dec_attn<64, RAW>(a, B, st);
   if (head_dim == 128) return launch_dec_attn<128, RAW>(a, B, st);
@@ -682,6 +737,8 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   da.part_ml = wsp<float>(m, m->L.dec_ml);
   da.counter = wsp<int>(m, m->L.dec_cnt);
   da.out = att;
+  da.cache_rows = (long long)m->max_batch * c.n_kv * da.S;
+  da.status = wsp<int>(m, m->L.status);
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
 
@@ -794,6 +851,8 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
   da.part_ml = wsp<float>(m, m->L.dec_ml);
   da.counter = wsp<int>(m, m->L.dec_cnt);
   da.out = att;
+  da.cache_rows = (long long)m->max_batch * c.n_kv * da.S;
+  da.status = wsp<int>(m, m->L.status);
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
 
@@ -906,6 +965,8 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     da.part_ml = wsp<float>(m, m->L.dec_ml);
     da.counter = wsp<int>(m, m->L.dec_cnt);
     da.out = att;
+    da.cache_rows = (long long)m->max_batch * c.n_kv * S;
+    da.status = status;
     DORY_TRY(pe(m, st, dec_attn<false>(da, B, c.head_dim, st)));
   } else {
     AttnArgs aa{};
@@ -1608,6 +1669,7 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
     da.part_ml = reinterpret_cast<float*>(sc + o_bytes);
     da.counter = reinterpret_cast<int*>(sc + o_bytes + ml_bytes);
     da.out = a.out;
+    da.cache_rows = P0 > 0 ? (long long)B * n_kv * a.S : 0;
     if (cudaMemsetAsync(da.counter, 0, (size_t)B * n_kv * 4, st) != cudaSuccess) return DORY_ECUDA;
     return dec_attn<false>(da, B, head_dim, st);
   }

@@ -21,6 +21,8 @@ enum : int {
   DEV_ATTN_SOFTMAX = 0x43,
   DEV_ATTN_DRAIN = 0x44,
   DEV_ATTN_ALIGN = 0x45,
+  DEV_DEC_PRODUCER = 0x51,
+  DEV_DEC_CONSUMER = 0x52,
 };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.

@@ -181,3 +181,43 @@ def test_tc_attention_matches_oracle_and_mma_sync(dev, nq, nkv, W, P0, C):
     finally:
         dev.set_debug_tc_attention(True)
     np.testing.assert_allclose(out, ref, atol=2e-2, rtol=2e-2)
+
+
+# One-token attention on the TMA-fed decode kernel (head_dim 128, cache rings
+# of a multiple of 64 slots): unaligned positions, windows below / above P0,
+# many splits.  (W, P0, S).
+DEC_TMA_CASES = [(0, 1000, 1024), (64, 200, 64), (192, 1000, 192), (4096, 5000, 4096),
+                 (0, 4095, 4096), (64, 63, 64), (0, 20000, 20480), (128, 130, 128)]
+
+
+@pytest.mark.parametrize("nq,nkv", [(8, 2), (16, 4)])
+@pytest.mark.parametrize("W,P0,S", DEC_TMA_CASES)
+def test_decode_tma_attention_mask_is_exact(dev, nq, nkv, W, P0, S):
+    import torch
+    B, dh, C = 2, 128, 1
+    out, *_ = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 0, uniform=True, S=S)
+    lo = 0 if W <= 0 else max(0, P0 - W + 1)
+    n = P0 - lo + 1
+    cnt = np.zeros(dh)
+    for j in range(lo, P0 + 1):
+        cnt[j % dh] += 1
+    want = (cnt.astype(np.float32) * (np.float32(1.0) / np.float32(n))).astype(np.float32)
+    want_bf = torch.tensor(want).to(torch.bfloat16).float().numpy()
+    for b in range(B):
+        for h in range(nq):
+            assert np.array_equal(out[b, 0, h], want_bf), (b, h)
+
+
+@pytest.mark.parametrize("nq,nkv", [(8, 2), (16, 4)])
+@pytest.mark.parametrize("W,P0,S", DEC_TMA_CASES)
+def test_decode_tma_attention_matches_oracle(dev, nq, nkv, W, P0, S):
+    B, dh, C = 2, 128, 1
+    out, q, k_all, v_all, gate = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 3, S=S)
+    G = nq // nkv
+    L = P0 + C
+    for b in range(B):
+        for h in range(nq):
+            o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G],
+                                 np.arange(P0, L), np.arange(L), W, W <= 0, math.sqrt(dh))
+            want = o * gate[b].reshape(C, nq, dh)[:, h]
+            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
