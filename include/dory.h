@@ -258,11 +258,21 @@ DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* 
                                   size_t scratch_bytes, void* stream);
 
 /* Multi-token (prefill) attention runs on the tcgen05 tensor cores when
- * head_dim is 128 and the key tiles of 128 positions line up (P0 a multiple
- * of 128, window and ring size multiples of 128), else on the mma.sync
+ * head_dim is 128 and the key tiles of 64 positions line up (P0 a multiple
+ * of 64, window and ring size multiples of 64), else on the mma.sync
  * kernel.  enable = 0 forces the mma.sync kernel (for comparison): for the
  * handle m, or, with m = NULL, for dory_debug_attention.  Host state only. */
 DORY_API int dory_set_tc_attention(dory_t* m, int enable);
+
+/* Multi-token (prefill) output and down projections: enable = 1 (the
+ * default) fuses the nGPT step h <- N(h + alpha (N(y) - h)) ("Dory1.0-4B:
+ * A Looped Normalized-GPT", Architecture) into the GEMM epilogue when d is a
+ * multiple of 256 with d / 256 <= 8: a thread-block cluster of d / 256 CTAs
+ * holds whole rows and sums both row norms through distributed shared
+ * memory.  enable = 0 runs the GEMM and a separate row kernel.  Both give
+ * the same results up to rounding order.  Host state only; EINVAL for m =
+ * NULL or enable not 0 / 1. */
+DORY_API int dory_set_fused_ngpt(dory_t* m, int enable);
 
 /* Scratch bytes dory_debug_attention needs for one-token (decode) calls. */
 DORY_API size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim);

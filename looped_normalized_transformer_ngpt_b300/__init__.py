@@ -80,6 +80,7 @@ _SIGS = {
     "dory_last_launch_count": (_I, [_P, ctypes.POINTER(_I)]),
     "dory_set_persistent_decode": (_I, [_P, _I]),
     "dory_set_tc_attention": (_I, [_P, _I]),
+    "dory_set_fused_ngpt": (_I, [_P, _I]),
     "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
     "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
     "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
@@ -283,6 +284,12 @@ class Model:
         """Prefill attention on tcgen05 where its tile rules hold (default)
         or always on the mma.sync kernel."""
         _check("dory_set_tc_attention", lib().dory_set_tc_attention(self.handle, 1 if enable else 0))
+
+    def set_fused_ngpt(self, enable: bool):
+        """nGPT step fused into the prefill output / down GEMM epilogues
+        (default, when d is a multiple of 256 with d / 256 <= 8) or a
+        separate row kernel."""
+        _check("dory_set_fused_ngpt", lib().dory_set_fused_ngpt(self.handle, 1 if enable else 0))
 
     def launch_count(self):
         v = ctypes.c_int()

@@ -398,6 +398,74 @@ int launch_gemv(GemvArgs a, cudaStream_t st) {
   return e == cudaSuccess ? DORY_OK : DORY_ECUDA;
 }
 
+// Output / down projection with the nGPT step fused (EPI_NGPT): clusters of
+// N / 256 CTAs, each cluster striding over 128-row blocks; h (fp32) is read
+// and rewritten through maps.out and its bf16 copy through maps.hb.  Returns
+// DORY_EUNSUPPORTED when N is not a multiple of 256 of at most 8 tiles or no
+// cluster of that size fits (the caller then runs the GEMM + row kernel).
+int launch_gemm_ngpt(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args,
+                     const EpiMaps& maps, cudaStream_t st) {
+  using Cf = GemmCfg<kGemmBN, EPI_NGPT>;
+  if (args.N % kGemmBN || args.N / kGemmBN < 1 || args.N / kGemmBN > 8) return DORY_EUNSUPPORTED;
+  const int cn = args.N / kGemmBN;
+  static bool attr = false;
+  static int max_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<kGemmBN, EPI_NGPT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cn;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Cf::SMEM;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (max_clusters[cn] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(cn * (num_sms() / cn));
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kGemmBN, EPI_NGPT>, &cfg) != cudaSuccess)
+      n = 0;
+    cudaGetLastError();
+    max_clusters[cn] = n > 0 ? n : -1;
+  }
+  if (max_clusters[cn] < 1) return DORY_EUNSUPPORTED;
+  args.tiles_m = (args.M + Cf::BM - 1) / Cf::BM;
+  args.tiles_n = cn;
+  args.k_splits = 1;
+  args.staged = 1;
+  if (args.tiles_m == 0) return DORY_OK;
+  const int n_clusters = args.tiles_m < max_clusters[cn] ? args.tiles_m : max_clusters[cn];
+  cfg.gridDim = dim3(n_clusters * cn);
+  // with programmatic serialisation where the runtime accepts it together
+  // with the cluster shape, else plain stream order
+  static int pdl_ok = -1;
+  cfg.numAttrs = pdl_ok != 0 ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kGemmBN, EPI_NGPT>, ta, tb, args, maps);
+  if (e != cudaSuccess && pdl_ok != 0) {
+    cudaGetLastError();
+    pdl_ok = 0;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kGemmBN, EPI_NGPT>, ta, tb, args, maps);
+  } else if (e == cudaSuccess && pdl_ok < 0) {
+    pdl_ok = 1;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    max_clusters[cn] = -1;                          // not launchable here: unfused path
+    return DORY_EUNSUPPORTED;
+  }
+  return DORY_OK;
+}
+
 // One-token attention of the forward pass (fused split merge, gate and KV
 // write), see attn_decode_kernel.  Fills chunk / n_splits.
 template <int DH, bool RAW>
@@ -586,6 +654,7 @@ struct dory_model {
   int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
   bool use_mk = false; // decode steps of <= kGemvMaxM sequences as one persistent kernel
   bool use_tc_attn = true;  // prefill attention on tcgen05 where its tile rules hold
+  bool use_ngpt_fused = true;   // nGPT step in the prefill O / down GEMM epilogues
   bool next_done = false;  // the last step also wrote the greedy tokens
   int launches = 0;
   // optional per-launch event timing
@@ -1016,6 +1085,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   go.out = wsp<float>(m, m->L.y32);
   go.ldo = c.d;
   pb(m, DORY_K_O_GEMM, st);
+  bool fused_o = false, fused_d = false;
   if (few) {
     GemvArgs g{};
     g.M = M;
@@ -1027,10 +1097,22 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.Y = go.out;
     g.ldy = c.d;
     DORY_TRY(pe(m, st, launch_gemv(g, st)));
-  } else {
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st, &em)));
+  } else if (m->use_ngpt_fused) {
+    // nGPT step fused into the GEMM epilogue (cluster over the d columns)
+    EpiMaps eh = em;
+    eh.hb = tm_hb;
+    if (!encode_f32_out(&eh.out, h, M, c.d, c.d)) return DORY_ECUDA;
+    go.h32 = h;
+    go.alpha = w.alpha_attn;
+    const int rc = launch_gemm_ngpt(tm_att, m->tm_o[l], go, eh, st);
+    if (rc != DORY_EUNSUPPORTED) {
+      DORY_TRY(pe(m, st, rc));
+      fused_o = true;
+    }
   }
-  DORY_TRY(ngpt_update(m, M, h, w.alpha_attn, st));
+  if (!few && !fused_o)
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_att, m->tm_o[l], go, st, &em)));
+  if (!fused_o) DORY_TRY(ngpt_update(m, M, h, w.alpha_attn, st));
 
   // SwiGLU MLP + nGPT step
   GemmArgs gu{};
@@ -1078,10 +1160,21 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.Y = gd.out;
     g.ldy = c.d;
     DORY_TRY(pe(m, st, launch_gemv(g, st)));
-  } else {
-    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st, &em)));
+  } else if (m->use_ngpt_fused) {
+    EpiMaps eh = em;
+    eh.hb = tm_hb;
+    if (!encode_f32_out(&eh.out, h, M, c.d, c.d)) return DORY_ECUDA;
+    gd.h32 = h;
+    gd.alpha = w.alpha_mlp;
+    const int rc = launch_gemm_ngpt(tm_m, m->tm_down[l], gd, eh, st);
+    if (rc != DORY_EUNSUPPORTED) {
+      DORY_TRY(pe(m, st, rc));
+      fused_d = true;
+    }
   }
-  return ngpt_update(m, M, h, w.alpha_mlp, st);
+  if (!few && !fused_d)
+    DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_m, m->tm_down[l], gd, st, &em)));
+  return fused_d ? DORY_OK : ngpt_update(m, M, h, w.alpha_mlp, st);
 }
 
 // Loop-boundary kernel on the current hidden buffer; an owed nGPT step is
@@ -1681,6 +1774,12 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
   if (head_dim == 64) return launch_attn<64>(a, B, st);
   if (head_dim == 128) return launch_attn<128>(a, B, st);
   return DORY_EUNSUPPORTED;
+}
+
+int dory_set_fused_ngpt(dory_t* m, int enable) {
+  if (!m || (enable != 0 && enable != 1)) return DORY_EINVAL;
+  m->use_ngpt_fused = enable != 0;
+  return DORY_OK;
 }
 
 int dory_set_tc_attention(dory_t* m, int enable) {

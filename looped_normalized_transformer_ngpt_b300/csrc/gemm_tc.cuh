@@ -29,6 +29,12 @@
 // 128-byte swizzled layout and one thread of each 4-warp half writes it with
 // TMA tensor stores (whole 128-byte rows; a thread-per-row store pattern
 // touches 32 rows per instruction).
+//   EPI_NGPT    output / down projection with the nGPT step fused: the CTAs
+//               of a thread-block cluster hold the d / 256 column tiles of
+//               the same 128 rows; y = the accumulator, and per row
+//               h <- N(h + alpha (N(y) - h)) with both row norms summed over
+//               the cluster through distributed shared memory; h is written
+//               back as fp32 and as the bf16 copy the next GEMM reads.
 //   EPI_PARTS   swapped operands for few activation rows (decode batches):
 //               A = 128 weight rows, B = BN activation rows, and K split into
 //               k_splits ranges so that even a 2048-wide projection spreads
@@ -40,7 +46,7 @@
 
 namespace dory {
 
-enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2, EPI_PARTS = 3 };
+enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2, EPI_PARTS = 3, EPI_NGPT = 4 };
 
 struct GemmArgs {
   int M, N, K;          // N: output columns of the GEMM (for SWIGLU: 2 * ffn)
@@ -71,6 +77,11 @@ struct GemmArgs {
   // EPI_F32 / EPI_SWIGLU with BN = 256: 1 if EpiMaps::out describes the
   // output (then it is written through shared memory), else direct stores
   int staged;
+  // EPI_NGPT: h fp32 [M, N] (read, then rewritten through EpiMaps::out; the
+  // bf16 copy through EpiMaps::hb) and alpha [N]; the cluster size is
+  // tiles_n (N / 256 <= 8)
+  const float* h32;
+  const float* alpha;
 };
 
 template <int BN, int EPI = 0>
@@ -81,6 +92,7 @@ struct GemmCfg {
   // {32 x 128} fp32 (64 KB), SwiGLU 2 halves x {64 x 128} bf16 (32 KB).
   // The first two cost a stage of the operand ring.
   static constexpr bool STAGED = BN == 256 && EPI != 3;
+  static constexpr bool NGPT = EPI == 4;
   static constexpr uint32_t OUT_BYTES = !STAGED ? 0 : (EPI == 2 ? 2 * 16384 : 4 * 16384);
   static constexpr int STAGES = STAGED ? (EPI == 2 ? 4 : 3) : (BN == 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -89,15 +101,21 @@ struct GemmCfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = 256;
   static constexpr uint32_t SQK_BYTES = EPI == 1 ? 512 : 0;   // s_qk of a 128-wide head
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES + 1024;
+  // EPI_NGPT: alpha slice [256], half partial sums for y and u [2][128] each,
+  // the cluster's per-row sums for y and u [8][128] each, two mbarriers
+  static constexpr uint32_t NGPT_BYTES = NGPT ? (256 + 2 * 256 + 2 * 8 * 128) * 4 + 16 : 0;
+  static constexpr size_t SMEM =
+      STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES + NGPT_BYTES + 1024;
 };
 
 // Destination maps of the staged epilogues, all with the 128-byte swizzle:
 //   QKV+gate  q, k, v, g: bf16 [M, heads x 128], {64 columns, 128 rows} boxes;
 //   fp32      out: fp32 [M, N], {32 columns, 128 rows} boxes;
-//   SwiGLU    out: bf16 [M, ffn], {64 columns, 128 rows} boxes.
+//   SwiGLU    out: bf16 [M, ffn], {64 columns, 128 rows} boxes;
+//   nGPT      out: h fp32 [M, d], {32 columns, 128 rows} boxes; hb: h bf16
+//             [M, d], {64 columns, 128 rows} boxes.
 struct EpiMaps {
-  CUtensorMap q, k, v, g, out;
+  CUtensorMap q, k, v, g, out, hb;
 };
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
@@ -470,6 +488,152 @@ __device__ __forceinline__ void epi_swiglu_staged(const GemmArgs& a, const CUten
   }
 }
 
+// Shared state of the fused nGPT epilogue (EPI_NGPT) in this CTA's shared
+// memory; xy / xu [rank][row] receive every cluster CTA's per-row partial
+// sums by st.async, each completing bytes on bar_y / bar_u.
+struct NgptSmem {
+  float* alpha;     // [256]   alpha of this CTA's columns
+  float* part_y;    // [2][128] per-half sums of y^2
+  float* part_u;    // [2][128] per-half sums of u^2
+  float* xy;        // [8][128]
+  float* xu;        // [8][128]
+  uint64_t* bar_y;
+  uint64_t* bar_u;
+};
+
+// Sends this row's CTA-level partial sum to slot [rank][rloc] of every CTA
+// of the cluster (including this one).
+__device__ __forceinline__ void ngpt_broadcast(float* x, uint64_t* bar, int cn, int rank, int rloc,
+                                               float v) {
+  const uint32_t la = smem_u32(x + rank * 128 + rloc), lb = smem_u32(bar);
+  for (int p = 0; p < cn; ++p) st_async_f32(mapa_shared(la, p), v, mapa_shared(lb, p));
+}
+
+// One 128 x 128 half tile of the fused nGPT step; this thread owns row rloc
+// and the half's 128 columns.  Phases of bar_y / bar_u: one per tile (ph).
+// Returns false (uniformly for the 8 epilogue warps) when an exchange wait
+// expired.
+__device__ __forceinline__ bool epi_ngpt(const GemmArgs& a, const EpiMaps& maps,
+                                         const NgptSmem& ns, uint32_t tacc, int rloc, int m0,
+                                         int n0, int c_lo, uint8_t* stage, int half, bool leader,
+                                         uint32_t& nst, uint32_t ph, int cn, int rank) {
+  const int row = m0 + rloc;
+  const bool row_ok = row < a.M;
+  const float* hrow = a.h32 + (long long)(row_ok ? row : 0) * a.N + n0 + c_lo;
+  const bool sender = half == 0;
+  const bool exch_leader = threadIdx.x == 64;          // first epilogue thread
+  // -- 1. sum of y^2 over the row (this half, then the CTA, then the cluster)
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 64) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32_nowait(tacc + c_lo + c, r0);
+    tmem_ld32_nowait(tacc + c_lo + c + 32, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float u0 = __uint_as_float(r0[i]), u1 = __uint_as_float(r1[i]);
+      ss = fmaf(u0, u0, ss);
+      ss = fmaf(u1, u1, ss);
+    }
+  }
+  ns.part_y[half * 128 + rloc] = ss;
+  named_bar(3, 256);
+  if (sender) ngpt_broadcast(ns.xy, ns.bar_y, cn, rank, rloc, ns.part_y[rloc] + ns.part_y[128 + rloc]);
+  // h of this row's first 32 columns, loaded while the sums travel
+  float4 hv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    hv[j] = row_ok ? __ldg(reinterpret_cast<const float4*>(hrow) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  bool ok = mbar_wait_bounded(ns.bar_y, ph, a.status, DEV_GEMM_NGPT);
+  if (!named_bar_and(3, 256, ok)) return false;
+  if (exch_leader) mbar_arrive_expect_tx(ns.bar_y, cn * 128 * 4);   // next tile's phase
+  float sy = 0.f;
+  for (int p = 0; p < cn; ++p) sy += ns.xy[p * 128 + rloc];
+  const float inv_y = 1.0f / sqrtf(fmaxf(sy, 1e-12f));
+  // -- 2. u = h + alpha (y / |y| - h), kept in TMEM; sum of u^2
+  float su = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    uint32_t yv[32];
+    tmem_ld32_nowait(tacc + c_lo + c, yv);
+    tmem_wait_ld();
+    const float4* al = reinterpret_cast<const float4*>(ns.alpha + c_lo + c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a4 = al[j];
+      const float hh[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+      const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float u = fmaf(aa[e], fmaf(__uint_as_float(yv[4 * j + e]), inv_y, -hh[e]), hh[e]);
+        yv[4 * j + e] = __float_as_uint(u);
+        su = fmaf(u, u, su);
+      }
+    }
+    if (c + 32 < 128) {                                  // next 32 columns of h
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        hv[j] = row_ok ? __ldg(reinterpret_cast<const float4*>(hrow + c + 32) + j)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    tmem_st32(tacc + c_lo + c, yv);
+  }
+  tmem_wait_st();
+  ns.part_u[half * 128 + rloc] = su;
+  named_bar(3, 256);
+  if (sender) ngpt_broadcast(ns.xu, ns.bar_u, cn, rank, rloc, ns.part_u[rloc] + ns.part_u[128 + rloc]);
+  ok = mbar_wait_bounded(ns.bar_u, ph, a.status, DEV_GEMM_NGPT);
+  if (!named_bar_and(3, 256, ok)) return false;
+  if (exch_leader) mbar_arrive_expect_tx(ns.bar_u, cn * 128 * 4);
+  float su_all = 0.f;
+  for (int p = 0; p < cn; ++p) su_all += ns.xu[p * 128 + rloc];
+  const float inv_u = 1.0f / sqrtf(fmaxf(su_all, 1e-12f));
+  // -- 3. h = u / |u| as fp32 (two {32 x 128} boxes) and bf16 (one {64 x 128}
+  // box) per 64 columns, through the half's two alternating 16 KB buffers
+  auto publish = [&](const CUtensorMap* map, int x) {
+    fence_proxy_async_smem();
+    if (leader) bulk_wait_read0();
+    named_bar(1 + half, 128);
+    if (leader) {
+      tma_store_2d(map, stage + (nst & 1) * 16384, x, m0);
+      bulk_commit();
+    }
+    ++nst;
+  };
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 64) {
+    uint32_t u[64];
+    tmem_ld32_nowait(tacc + c_lo + c, u);
+    tmem_ld32_nowait(tacc + c_lo + c + 32, u + 32);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * inv_u);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {                        // fp32 boxes
+      uint8_t* buf = stage + (nst & 1) * 16384;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *sw128_chunk(buf, rloc, j) =
+            make_uint4(u[32 * b + 4 * j], u[32 * b + 4 * j + 1], u[32 * b + 4 * j + 2],
+                       u[32 * b + 4 * j + 3]);
+      publish(&maps.out, n0 + c_lo + c + 32 * b);
+    }
+    {                                                    // bf16 box
+      uint8_t* buf = stage + (nst & 1) * 16384;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *sw128_chunk(buf, rloc, j) = make_uint4(
+            pack_bf16x2(__uint_as_float(u[8 * j]), __uint_as_float(u[8 * j + 1])),
+            pack_bf16x2(__uint_as_float(u[8 * j + 2]), __uint_as_float(u[8 * j + 3])),
+            pack_bf16x2(__uint_as_float(u[8 * j + 4]), __uint_as_float(u[8 * j + 5])),
+            pack_bf16x2(__uint_as_float(u[8 * j + 6]), __uint_as_float(u[8 * j + 7])));
+      publish(&maps.hb, n0 + c_lo + c);
+    }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------- the kernel
 constexpr int kGemmThreads = 320;   // producer, MMA, 8 epilogue warps
 
@@ -486,6 +650,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES);
   float* sqk = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES +
                                         C::BAR_BYTES);               // EPI_QKVG: s_qk[128]
+  NgptSmem ns{};
+  if (C::NGPT) {
+    float* f = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES +
+                                        C::BAR_BYTES + C::SQK_BYTES);
+    ns.alpha = f;
+    ns.part_y = f + 256;
+    ns.part_u = f + 512;
+    ns.xy = f + 768;
+    ns.xu = f + 768 + 1024;
+    ns.bar_y = reinterpret_cast<uint64_t*>(f + 768 + 2048);
+    ns.bar_u = ns.bar_y + 1;
+  }
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;   // [2]
   uint64_t* tempty_bar = tfull_bar + 2;       // [2]
@@ -514,14 +690,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty_bar[b], 256);
     }
     mbar_init(drain_bar, 1);
+    if (C::NGPT) {
+      mbar_init(ns.bar_y, 1);
+      mbar_init(ns.bar_u, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
+    if (C::NGPT) {                                  // phase 0: every cluster CTA's row sums
+      mbar_arrive_expect_tx(ns.bar_y, args.tiles_n * 128 * 4);
+      mbar_arrive_expect_tx(ns.bar_u, args.tiles_n * 128 * 4);
+    }
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  // the exchange barriers of every CTA of the cluster exist before any
+  // st.async reaches them
+  if (C::NGPT) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // set-up above overlaps the previous kernel; global memory only from here
@@ -535,7 +722,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
         const int tt = tile % (args.tiles_m * args.tiles_n);
-        const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
+        // EPI_NGPT: the cluster's CTAs take the tiles_n column tiles of a row block
+        const int tm = C::NGPT ? tt / args.tiles_n : tt % args.tiles_m;
+        const int tn = C::NGPT ? tt % args.tiles_n : tt / args.tiles_m;
         const int m0 = tm * BM;
         int kb_lo, kb_hi;
         kb_range(tile, kb_lo, kb_hi);
@@ -620,11 +809,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool leader = (warp & 3) == 2 && lane == 0;   // one thread per half
     constexpr int OUT_HALF = C::OUT_BYTES / 2;
     uint8_t* my_stage = out_stage + chalf * OUT_HALF;
-    const bool staged = C::STAGED && (EPI == EPI_QKVG ? args.head_dim == 128 : args.staged != 0);
+    const bool staged =
+        C::STAGED && (EPI == EPI_QKVG ? args.head_dim == 128 : (C::NGPT || args.staged != 0));
     uint32_t nst = 0;                             // fp32: boxes this half has staged
     if (EPI == EPI_QKVG && C::STAGED) {
       const int e = threadIdx.x - 64;
       if (e < 128) sqk[e] = args.s_qk && e < args.head_dim ? args.s_qk[e] : 1.0f;
+      named_bar(3, 256);
+    }
+    const int ng_rank = C::NGPT ? (int)(blockIdx.x % args.tiles_n) : 0;   // = cluster rank
+    if (C::NGPT) {                                  // alpha of this CTA's 256 columns
+      const int e = threadIdx.x - 64;
+      const int col = ng_rank * BN + e;
+      ns.alpha[e] = col < args.N ? args.alpha[col] : 0.f;
       named_bar(3, 256);
     }
     int it = 0;
@@ -635,7 +832,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       const int tt = tile % (args.tiles_m * args.tiles_n);
-      const int tm = tt % args.tiles_m, tn = tt / args.tiles_m;
+      const int tm = C::NGPT ? tt / args.tiles_n : tt % args.tiles_m;
+      const int tn = C::NGPT ? tt % args.tiles_n : tt / args.tiles_m;
       const int row = tm * BM + quarter * 32 + lane;
       constexpr int CW = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 2;   // columns per half
       const int c_lo = chalf * CW, c_hi = c_lo + CW;
@@ -645,7 +843,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         qkvg_rope_load(args, row, qkvg_rope_head(args, tn * BN + c_lo) && row < args.M, 0, cs);
       bool ready = !*abort_flag &&
                    mbar_wait_bounded(&tfull_bar[acc], aph, args.status, DEV_GEMM_EPI);
-      ready = C::STAGED ? named_bar_and(1 + chalf, 128, ready) : __all_sync(0xffffffffu, ready);
+      // (EPI_NGPT: uniform over all 8 epilogue warps, which meet at one barrier)
+      ready = C::NGPT      ? named_bar_and(3, 256, ready)
+              : C::STAGED ? named_bar_and(1 + chalf, 128, ready)
+                          : __all_sync(0xffffffffu, ready);
       if (!ready) {
         *abort_flag = 1;
         break;
@@ -676,6 +877,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (EPI == EPI_PARTS)
         epi_parts<BN>(args, tacc, row, tn * BN, tile / (args.tiles_m * args.tiles_n), c_lo, c_hi);
+      if (C::NGPT) {
+        if (!epi_ngpt(args, maps, ns, tacc, rloc, m0, tn * BN, c_lo, my_stage, chalf, leader, nst,
+                      (uint32_t)(it & 1), args.tiles_n, ng_rank)) {
+          *abort_flag = 1;
+          break;
+        }
+      }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -689,6 +897,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // shared memory is released
     for (int i = 0; i < 64; ++i) __nanosleep(1000);
   }
+  // no CTA of the cluster leaves while another may still write its shared
+  // memory (every exchange wait above is bounded, so all threads get here)
+  if (C::NGPT) cluster_sync();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -16,6 +16,7 @@ enum : int {
   DEV_GEMM_MMA_TMEM = 0x13,
   DEV_GEMM_EPI = 0x14,
   DEV_GEMM_DRAIN = 0x15,
+  DEV_GEMM_NGPT = 0x16,
   DEV_ATTN_PRODUCER = 0x41,
   DEV_ATTN_MMA = 0x42,
   DEV_ATTN_SOFTMAX = 0x43,
@@ -146,6 +147,32 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// all threads of all CTAs of the cluster (release / acquire)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 4-byte store into another CTA's shared memory that completes 4 bytes of
+// transaction on that CTA's mbarrier (both addresses from mapa_shared)
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   remote_addr),
+               "r"(__float_as_uint(v)), "r"(remote_bar)
+               : "memory");
 }
 
 // 2^x with the special-function unit (approximate, subnormal results flushed
