@@ -33,6 +33,12 @@ if ROOT not in sys.path:
 
 METRIC = "looped fwd tokens/s at k=1/2/4 (prefill, decode); % of BF16 TC / HBM roofline"
 BATCH, SEQ, DECODE = 4, 2048, 8
+
+
+def ctx64(n: int) -> int:
+    """Context capacity rounded up to a multiple of 64 positions, so every cache
+    ring qualifies for the TMA-fed decode attention."""
+    return (n + 63) // 64 * 64
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -217,7 +223,7 @@ def run_gpu(args):
     sh = synth.SMALL
     K, D = args.k, args.decode
     w = synth.make_weights(sh)
-    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=SEQ + D, max_chunk=SEQ, k_max=max(K, 4),
+    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=ctx64(SEQ + D), max_chunk=SEQ, k_max=max(K, 4),
                    cache_mode=dory.LAST_LOOP, device=dev)
     del w
     prompt_np = synth.tokens(sh, BATCH, SEQ, seed=1000 + rank)
@@ -510,7 +516,7 @@ def run_workload_4b(args):
             # 262144-token context prefilled in 16384-token chunks at k = 4
             # (last-loop cache), then decode steps at that context
             T, CH, K, D = args.ctx or 262144, 16384, 4, 8
-            m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T + D,
+            m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=ctx64(T + D),
                            max_chunk=CH, k_max=K)
             tok = torch.tensor(synth.tokens(sh, 1, T, seed=5), device="cuda")
             lg = torch.empty((1, sh.vocab), device="cuda")
@@ -558,7 +564,7 @@ def run_workload_4b(args):
             m = None
             for mode in (dory.PER_LOOP, dory.LAST_LOOP):
                 if m is None:
-                    m = dory.Model(sh, weights, max_batch=1, max_ctx=T + D, max_chunk=CH,
+                    m = dory.Model(sh, weights, max_batch=1, max_ctx=ctx64(T + D), max_chunk=CH,
                                    k_max=K, cache_mode=mode)
                 else:
                     m.bind(1, T + D, CH, K, mode)
@@ -770,7 +776,7 @@ def run_profile_target(args):
     _build.build()
     sh = synth.SMALL
     w = synth.make_weights(sh)
-    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=SEQ + 1, max_chunk=SEQ, k_max=max(args.k, 4),
+    m = dory.Model(sh, w, max_batch=BATCH, max_ctx=ctx64(SEQ + 1), max_chunk=SEQ, k_max=max(args.k, 4),
                    cache_mode=dory.LAST_LOOP)
     prompt = torch.tensor(synth.tokens(sh, BATCH, SEQ, seed=1000), device="cuda")
     first = torch.tensor(synth.tokens(sh, BATCH, 1, seed=2000)[:, 0], device="cuda")

@@ -142,6 +142,17 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
   }
 
   // ------------------------------------------------ consumers (warps 0-3)
+  // RoPE (cos, sin) of position P0 and s_qk for this lane's columns: weights
+  // and a table written before the previous kernel, so read before its wait
+  float2 rcs[HALF / 32];
+  float rsq[HALF / 32][2];
+#pragma unroll
+  for (int e = 0; e < HALF / 32; ++e) {
+    const int i = lane + 32 * e;
+    rcs[e] = RAW && a.rope ? a.rope[i] : make_float2(1.f, 0.f);
+    rsq[e][0] = RAW ? a.s_qk[i] : 1.f;
+    rsq[e][1] = RAW ? a.s_qk[i + HALF] : 1.f;
+  }
   auto csync = [] { named_bar(1, 128); };
   bool first = true;
   int g = 0;
@@ -157,63 +168,74 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
       csync();                                           // shared state of the last item free
     }
 
-    // ---- prologue: q^ (rows of sQ), current k^ and v, gate
+    // ---- prologue: q^ (rows of sQ), current k^ and v, gate.  Every global
+    // load of the item is issued before any is used (one memory round trip);
+    // warp w forms heads hh = w and w + 4 (hh < G: query head kvh G + hh,
+    // hh == G: key, hh == G + 1: value), lane l columns l, l + 32 of each half.
     for (int idx = tid; idx < 16 * CH; idx += 128) {     // zero rows >= G
       const int r = idx / CH, c = idx % CH;
       if (r >= G) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sQ) + swz_off<DH>(r, c)) =
           make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int idx = tid; idx < G * DH; idx += 128) {
-      const int r = idx / DH, dd = idx % DH;
-      float gt;
-      if (RAW) {
-        float gr = 0.f;
-        const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
-                          (kvh * G + r) * DH + dd;
-        for (int p = 0; p < a.n_parts; ++p) gr += yg[p * a.part_stride];
-        gt = 1.0f / (1.0f + __expf(-gr));
-      } else {
-        gt = __bfloat162float(a.gate[((long long)b * a.n_q + kvh * G + r) * DH + dd]);
+    constexpr int GPT = kDecMaxG * DH / 128;             // gate values per thread (max)
+    float gv[GPT];
+#pragma unroll
+    for (int e = 0; e < GPT; ++e) {
+      const int idx = tid + 128 * e;
+      gv[e] = 0.f;
+      if (idx < G * DH) {
+        const int r = idx / DH, dd = idx % DH;
+        if (RAW) {
+          const float* yg = a.y + (long long)b * a.ldy + (long long)(a.n_q + 2 * a.n_kv) * DH +
+                            (kvh * G + r) * DH + dd;
+          for (int p = 0; p < a.n_parts; ++p) gv[e] += yg[p * a.part_stride];
+        } else {
+          gv[e] = __bfloat162float(a.gate[((long long)b * a.n_q + kvh * G + r) * DH + dd]);
+        }
       }
-      sGate[idx] = gt;
     }
-    for (int hh = warp; hh < G + 2; hh += 4) {
-      // hh < G: query head kvh * G + hh; hh == G: key; hh == G + 1: value
-      if (RAW) {
-        const int col0 = hh < G ? (kvh * G + hh) * DH
-                                : (hh == G ? (a.n_q + kvh) * DH : (a.n_q + a.n_kv + kvh) * DH);
-        const float* yr = a.y + (long long)b * a.ldy + col0;
-        float x1[HALF / 32], x2[HALF / 32];
+    if (RAW) {
+      float x1[2][HALF / 32], x2[2][HALF / 32];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int hh = warp + 4 * s2;
+#pragma unroll
+        for (int e = 0; e < HALF / 32; ++e) x1[s2][e] = x2[s2][e] = 0.f;
+        if (hh < G + 2) {
+          const int col0 = hh < G ? (kvh * G + hh) * DH
+                                  : (hh == G ? (a.n_q + kvh) * DH : (a.n_q + a.n_kv + kvh) * DH);
+          const float* yr = a.y + (long long)b * a.ldy + col0;
+          for (int p = 0; p < a.n_parts; ++p) {
+#pragma unroll
+            for (int e = 0; e < HALF / 32; ++e) {
+              const int i = lane + 32 * e;
+              x1[s2][e] += yr[p * a.part_stride + i];
+              x2[s2][e] += yr[p * a.part_stride + i + HALF];
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int hh = warp + 4 * s2;
+        if (hh >= G + 2) continue;                         // uniform for the warp
         float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < HALF / 32; ++e) {
-          const int i = lane + 32 * e;
-          x1[e] = x2[e] = 0.f;
-          for (int p = 0; p < a.n_parts; ++p) {
-            x1[e] += yr[p * a.part_stride + i];
-            x2[e] += yr[p * a.part_stride + i + HALF];
-          }
-          ss += x1[e] * x1[e] + x2[e] * x2[e];
-        }
+        for (int e = 0; e < HALF / 32; ++e) ss += x1[s2][e] * x1[s2][e] + x2[s2][e] * x2[s2][e];
         if (hh <= G) {
           const float inv = 1.0f / sqrtf(fmaxf(warp_sum(ss), 1e-12f));
 #pragma unroll
           for (int e = 0; e < HALF / 32; ++e) {
-            const int i = lane + 32 * e;
-            float c1 = x1[e], c2 = x2[e];
-            if (a.rope) {
-              const float2 cs = a.rope[i];
-              c1 = x1[e] * cs.x - x2[e] * cs.y;
-              c2 = x2[e] * cs.x + x1[e] * cs.y;
-            }
-            x1[e] = c1 * inv * a.s_qk[i];
-            x2[e] = c2 * inv * a.s_qk[i + HALF];
+            const float c1 = x1[s2][e] * rcs[e].x - x2[s2][e] * rcs[e].y;
+            const float c2 = x2[s2][e] * rcs[e].x + x1[s2][e] * rcs[e].y;
+            x1[s2][e] = c1 * inv * rsq[e][0];
+            x2[s2][e] = c2 * inv * rsq[e][1];
           }
         }
 #pragma unroll
         for (int e = 0; e < HALF / 32; ++e) {
           const int i = lane + 32 * e;
-          const __nv_bfloat16 b1 = __float2bfloat16_rn(x1[e]), b2 = __float2bfloat16_rn(x2[e]);
+          const __nv_bfloat16 b1 = __float2bfloat16_rn(x1[s2][e]), b2 = __float2bfloat16_rn(x2[s2][e]);
           if (hh < G) {
             sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] = b1;
             sQ[(swz_off<DH>(hh, (i + HALF) / 8) >> 1) + (i & 7)] = b2;
@@ -229,7 +251,9 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
             }
           }
         }
-      } else {
+      }
+    } else {
+      for (int hh = warp; hh < G + 2; hh += 4) {
         for (int i = lane; i < DH; i += 32) {
           if (hh < G) {
             sQ[(swz_off<DH>(hh, i / 8) >> 1) + (i & 7)] =
@@ -245,6 +269,11 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
           }
         }
       }
+    }
+#pragma unroll
+    for (int e = 0; e < GPT; ++e) {
+      const int idx = tid + 128 * e;
+      if (idx < G * DH) sGate[idx] = RAW ? 1.0f / (1.0f + __expf(-gv[e])) : gv[e];
     }
     csync();
 
@@ -432,13 +461,15 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
       const float* wr = sW + r * (NS + 1);
       float acc = wr[NS] * sVc[dd];
       const float* po = a.part_o + bh * NS * DH + dd;
-      int sp = 0;
-      for (; sp + 4 <= NS; sp += 4) {
-        const float o0 = __ldcg(po + (sp + 0) * DH), o1 = __ldcg(po + (sp + 1) * DH);
-        const float o2 = __ldcg(po + (sp + 2) * DH), o3 = __ldcg(po + (sp + 3) * DH);
-        acc += wr[sp] * o0 + wr[sp + 1] * o1 + wr[sp + 2] * o2 + wr[sp + 3] * o3;
+      // 16 partials in flight per round
+      for (int sp0 = 0; sp0 < NS; sp0 += 16) {
+        float ov[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) ov[u] = sp0 + u < NS ? __ldcg(po + (sp0 + u) * DH) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (sp0 + u < NS) acc += wr[sp0 + u] * ov[u];
       }
-      for (; sp < NS; ++sp) acc += wr[sp] * __ldcg(po + sp * DH);
       a.out[bh * DH + dd] = __float2bfloat16_rn(acc * sM[r] * sGate[idx]);
     }
     if (tid == 0) a.counter[b * a.n_kv + kvh] = 0;
