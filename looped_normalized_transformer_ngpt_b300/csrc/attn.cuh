@@ -490,7 +490,7 @@ namespace dory {
 //
 // Grid (split, kv head, sequence), 128 threads.  The CTA's 16 mma rows are the
 // G query heads of its kv head (rows >= G are zero).  Cached keys of the
-// split stream through a 3-stage cp.async ring of 64-key K/V tiles (XOR
+// split stream through a 2-stage cp.async ring of 64-key K/V tiles (XOR
 // swizzled 16-byte chunks, ldmatrix-friendly); warp w takes keys 16w..16w+15
 // of every tile with mma.sync m16n8k16 (bf16 in, fp32 accumulate) and keeps
 // its own online-softmax state; the 4 warps merge through shared memory and

@@ -141,3 +141,24 @@ def test_bench_visible_key_count_matches_brute_force():
                 brute = sum(t + 1 if sh.is_full(l) else min(t + 1, sh.window)
                             for t in range(P0, P0 + C))
                 assert bench.visible_keys(sh, l, P0, C) == brute
+
+
+def test_path_switches_validate_arguments(L):
+    """The comparison switches are host state: argument errors come back
+    without any CUDA call, on a created (unbound) handle."""
+    shape = synth.TINY
+    w, keep = _fake_weights(shape)
+    cfg = dory.config_from_shape(shape)
+    h = ctypes.c_void_p()
+    assert L.dory_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == dory.DORY_OK
+    try:
+        assert L.dory_set_fused_ngpt(None, 1) == dory.DORY_EINVAL
+        assert L.dory_set_fused_ngpt(h, 2) == dory.DORY_EINVAL
+        assert L.dory_set_fused_ngpt(h, 0) == dory.DORY_OK
+        assert L.dory_set_fused_ngpt(h, 1) == dory.DORY_OK
+        assert L.dory_set_tc_attention(h, 3) == dory.DORY_EINVAL
+        assert L.dory_set_tc_attention(h, 0) == dory.DORY_OK
+        assert L.dory_set_persistent_decode(h, -1) == dory.DORY_EINVAL
+        assert L.dory_set_persistent_decode(h, 0) == dory.DORY_OK
+    finally:
+        assert L.dory_destroy(h) == dory.DORY_OK
