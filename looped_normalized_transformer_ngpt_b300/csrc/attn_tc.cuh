@@ -415,7 +415,16 @@ __global__ void __launch_bounds__(kAttnTcThreads, 2)
         mbar_arrive(p_full);
       }
       if (!ok) break;
-      // final: O / l * gate, then O is free for the next item
+      // final: O / l * gate, then O is free for the next item.  The gate row
+      // of this thread (256 bytes) is loaded before the wait for the last PV
+      // MMA, so its latency overlaps that MMA instead of the output loop.
+      const long long row = (long long)it.b * a.C + it.q0 + i;
+      const long long base = row * a.n_q * 128 + (long long)(it.kvh * a.G + hg) * 128;
+      uint4 gr[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        gr[e] = row_ok ? __ldg(reinterpret_cast<const uint4*>(a.gate + base) + e)
+                       : make_uint4(0u, 0u, 0u, 0u);
       bool fin = !*abort_flag && mbar_wait_bounded(o_done, (g + it.ntiles - 1) & 1, a.status,
                                                    DEV_ATTN_SOFTMAX);
       if (!__all_sync(0xffffffffu, fin)) {
@@ -424,27 +433,25 @@ __global__ void __launch_bounds__(kAttnTcThreads, 2)
       }
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      const long long row = (long long)it.b * a.C + it.q0 + i;
-      const long long base = row * a.n_q * 128 + (long long)(it.kvh * a.G + hg) * 128;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
         tmem_ld32_nowait(tmem + 2 * Cf::BK + lane_off + c * 32, ov);
         tmem_wait_ld();
-        if (!row_ok) continue;
+        if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          const uint4 gr = *reinterpret_cast<const uint4*>(a.gate + base + c * 32 + e);
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
-          uint4 o;
-          uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr[4 * c + e]);
+            uint4 o;
+            uint32_t* op = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 gf = __bfloat1622float2(g2[u]);
-            op[u] = pack_bf16x2(__uint_as_float(ov[e + 2 * u]) * inv * gf.x,
-                                __uint_as_float(ov[e + 2 * u + 1]) * inv * gf.y);
+            for (int u = 0; u < 4; ++u) {
+              const float2 gf = __bfloat1622float2(g2[u]);
+              op[u] = pack_bf16x2(__uint_as_float(ov[8 * e + 2 * u]) * inv * gf.x,
+                                  __uint_as_float(ov[8 * e + 2 * u + 1]) * inv * gf.y);
+            }
+            *reinterpret_cast<uint4*>(a.out + base + c * 32 + 8 * e) = o;
           }
-          *reinterpret_cast<uint4*>(a.out + base + c * 32 + e) = o;
         }
       }
       tc_fence_before();
