@@ -44,7 +44,9 @@ def weights():
 
 @pytest.fixture(scope="module")
 def model_last(dev, weights):
-    return dev.Model(SHAPE, weights, max_batch=64, max_ctx=400, max_chunk=400, k_max=4,
+    # a capacity of a multiple of 64 positions: the decode steps run the TMA-fed
+    # decode attention (its inputs here are split-K partial sums)
+    return dev.Model(SHAPE, weights, max_batch=64, max_ctx=448, max_chunk=400, k_max=4,
                      cache_mode=dev.LAST_LOOP)
 
 
@@ -91,8 +93,8 @@ def test_4b_width_chunked_prefill_then_decode(dev, weights, mode):
     o = oracle.Oracle(SHAPE, weights, dtype=np.float32)
     for c0 in range(0, T, chunk):
         ref = o.prefill(prompt[:, c0:c0 + chunk], k, mode)
-    m = dev.Model(SHAPE, weights, max_batch=B, max_ctx=T + D, max_chunk=chunk, k_max=k,
-                  cache_mode=mode)
+    m = dev.Model(SHAPE, weights, max_batch=B, max_ctx=(T + D + 63) // 64 * 64, max_chunk=chunk,
+                  k_max=k, cache_mode=mode)
     lg = m.prefill(_tok(prompt), k, mode)
     check_logits(lg.cpu().numpy(), ref["logits"][:, -1])
     for s in range(D):
