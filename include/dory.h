@@ -153,7 +153,11 @@ DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k,
  * NULL (requires logits).
  * Decode steps of up to 16 sequences run five kernels per layer application
  * (see dory_set_persistent_decode for the single-kernel alternative); larger
- * batches run the tensor-core projections with K split over the SMs. */
+ * batches run the tensor-core projections with K split over the SMs.  With
+ * head_dim 128 and ring sizes that are multiples of 64 (max_ctx and window,
+ * as given to dory_bind / dory_create) the attention streams the cached K/V
+ * with TMA through a 4-stage ring; otherwise a cp.async kernel does (same
+ * results up to rounding order, slower on long contexts). */
 DORY_API int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                      float* logits, int32_t* next, void* stream);
 
