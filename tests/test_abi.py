@@ -162,3 +162,29 @@ def test_path_switches_validate_arguments(L):
         assert L.dory_set_persistent_decode(h, 0) == dory.DORY_OK
     finally:
         assert L.dory_destroy(h) == dory.DORY_OK
+
+
+def test_bench_work_models_match_the_closed_forms():
+    """bench.py's algorithmic work per step (the numerators of every
+    roofline fraction) against the closed-form figures of the workloads:
+    prefill FLOP per token (layer applications 32 + 40k at 2 x parameters,
+    attention over visible pairs, the LM head on one row per sequence) and
+    decode bytes per step (every weight once, the LM head, the visible
+    cached K/V)."""
+    import bench
+    import synth
+
+    def close(a, b, rel=5e-3):
+        return abs(a - b) <= rel * b
+
+    for sh, B, C, want in ((synth.DORY4B, 1, 8192, (9.51, 14.80, 25.37)),
+                           (synth.SMALL, 4, 2048, (0.486, 0.756, 1.295))):
+        for k, w in zip((1, 2, 4), want):
+            f = bench.step_flops(sh, B, C, k)
+            assert close(sum(f.values()) / (B * C) / 1e9, w), (sh.name, k)
+    for k, w in zip((1, 2, 3, 4), (114.4, 177.6, 240.9, 304.1)):
+        d = bench.decode_step_bytes(synth.DORY4B, 64, k, 32768)
+        assert close((d["weights"] + d["kv"]) / 1e9, w), k
+    for k, w in ((1, 18.2), (4, 47.6)):
+        d = bench.decode_step_bytes(synth.DORY4B, 1, k, 262144)
+        assert close((d["weights"] + d["kv"]) / 1e9, w), k
