@@ -318,8 +318,114 @@ def test_per_loop_rejects_k_change():
 
 
 def test_greedy_ties_lowest_index():
-    z = np.array([[0.1, 0.7, 0.7, 0.2]])
-    assert int(np.argmax(z, axis=-1)[0]) == 1
+    """Greedy decoding picks the lowest index among equal maxima.  Two rows of
+    E_out are set to the decode step's own final hidden state (a unit vector,
+    and the LM head does not feed back into it), so those two logits are
+    exactly 1, the maximum over unit rows; the next token must be the lower
+    of the two indices whichever order they are planted in."""
+    sh = synth.TINY
+    w = synth.make_weights(sh)
+    prompt = synth.tokens(sh, 2, 10)
+    tok = synth.tokens(sh, 2, 1, seed=1)[:, 0]
+    o = oracle.Oracle(sh, w)
+    o.prefill(prompt, 2, LAST_LOOP)
+    h = o.decode(tok, 2, LAST_LOOP)["hidden"]
+    for lo, hi in ((37, 411), (5, 6)):
+        for b in range(2):
+            w2 = dict(w)
+            e = w["embed_out"].astype(np.float64).copy()
+            e[lo] = e[hi] = h[b]
+            w2["embed_out"] = e
+            o2 = oracle.Oracle(sh, w2)
+            o2.prefill(prompt, 2, LAST_LOOP)
+            r = o2.decode(tok, 2, LAST_LOOP)
+            assert r["logits"][b, lo] == r["logits"][b, hi]
+            assert r["logits"][b, lo] == np.max(r["logits"][b])
+            assert int(r["next"][b]) == lo
+
+
+def _final_loop_everywhere(o, sh, k):
+    """Cache surgery on a per-loop oracle: every loop's slice of every
+    recurrent layer is replaced by the final loop's keys and values."""
+    for l in range(sh.n_in, sh.n_in + sh.n_rec):
+        fin = o.cache[(l, k)]
+        for i in range(1, k):
+            o.cache[(l, i)] = type(fin)(fin.k.copy(), fin.v.copy())
+
+
+@pytest.mark.parametrize("k", [2, 4])
+def test_last_loop_decode_equals_recompute_with_final_loop_keys(k):
+    """Last-Loop KV Caching: past positions are seen through the final
+    loop's keys and values whichever loop the query is in, while the current
+    token uses its own current-loop values.  Built by hand from the per-loop
+    cache (pinned against full recompute above): after the prompt and after
+    each decode step, every loop's slice is overwritten with loop k's, and
+    the per-loop step that follows must then reproduce the last-loop step
+    exactly.  A last-loop rule that kept any other loop's entries fails."""
+    sh = synth.TINY_LOOPFULL
+    w = synth.make_weights(sh)
+    prompt = synth.tokens(sh, 2, 40)
+    dec = synth.tokens(sh, 2, 4, seed=1)
+    a = oracle.Oracle(sh, w)
+    b = oracle.Oracle(sh, w)
+    a.prefill(prompt, k, LAST_LOOP)
+    b.prefill(prompt, k, PER_LOOP)
+    for s in range(dec.shape[1]):
+        _final_loop_everywhere(b, sh, k)
+        ra = a.decode(dec[:, s], k, LAST_LOOP)
+        rb = b.decode(dec[:, s], k, PER_LOOP)
+        assert np.array_equal(ra["logits"], rb["logits"])
+        assert np.array_equal(ra["hidden"], rb["hidden"])
+
+
+def test_last_loop_chunked_prefill_equals_final_loop_surgery():
+    """The same rule across prefill chunks: a later chunk sees the earlier
+    chunks through their final-loop entries."""
+    sh = synth.TINY_LOOPFULL
+    k = 3
+    w = synth.make_weights(sh)
+    prompt = synth.tokens(sh, 2, 45)
+    a = oracle.Oracle(sh, w)
+    b = oracle.Oracle(sh, w)
+    for c0, c1 in ((0, 9), (9, 30), (30, 45)):
+        if c0:
+            _final_loop_everywhere(b, sh, k)
+        ra = a.prefill(prompt[:, c0:c1], k, LAST_LOOP, all_logits=True)
+        rb = b.prefill(prompt[:, c0:c1], k, PER_LOOP, all_logits=True)
+        assert np.array_equal(ra["logits"], rb["logits"])
+
+
+def test_rope_base_follows_layer_type():
+    """Long-Context Extension: sliding-window layers rotate with base 1e4,
+    full-attention layers with base 1e7.  One head of width 4 (pairs (0, 2)
+    at frequency 1 and (1, 3) at base^-1/2), two tokens whose query/key
+    parts are both e1 at positions 0 and p, so their rotated dot product is
+    cos(p * base^-1/2) while each token's own score is 1.  Their values are
+    orthogonal and W_o, the gate and alpha = 1 pass the attention output
+    through, so the second token's new state is N(w0 e0 + w1 e1) with
+    w0 / w1 = exp(scale * (cos(p base^-1/2) - 1)), scale = sqrt(4) = 2."""
+    sh = synth.TINY.replace(d=6, n_q=1, n_kv=1, head_dim=4, n_in=2, n_rec=0, n_out=0,
+                            full_every=2, full_offset=1, window=10**6)
+    assert not sh.is_full(0) and sh.is_full(1)
+    o = oracle.Oracle.__new__(oracle.Oracle)
+    o.shape, o.dtype, o.trace = sh, np.float64, None
+    qk = np.zeros((4, 6)); qk[:4, :4] = np.eye(4)
+    wv = np.zeros((4, 6)); wv[0, 4] = 1.0; wv[1, 5] = 1.0
+    wo = np.zeros((6, 4)); wo[:4, :4] = np.eye(4)
+    lw = {"w_q": qk, "w_k": qk, "w_v": wv, "w_g": np.zeros((4, 6)), "w_o": wo,
+          "alpha_attn": np.ones(6), "s_qk": np.ones(4)}
+    o.w = {"layers": [lw, lw]}
+    h = np.zeros((1, 2, 6))
+    h[0, 0, [1, 4]] = 1 / math.sqrt(2)
+    h[0, 1, [1, 5]] = 1 / math.sqrt(2)
+    for p in (100, 3000):
+        for layer, base in ((0, 1.0e4), (1, 1.0e7)):
+            o.reset()
+            out = o.attn_sublayer(layer, h, np.array([0, p]), None, LAST_LOOP, 1)
+            ratio = out[0, 1, 0] / out[0, 1, 1]
+            want = math.exp(2.0 * (math.cos(p * base ** -0.5) - 1.0))
+            np.testing.assert_allclose(ratio, want, rtol=1e-12)
+            np.testing.assert_allclose(np.linalg.norm(out[0, 1]), 1.0, atol=1e-15)
 
 
 # ------------------------------------------------------------- KV footprint
@@ -418,3 +524,18 @@ def test_qk_scale_parameter_scales_logits_quadratically():
     x = oracle.Oracle(sh, w).prefill(tok, 1, LAST_LOOP)["logits"]
     y = oracle.Oracle(sh, w2).prefill(tok, 1, LAST_LOOP)["logits"]
     assert np.max(np.abs(x - y)) > 1e-6          # s_qk reaches the scores
+
+
+def test_logit_scale_is_per_vocabulary_entry():
+    """logits = s_z * (E_out h): a per-entry scale multiplies each vocabulary
+    column of the logits and leaves the hidden state alone."""
+    sh = synth.TINY
+    w = synth.make_weights(sh)
+    tok = synth.tokens(sh, 2, 12)
+    a = oracle.Oracle(sh, w).prefill(tok, 2, LAST_LOOP)
+    s = np.linspace(0.5, 3.0, sh.vocab)
+    b = oracle.Oracle(sh, dict(w, s_z=s)).prefill(tok, 2, LAST_LOOP)
+    assert np.array_equal(a["hidden"], b["hidden"])
+    np.testing.assert_allclose(b["logits"], a["logits"] * s, rtol=1e-14, atol=1e-16)
+    np.testing.assert_allclose(a["logits"], a["hidden"] @ w["embed_out"].astype(np.float64).T,
+                               rtol=1e-13, atol=1e-15)
