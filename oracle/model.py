@@ -135,8 +135,9 @@ def slot_positions(written_positions, n_slots: int) -> np.ndarray:
 
 @dataclass
 class _Cache:
-    k: np.ndarray       # [B, n_kv, L, dh]  L = number of cached positions
+    k: np.ndarray       # [B, n_kv, L, dh]: keys of positions first .. first + L - 1
     v: np.ndarray
+    first: int = 0      # sliding-window layers drop keys no later query can see
 
 
 @dataclass
@@ -197,12 +198,13 @@ class Oracle:
         sl = self._slice(l, loop, mode)
         past = self.cache.get((l, sl))
         P0 = pos[0]
-        if past is not None and P0 > 0:
-            k_all = np.concatenate([past.k[:, :, :P0], kh], axis=2)
-            v_all = np.concatenate([past.v[:, :, :P0], v], axis=2)
+        if past is not None and P0 > past.first:
+            n_old = P0 - past.first
+            k_all = np.concatenate([past.k[:, :, :n_old], kh], axis=2)
+            v_all = np.concatenate([past.v[:, :, :n_old], v], axis=2)
+            k_pos = np.arange(past.first, P0 + C)
         else:
-            k_all, v_all = kh, v
-        k_pos = np.arange(k_all.shape[2])
+            k_all, v_all, k_pos = kh, v, pos
         o = np.empty((B, nq, C, dh), self.dtype)
         for b in range(B):
             for hq in range(nq):
@@ -242,11 +244,19 @@ class Oracle:
         B, nkv, C, dh = kh.shape
         c = self.cache.get((l, sl))
         if c is None:
-            c = _Cache(np.zeros((B, nkv, 0, dh), self.dtype), np.zeros((B, nkv, 0, dh), self.dtype))
+            c = _Cache(np.zeros((B, nkv, 0, dh), self.dtype), np.zeros((B, nkv, 0, dh), self.dtype),
+                       P0)
         # positions >= P0 are (re)written; earlier ones are kept
-        c = _Cache(np.concatenate([c.k[:, :, :P0], kh], axis=2),
-                   np.concatenate([c.v[:, :, :P0], v], axis=2))
-        self.cache[(l, sl)] = c
+        n_old = P0 - c.first
+        k = np.concatenate([c.k[:, :, :n_old], kh], axis=2)
+        v = np.concatenate([c.v[:, :, :n_old], v], axis=2)
+        first = c.first
+        if not self.shape.is_full(l):
+            # keep the last W positions: a query at position t >= P0 + C sees
+            # keys j > t - W only, so older keys are never read again
+            drop = max(0, P0 + C - self.shape.window - first)
+            k, v, first = k[:, :, drop:], v[:, :, drop:], first + drop
+        self.cache[(l, sl)] = _Cache(k, v, first)
         self.written.setdefault((l, sl), set()).update(range(P0, P0 + C))
 
     # --------------------------------------------------------------- forward

@@ -350,7 +350,7 @@ def _final_loop_everywhere(o, sh, k):
     for l in range(sh.n_in, sh.n_in + sh.n_rec):
         fin = o.cache[(l, k)]
         for i in range(1, k):
-            o.cache[(l, i)] = type(fin)(fin.k.copy(), fin.v.copy())
+            o.cache[(l, i)] = type(fin)(fin.k.copy(), fin.v.copy(), fin.first)
 
 
 @pytest.mark.parametrize("k", [2, 4])
