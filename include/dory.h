@@ -236,6 +236,14 @@ DORY_API int dory_profile_end(dory_t* m, double* ms, int* launches);
  * C = tokens per sequence in that chunk.  dst: device fp32. */
 DORY_API int dory_debug_hidden(dory_t* m, float* dst, int max_rows, void* stream);
 
+/* Test-only: launches one block whose mbarrier wait is never completed,
+ * bounded by limit_us microseconds (1 .. 100000) instead of the kernels' 2 s.
+ * The wait gives up, writes 0x71 to the handle's device status word (read
+ * and cleared by dory_device_status) and the kernel returns, leaving the
+ * context usable.  It runs the bounded-wait routine every TMA / tcgen05
+ * kernel of the library uses.  DORY_EUNBOUND before dory_bind. */
+DORY_API int dory_debug_expire_wait(dory_t* m, int limit_us, void* stream);
+
 /* Byte offset of the K (which = 0) or V (which = 1) block of (layer, slice)
  * inside the KV region, and its ring size in slots. */
 DORY_API int dory_debug_kv_offset(const dory_t* m, int layer, int slice, int which,
@@ -289,20 +297,35 @@ DORY_API size_t dory_debug_attention_scratch_bytes(int B, int n_q, int head_dim)
  * or a latency-critical serving loop that forbids cudaMalloc after start-up
  * because it can block and synchronise the device.
  *
- * Arguments and result are those of dory_debug_attention with C == 1 (q
- * [B, n_q, head_dim], k_cur / v_cur [B, n_kv, head_dim], gate and out
- * [B, n_q * head_dim], cache [B, n_kv, S, head_dim] holding positions < P0 in
- * slot p mod S; bf16, device).  The split-key partial results live in a fixed
- * 16 MiB array inside the library; every GPU that loads the library holds it
- * until the process exits.  Calls with
- * dory_debug_attention_scratch_bytes(B, n_q, head_dim) > 16 MiB are refused
- * with DORY_ECAPACITY before any launch (for head_dim 128 that is
- * B * n_q > 252).  The first call on a device looks the array's device
- * address up (cudaGetSymbolAddress, device current); make that first call
- * before any stream capture.  All calls share the one array and leave it
- * holding their partials; nothing in it needs to start at zero, but calls
- * whose kernels overlap on the GPU (other streams, other threads) race on it,
- * so serialise them. */
+ * Arguments: q [B, n_q, head_dim] (queries already rotated, normalised and
+ * scaled), k_cur / v_cur [B, n_kv, head_dim] (the new token's key and value,
+ * at position P0), gate and out [B, n_q * head_dim], k_cache / v_cache
+ * [B, n_kv, S, head_dim] holding positions < P0 in ring slot p mod S; all
+ * bf16, device.  out = gate * softmax-weighted values over the keys that the
+ * mask shows (positions j <= P0, and P0 - j < window when window > 0).
+ * It runs the split-key kernel pair of attn.cuh (attn_decode_split_kernel:
+ * one CTA per (split, kv head, sequence), scalar fp32 dot products; then
+ * attn_decode_combine_kernel merges the splits and applies the gate), not
+ * the TMA-fed kernel of the forward pass; results agree with
+ * dory_debug_attention with C == 1 up to rounding order.
+ *
+ * Refusals, all before any launch: DORY_EINVAL for null pointers, n_q not a
+ * multiple of n_kv or n_q / n_kv > 8, k_cur / v_cur / k_cache / v_cache not
+ * 16-byte aligned (q, gate, out: 2-byte), or a ring too small for the keys
+ * the mask shows (S < P0 with window <= 0, S < min(P0, window - 1) with a
+ * window); DORY_EUNSUPPORTED for head_dim outside {32, 64, 128};
+ * DORY_ECAPACITY when the partials would not fit the array (below).
+ *
+ * The split-key partial results live in a fixed 16 MiB array inside the
+ * library; every GPU that loads the library holds it until the process
+ * exits.  Calls with dory_debug_attention_scratch_bytes(B, n_q, head_dim) >
+ * 16 MiB are refused (for head_dim 128 that is B * n_q > 252).  Every call
+ * looks up the array's device address in the current device's context
+ * (cudaGetSymbolAddress); the first call on a device also loads the module
+ * there, so make that first call before any stream capture.  All calls share
+ * the one array and leave it holding their partials; nothing in it needs to
+ * start at zero, but calls whose kernels overlap on the GPU (other streams,
+ * other threads) race on it, so serialise them. */
 DORY_API int dory_decode_attention_noalloc(const void* q, const void* k_cur, const void* v_cur,
                                            const void* k_cache, const void* v_cache,
                                            const void* gate, void* out, int B, int P0, int S,

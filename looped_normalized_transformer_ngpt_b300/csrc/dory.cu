@@ -1675,6 +1675,34 @@ int dory_debug_hidden(dory_t* m, float* dst, int max_rows, void* stream) {
              : DORY_ECUDA;
 }
 
+}  // extern "C"
+
+namespace {
+// Test-only: thread 0 waits for phase 0 of an mbarrier that expects one
+// arrival and never gets it, through the same bounded wait the TMA and
+// tcgen05 kernels use, with a short limit; the wait gives up, writes
+// DEV_PROBE_WAIT to the status word and the kernel returns.
+__global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, status, DEV_PROBE_WAIT, limit_ns);
+}
+}  // namespace
+
+extern "C" {
+
+int dory_debug_expire_wait(dory_t* m, int limit_us, void* stream) {
+  if (!m || limit_us < 1 || limit_us > 100000) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      (unsigned long long)limit_us * 1000ull, wsp<int>(m, m->L.status));
+  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
 int dory_debug_kv_offset(const dory_t* m, int layer, int slice, int which, size_t* offset,
                          int* slots) {
   if (!m || !offset || !slots) return DORY_EINVAL;
@@ -1801,24 +1829,19 @@ static constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;   // 16 MiB per
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
-
-// Device address of the array on the current device, looked up once per
-// device (host code cannot use the symbol itself as a device pointer).
+// Device address of the array in the current device's context.  Host code
+// cannot use the symbol itself as a device pointer.  The address is looked up
+// on every call (a host-side table lookup once the module is loaded), so a
+// context torn down and created again never leaves a stale pointer behind.
 int noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
-    return DORY_ECUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORY_ECUDA;
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORY_ECUDA;
+  *out = p;
   return DORY_OK;
+}
+
+bool aligned_to(const void* p, uintptr_t bytes) {
+  return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
 }
 }  // namespace
 
@@ -1832,6 +1855,14 @@ extern "C" int dory_decode_attention_noalloc(const void* q, const void* k_cur, c
     return DORY_EINVAL;
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return DORY_EUNSUPPORTED;
   if (P0 > 0 && (!k_cache || !v_cache || S <= 0)) return DORY_EINVAL;
+  // keys and values are read as 16-byte vectors, q, gate and out as bf16
+  if (!aligned_to(k_cur, 16) || !aligned_to(v_cur, 16) || !aligned_to(q, 2) ||
+      !aligned_to(gate, 2) || !aligned_to(out, 2))
+    return DORY_EINVAL;
+  if (P0 > 0 && (!aligned_to(k_cache, 16) || !aligned_to(v_cache, 16))) return DORY_EINVAL;
+  // the ring must still hold every cached key the mask shows: P0 of them
+  // under full attention, min(P0, window - 1) under a window
+  if (P0 > 0 && S < (window > 0 ? (P0 < window - 1 ? P0 : window - 1) : P0)) return DORY_EINVAL;
   const size_t need = dory_debug_attention_scratch_bytes(B, n_q, head_dim);
   if (need == 0 || need > kNoAllocScratchBytes) return DORY_ECAPACITY;
   void* scratch = nullptr;
