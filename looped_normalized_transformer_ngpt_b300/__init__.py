@@ -84,6 +84,7 @@ _SIGS = {
     "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
     "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
     "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "dory_debug_expire_wait": (_I, [_P, _I, _P]),
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -273,6 +274,12 @@ class Model:
         _check("dory_device_status", lib().dory_device_status(self.handle, ctypes.byref(v),
                                                               _stream_ptr(stream)))
         return v.value
+
+    def expire_wait(self, limit_us=1000, stream=None):
+        """Test-only: one kernel whose bounded wait is never completed gives up
+        after limit_us and sets the device status word (code 0x71)."""
+        _check("dory_debug_expire_wait", lib().dory_debug_expire_wait(self.handle, limit_us,
+                                                                      _stream_ptr(stream)))
 
     def set_persistent_decode(self, enable: bool):
         """Decode steps of <= 16 sequences as one persistent kernel (default)

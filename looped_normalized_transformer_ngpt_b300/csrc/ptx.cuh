@@ -24,6 +24,7 @@ enum : int {
   DEV_ATTN_ALIGN = 0x45,
   DEV_DEC_PRODUCER = 0x51,
   DEV_DEC_CONSUMER = 0x52,
+  DEV_PROBE_WAIT = 0x71,   // the test-only kernel whose wait nobody completes
 };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
@@ -71,15 +72,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity.  Returns false (after writing
-// `code` to *status, if non-null) when kWaitLimitNs pass first.
+// `code` to *status, if non-null) when limit_ns pass first.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
-                                                  int code) {
+                                                  int code,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if ((++n & 255u) == 0 && globaltimer() - t0 > limit_ns) {
       if (status) atomicCAS(status, 0, code);
       return false;
     }

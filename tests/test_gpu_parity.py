@@ -196,3 +196,32 @@ def test_bad_token_sets_device_status(dev):
     m.prefill(_tok(np.array([[1, 2, shape.vocab + 5, 3]], np.int32)), 1)
     assert m.device_status() != 0
     assert m.device_status() == 0                      # cleared by the read
+
+
+def test_expired_bounded_wait_sets_device_status_and_context_survives(dev):
+    """Failure detection without a fault: a kernel waits on an mbarrier phase
+    that nothing completes, with a 2 ms limit instead of 2 s.  It gives up,
+    reports its site code (0x71) through the status word and returns; the
+    same handle then computes a prefill that still matches the oracle."""
+    import time
+
+    import torch
+    shape = synth.TINY
+    w = synth.make_weights(shape)
+    m = dev.Model(shape, w, max_batch=1, max_ctx=16, max_chunk=16)
+    assert m.device_status() == 0
+    t0 = time.perf_counter()
+    m.expire_wait(2000)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert 0.002 <= waited < 1.0, waited
+    assert m.device_status() == 0x71
+    assert m.device_status() == 0
+    prompt = synth.tokens(shape, 1, 12, seed=3)
+    lg = m.prefill(_tok(prompt), 2).cpu().numpy()
+    ref = oracle.Oracle(shape, w).prefill(prompt, 2, oracle.LAST_LOOP)
+    check_logits(lg, ref["logits"][:, -1])
+    assert m.device_status() == 0
+    with pytest.raises(dev.DoryError):
+        m.expire_wait(0)
+    m.close()
