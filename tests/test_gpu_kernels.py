@@ -20,6 +20,17 @@ def dev(cuda_ok):
     return dory
 
 
+def assert_rows_close(got, want, tol=8e-3):
+    """Error of each output row (one query head, all head_dim values)
+    relative to that row's norm.  The attention outputs are about
+    0.3 / sqrt(visible keys) in size, so a fixed absolute tolerance at bf16
+    scale would pass anything once the context is long; relative to the row,
+    bf16 inputs and outputs leave a few 1e-3."""
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    rel = np.linalg.norm(got - want, axis=-1) / np.maximum(np.linalg.norm(want, axis=-1), 1e-30)
+    assert rel.max() <= tol, (rel.max(), np.unravel_index(rel.argmax(), rel.shape))
+
+
 def _bf16(t):
     import torch
     return t.to(torch.bfloat16)
@@ -131,7 +142,7 @@ def test_attention_matches_oracle(dev, dh, nq, nkv, W, P0, C):
             o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G], qpos,
                                  np.arange(L), W, W <= 0, math.sqrt(dh))
             want = o * gate[b].reshape(C, nq, dh)[:, h]
-            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
+            assert_rows_close(out[b, :, h], want)
 
 
 # Shapes on the tcgen05 prefill attention (head_dim 128, key tiles of 128
@@ -174,13 +185,13 @@ def test_tc_attention_matches_oracle_and_mma_sync(dev, nq, nkv, W, P0, C):
             o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G], qpos,
                                  np.arange(L), W, W <= 0, math.sqrt(dh))
             want = o * gate[b].reshape(C, nq, dh)[:, h]
-            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
+            assert_rows_close(out[b, :, h], want)
     dev.set_debug_tc_attention(False)
     try:
         ref, *_ = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 2)
     finally:
         dev.set_debug_tc_attention(True)
-    np.testing.assert_allclose(out, ref, atol=2e-2, rtol=2e-2)
+    assert_rows_close(out, ref)
 
 
 # One-token attention on the TMA-fed decode kernel (head_dim 128, cache rings
@@ -220,4 +231,4 @@ def test_decode_tma_attention_matches_oracle(dev, nq, nkv, W, P0, S):
             o = oracle.attention(q[b, :, h], k_all[b, :, h // G], v_all[b, :, h // G],
                                  np.arange(P0, L), np.arange(L), W, W <= 0, math.sqrt(dh))
             want = o * gate[b].reshape(C, nq, dh)[:, h]
-            np.testing.assert_allclose(out[b, :, h], want, atol=2e-2, rtol=2e-2)
+            assert_rows_close(out[b, :, h], want)

@@ -56,13 +56,16 @@ def test_full_size_prefill_sampled_sequences(dev, weights, k):
 
 @pytest.mark.parametrize("k,mode", [(2, oracle.LAST_LOOP), (3, oracle.PER_LOOP)])
 @pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "perkernel"])
-def test_decode_steps(dev, weights, k, mode, persistent):
+@pytest.mark.parametrize("max_ctx", [99, 128], ids=["ring99", "ring128"])
+def test_decode_steps(dev, weights, k, mode, persistent, max_ctx):
+    """A cache capacity of 99 positions runs the cp.async decode attention; 128
+    (a multiple of 64) the TMA-fed one that the benchmark times."""
     sh = synth.SMALL
     B, T, D = 3, 96, 3
     prompt = synth.tokens(sh, B, T, seed=7)
     dec = synth.tokens(sh, B, D, seed=8)
     o = oracle.Oracle(sh, weights, dtype=np.float32)
-    m = dev.Model(sh, weights, max_batch=B, max_ctx=T + D, max_chunk=T, k_max=k, cache_mode=mode)
+    m = dev.Model(sh, weights, max_batch=B, max_ctx=max_ctx, max_chunk=T, k_max=k, cache_mode=mode)
     m.set_persistent_decode(persistent)
     r = o.prefill(prompt, k, mode)
     lg = m.prefill(_tok(prompt), k, mode)
