@@ -259,6 +259,27 @@ class Oracle:
         self.cache[(l, sl)] = _Cache(k, v, first)
         self.written.setdefault((l, sl), set()).update(range(P0, P0 + C))
 
+    def restore(self, length: int, mode: int, k: int, caches: dict):
+        """Start from a saved cache state, to replay single steps at contexts
+        too long to prefill here.  caches maps (layer, slice) to (K, V, first):
+        arrays [B, n_kv, L, dh] holding positions first .. first + L - 1 of
+        every sequence, L = length - first.  Slices are numbered as in step():
+        loop index 1..k for recurrent layers under per-loop caching, else 0.
+        Last-Loop KV Caching fixes what each slice holds; the caller supplies
+        the values."""
+        self.reset()
+        self.length = length
+        self.mode_bound = mode
+        if mode == PER_LOOP:
+            self.k_bound = k
+        for (l, sl), (kk, vv, first) in caches.items():
+            kk, vv = np.asarray(kk, self.dtype), np.asarray(vv, self.dtype)
+            if kk.shape != vv.shape or first + kk.shape[2] != length:
+                raise ValueError("cache slice does not end at the current length")
+            self.batch = kk.shape[0]
+            self.cache[(l, sl)] = _Cache(kk, vv, first)
+            self.written[(l, sl)] = set(range(first, length))
+
     # --------------------------------------------------------------- forward
     def step(self, tokens: np.ndarray, k: int, mode: int):
         """Process tokens [B, C] at positions length .. length+C-1.

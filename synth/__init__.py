@@ -141,10 +141,24 @@ def embeddings(shape: Shape, shape_id: int | None = None) -> dict:
     }
 
 
-def make_weights(shape: Shape, shape_id: int | None = None) -> dict:
-    """All weights of a model: {'embed_in', 'embed_out', 's_z', 'layers': [...]}"""
-    w = embeddings(shape, shape_id)
-    w["layers"] = [layer_weights(shape, l, shape_id) for l in range(shape.n_layers)]
+def make_weights(shape: Shape, shape_id: int | None = None, workers: int = 1) -> dict:
+    """All weights of a model: {'embed_in', 'embed_out', 's_z', 'layers': [...]}.
+
+    workers > 1 draws the tensors on that many threads (each tensor has its
+    own seed, so the values do not depend on the thread count)."""
+    if workers <= 1:
+        w = embeddings(shape, shape_id)
+        w["layers"] = [layer_weights(shape, l, shape_id) for l in range(shape.n_layers)]
+        return w
+    from concurrent.futures import ThreadPoolExecutor
+    sid = SHAPE_ID[shape.name] if shape_id is None else shape_id
+    V, d = shape.vocab, shape.d
+    emb = lambda name: round_bf16(_unit_rows(_gauss(sid, -1, _TID[name], (V, d))))
+    with ThreadPoolExecutor(workers) as ex:
+        e_in, e_out = ex.submit(emb, "embed_in"), ex.submit(emb, "embed_out")
+        layers = list(ex.map(lambda l: layer_weights(shape, l, shape_id), range(shape.n_layers)))
+        w = {"embed_in": e_in.result(), "embed_out": e_out.result(), "s_z": np.ones(V, np.float32),
+             "layers": layers}
     return w
 
 

@@ -539,3 +539,25 @@ def test_logit_scale_is_per_vocabulary_entry():
     np.testing.assert_allclose(b["logits"], a["logits"] * s, rtol=1e-14, atol=1e-16)
     np.testing.assert_allclose(a["logits"], a["hidden"] @ w["embed_out"].astype(np.float64).T,
                                rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("mode", [LAST_LOOP, PER_LOOP], ids=["last", "perloop"])
+def test_restore_replays_the_next_step(mode):
+    """A step replayed from a copy of the cache state (what the GPU tests
+    export at long contexts) equals the step taken by the oracle that built
+    that state."""
+    sh, k = synth.TINY_LOOPFULL, 3
+    w = synth.make_weights(sh)
+    a = oracle.Oracle(sh, w)
+    a.prefill(synth.tokens(sh, 2, 37), k, mode)
+    a.decode(synth.tokens(sh, 2, 1, seed=1)[:, 0], k, mode)
+    saved = {key: (c.k.copy(), c.v.copy(), c.first) for key, c in a.cache.items()}
+    b = oracle.Oracle(sh, w)
+    b.restore(a.length, mode, k, saved)
+    tok = synth.tokens(sh, 2, 1, seed=2)[:, 0]
+    ra, rb = a.decode(tok, k, mode), b.decode(tok, k, mode)
+    assert np.array_equal(ra["logits"], rb["logits"])
+    chunk = synth.tokens(sh, 2, 9, seed=3)
+    assert np.array_equal(a.prefill(chunk, k, mode)["logits"], b.prefill(chunk, k, mode)["logits"])
+    with pytest.raises(ValueError):
+        b.restore(a.length + 1, mode, k, saved)
