@@ -1,12 +1,16 @@
 #!/usr/bin/env python
 """Throughput of the looped normalized-GPT forward pass on B300.
 
-One step = one request pass over the small looped nGPT (d = 1024, 4 input /
-10 recurrent / 4 output layers, 8 q / 2 kv heads, head_dim 128, SwiGLU 2816,
-vocab 32000, window 512, 3:1 sliding-window : full): prefill of 4 x 2048
-uniform-random tokens at loop count k (default 4) with the last-loop KV cache,
-then 8 greedy decode steps of the same 4 sequences.  Weights are random
-unit-norm bf16 matrices (synthetic; no trained checkpoint), tokens seeded.
+Default line: the 4B-class model (d 2048, 16 input / 40 recurrent / 16
+output layers, 16 q / 4 kv heads of 128, SwiGLU 6144, vocab 131072, window
+4096, 3:1 sliding-window : full).  One step = prefill of one 8192-token
+sequence at loop count k (default 4) with the last-loop KV cache, then 8
+greedy decode steps of 64 other sequences that each hold a 32768-position
+last-loop cache (built once, untimed, by chunked prefill of random tokens).
+Weights are random unit-norm bf16 matrices (synthetic; no trained
+checkpoint), tokens seeded.  Per-k breakdowns report prefill at k = 1, 2, 4
+and decode at k = 1..4.  `--workload small` runs the small looped nGPT line
+(d 1024, 4/10/4 layers, 4 x 2048 prefill + 8 decode steps of those 4).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -32,7 +36,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "looped fwd tokens/s at k=1/2/4 (prefill, decode); % of BF16 TC / HBM roofline"
-BATCH, SEQ, DECODE = 4, 2048, 8
+BATCH, SEQ, DECODE = 4, 2048, 8                 # small looped nGPT line
+HEAD_T, HEAD_B, HEAD_CTX = 8192, 64, 32768      # 4B-class line: prefill 1 x 8192, decode 64 x 32768
+BUILD_CHUNK = 1024                              # chunk of the untimed cache-building prefill
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 
 
 def ctx64(n: int) -> int:
@@ -416,6 +423,278 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------ 4B-class line
+def layer_apps(sh, k):
+    """Layer indices in execution order: input block, k passes of the
+    recurrent block, output block (32 + 40k applications at the 4B class)."""
+    return list(range(sh.n_in)) + [l for _ in range(k) for l in range(sh.n_in, sh.n_in + sh.n_rec)] \
+        + list(range(sh.n_in + sh.n_rec, sh.n_layers))
+
+
+def decode_class_bytes(sh, B, k, P0):
+    """Algorithmic HBM bytes of one decode step at position P0 per kernel
+    class: each projection's weights once per layer application, the LM head
+    once, and the attention's visible cached K/V (its own new K/V is not read
+    from HBM).  Sums to decode_step_bytes."""
+    lp = layer_params(sh)
+    by = {"qkvg_gemm": 0, "o_gemm": 0, "upgate_gemm": 0, "down_gemm": 0, "attention": 0}
+    for l in layer_apps(sh, k):
+        for c in ("qkvg", "o", "upgate", "down"):
+            by[c + "_gemm"] += 2 * lp[c]
+        keys = P0 if sh.is_full(l) else min(P0, sh.window - 1)
+        by["attention"] += B * 2 * sh.n_kv * sh.head_dim * 2 * keys
+    by["lm_head"] = 2 * sh.vocab * sh.d
+    return by
+
+
+def _roof(bound, kernel, ach, peaks, peak_src, unit, **extra):
+    peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+    nom = NOMINAL["bf16_tflops"] if bound == "tensor" else NOMINAL["hbm_gbs"]
+    src = "bf16 burst: kernels event-timed launch by launch" if bound == "tensor" else "hbm copy"
+    r = {"bound": bound, "kernel": kernel, "achieved": round(ach, 1), "peak": peak,
+         "peak_source": f"{peak_src} ({src})", "unit": unit, "frac": round(ach / peak, 4),
+         "frac_of_nominal": round(ach / nom, 4), "nominal_peak": nom}
+    r.update(extra)
+    return r
+
+
+def run_gpu_headline(args):
+    import torch
+
+    import synth
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    _build.build()
+    sh = synth.DORY4B
+    K, D = args.k, args.decode
+    T, B, CTX = HEAD_T, HEAD_B, HEAD_CTX
+    w = synth.make_weights_torch(sh, device=dev, seed=rank)
+    w["layers"] = list(w["layers"])
+    mp = dory.Model(sh, w, max_batch=1, max_ctx=T, max_chunk=T, k_max=4, device=dev)
+    md = dory.Model(sh, w, max_batch=B, max_ctx=ctx64(CTX + D), max_chunk=BUILD_CHUNK, k_max=4,
+                    device=dev)
+    del w
+    torch.cuda.empty_cache()
+    stream = torch.cuda.Stream(device=dev)
+    prompt_np = synth.tokens(sh, 1, T, seed=3000 + rank)
+    first_np = synth.tokens(sh, B, 1, seed=5000 + rank)[:, 0]
+    prompt = torch.tensor(prompt_np, device=dev)
+    first = torch.tensor(first_np, device=dev)
+    # the decode sequences' caches: chunked prefill of 64 x 32768 random
+    # tokens at k = 1 (last-loop caches have the same layout at any k)
+    t_build = time.perf_counter()
+    with torch.cuda.stream(stream):
+        md.reset()
+        md.prefill(torch.tensor(synth.tokens(sh, B, CTX, seed=4000 + rank), device=dev), 1,
+                   stream=stream)
+    stream.synchronize()
+    t_build = time.perf_counter() - t_build
+    assert md.device_status(stream) == 0, "device status word set while building the caches"
+    V = sh.vocab
+    lg_p = torch.empty((1, V), dtype=torch.float32, device=dev)
+    lg_d = torch.empty((B, V), dtype=torch.float32, device=dev)
+    nxt = torch.empty((D, B), dtype=torch.int32, device=dev)
+
+    def prefill_part(k):
+        mp.reset()
+        mp.prefill(prompt, k, logits=lg_p, stream=stream)
+
+    def decode_part(k):
+        md.set_length(B, CTX)
+        for s_ in range(D):
+            md.decode(first if s_ == 0 else nxt[s_ - 1], k, logits=lg_d, next_tokens=nxt[s_],
+                      stream=stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()                                   # eager warm-up (lazy init)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def replay(g, n):
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                g.replay()
+
+    def time_graph(g, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(g, n)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # ---- headline: K steps of (prefill 1 x 8192 + D decode steps of 64) at loop count K
+    with torch.cuda.stream(stream):
+        prefill_part(K)
+        n_launch = mp.launch_count()
+        decode_part(K)
+        n_launch += D * md.launch_count()
+    g_step = capture(lambda: (prefill_part(K), decode_part(K)))
+    replay(g_step, args.warmup)
+    stream.synchronize()
+    dist_barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(g_step, args.steps)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        dist_barrier()
+    ms_step = dist_max(e0.elapsed_time(e1) / args.steps, dev)
+    tok_step = T + B * D
+    value = aggregate_throughput(tok_step, world, ms_step / 1e3)
+    assert mp.device_status(stream) == 0 and md.device_status(stream) == 0, \
+        "device status word set during the timed steps"
+    del g_step
+    peaks, peak_src = load_peaks()
+
+    # ---- per-k: prefill (k = 1, 2, 4) and decode (k = 1..4) timed as graphs
+    reps = max(3, args.steps // 4)
+    per_k = {}
+    for k in args.per_k:
+        g = capture(lambda: prefill_part(k))
+        replay(g, 2)
+        tp = time_graph(g, reps)
+        del g
+        fl = step_flops(sh, 1, T, k, logit_rows=1)
+        tf = sum(fl.values()) / (tp / 1e3) / 1e12
+        per_k.setdefault(str(k), {}).update({
+            "prefill_tok_s": round(T / (tp / 1e3), 1), "prefill_ms": round(tp, 3),
+            "prefill_tflops": round(tf, 1), "prefill_frac_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
+            "prefill_frac_bf16_nominal": round(tf / NOMINAL["bf16_tflops"], 4)})
+    for k in args.decode_k:
+        g = capture(lambda: decode_part(k))
+        replay(g, 2)
+        td = time_graph(g, reps) / D
+        del g
+        by = sum(sum(decode_class_bytes(sh, B, k, CTX + s_).values()) for s_ in range(D)) / D
+        gbs = by / (td / 1e3) / 1e9
+        per_k.setdefault(str(k), {}).update({
+            "decode_tok_s": round(B / (td / 1e3), 1), "decode_ms_per_step": round(td, 3),
+            "decode_GB_per_step": round(by / 1e9, 2), "decode_GBs": round(gbs, 1),
+            "decode_frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "decode_frac_hbm_nominal": round(gbs / NOMINAL["hbm_gbs"], 4)})
+
+    # ---- roofline: every launch of one eager step event-timed, per kernel class
+    mp.profile_begin(1 << 16)
+    with torch.cuda.stream(stream):
+        prefill_part(K)
+    pprof = mp.profile_end()
+    md.profile_begin(1 << 16)
+    with torch.cuda.stream(stream):
+        decode_part(K)
+    dprof = md.profile_end()
+    pfl = step_flops(sh, 1, T, K, logit_rows=1)
+    dby = {}
+    for s_ in range(D):
+        for c, v in decode_class_bytes(sh, B, K, CTX + s_).items():
+            dby[c] = dby.get(c, 0) + v
+    classes = []
+    for phase, prof, work, bound, unit, scale in (("prefill", pprof, pfl, "tensor", "TFLOP/s", 1e12),
+                                                  ("decode", dprof, dby, "hbm", "GB/s", 1e9)):
+        for name, (ms, cnt) in prof.items():
+            if cnt == 0:
+                continue
+            if name in work and ms > 0:
+                classes.append((ms, f"{phase} {name}", cnt, bound, work[name] / (ms / 1e3) / scale,
+                                unit, work[name] / cnt))
+            else:
+                classes.append((ms, f"{phase} {name}", cnt, None, None, None, None))
+    classes.sort(key=lambda c: -c[0])
+    top = next(c for c in classes if c[3] is not None)
+    ms, name, cnt, bound, ach, unit, per_launch = top
+    roofline = _roof(bound, name, ach, peaks, peak_src, unit,
+                     traffic=traffic_for(name, "4b_headline"),
+                     algorithmic_per_launch=round(per_launch), launches=cnt,
+                     avg_launch_us=round(ms / cnt * 1e3, 2),
+                     unit_of_work="bytes of visible cached K/V read" if bound == "hbm"
+                     else "FLOPs over visible (query, key) pairs / GEMM 2MNK")
+    gemm = ("qkvg_gemm", "o_gemm", "upgate_gemm", "down_gemm")
+    g_ms = sum(pprof[n][0] for n in gemm)
+    roof_gemm = _roof("tensor", "prefill projection GEMMs (QKV+gate, O + nGPT step, up+gate + "
+                      "SwiGLU, down + nGPT step)", sum(pfl[n] for n in gemm) / (g_ms / 1e3) / 1e12,
+                      peaks, peak_src, "TFLOP/s", ms=round(g_ms, 3))
+    dk = per_k[str(K)]
+    roof_dec = _roof("hbm", f"whole decode step (64 x {CTX}, k={K}, CUDA graph)",
+                     dk["decode_GBs"], peaks, peak_src, "GB/s")
+    breakdown = {c[1]: {"ms": round(c[0], 3), "launches": c[2],
+                        "achieved": None if c[4] is None else round(c[4], 1), "unit": c[5]}
+                 for c in classes}
+
+    # ---- end to end through the public API with host buffers (eager calls)
+    host_prompt = torch.tensor(prompt_np).pin_memory()
+    host_first = torch.tensor(first_np).pin_memory()
+    host_out = torch.empty((D, B), dtype=torch.int32).pin_memory()
+    d_prompt = torch.empty_like(prompt)
+    d_first = torch.empty_like(first)
+
+    def e2e_step():
+        d_prompt.copy_(host_prompt, non_blocking=True)
+        d_first.copy_(host_first, non_blocking=True)
+        mp.reset()
+        mp.prefill(d_prompt, K, logits=lg_p, stream=stream)
+        md.set_length(B, CTX)
+        for s_ in range(D):
+            md.decode(d_first if s_ == 0 else nxt[s_ - 1], K, logits=lg_d, next_tokens=nxt[s_],
+                      stream=stream)
+        host_out.copy_(nxt, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        n_e2e = max(3, args.steps // 2)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        stream.synchronize()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+    t_e2e = dist_max(t_e2e, dev)
+    e2e = {"value": round(aggregate_throughput(tok_step, world, t_e2e), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(host_prompt.numel() * 4 + host_first.numel() * 4),
+           "d2h_bytes_per_step": int(host_out.numel() * 4),
+           "note": "eager C-ABI calls (no graph), pinned host tokens in, greedy tokens out"}
+    assert mp.device_status(stream) == 0 and md.device_status(stream) == 0
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded uniform tokens, random unit-norm bf16 weights)",
+           "config": {"workload": f"4B-class looped nGPT (d 2048, 16/40/16 layers, 16/4 heads, "
+                                  f"ffn 6144, vocab 131072, window 4096): prefill 1x{T} + {D} "
+                                  f"greedy decode steps of {B} sequences at {CTX} cached "
+                                  f"positions, k={K}, last-loop KV cache",
+                      "prefill_batch": 1, "seq_len": T, "decode_batch": B,
+                      "decode_context": CTX, "decode_steps": D, "k": K,
+                      "cache_mode": "last_loop", "parallelism": f"replicas x{world}",
+                      "graph": "whole step captured in one CUDA graph",
+                      "decode_cache": f"built untimed by chunked prefill of random tokens at k=1 "
+                                      f"({t_build:.1f} s)",
+                      "l2": "not flushed: each step streams ~8.6 GB of weights per pass and "
+                            "~2.4 TB of cached K/V, far above the 126 MB L2"},
+           "roofline": roofline, "roofline_prefill_gemms": roof_gemm,
+           "roofline_decode_step": roof_dec,
+           "gpu_launches": int(n_launch * args.steps),
+           "clocks": clk.summary(), "e2e": e2e, "per_k": per_k, "breakdown_eager": breakdown}
+    mp.close()
+    md.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_4b(K, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ 4B-class workloads
 def decode_step_bytes(sh, B, k, P0):
     """Algorithmic HBM bytes of one decode step at position P0: every weight
@@ -731,6 +1010,69 @@ def cpu_baseline(k, budget_s=20.0):
                       f"at k={k} (last-loop), small looped nGPT; {t:.1f} s"}
 
 
+def oracle_sample_4b(k, n_tokens, weights):
+    """Times the float32 oracle on the first n_tokens of the 4B-class prefill
+    prompt at loop count k.  Returns seconds."""
+    import numpy as np
+
+    import oracle
+    import synth
+    o = oracle.Oracle(synth.DORY4B, weights, dtype=np.float32)
+    tok = synth.tokens(synth.DORY4B, 1, HEAD_T, seed=3000)[:, :n_tokens]
+    t0 = time.perf_counter()
+    o.prefill(tok, k, oracle.LAST_LOOP)
+    return time.perf_counter() - t0
+
+
+def _weights_4b_host():
+    import synth
+    return synth.make_weights(synth.DORY4B, workers=min(32, os.cpu_count() or 1))
+
+
+def cpu_baseline_4b(k, budget_s=20.0):
+    w = _weights_4b_host()
+    t16 = oracle_sample_4b(k, 16, w)                      # calibration
+    n = int(max(16, min(HEAD_T, 16 * budget_s / max(t16, 1e-6))))
+    t = oracle_sample_4b(k, n, w)
+    return {"value": round(n / t, 2), "unit": "tokens/s", "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"numpy float32 oracle, prefill of the first {n} tokens of the 1x{HEAD_T} "
+                      f"prompt at k={k} (last-loop), full 72-layer 4B-class model; {t:.1f} s"}
+
+
+def run_reference_4b(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    K = args.k
+    w = _weights_4b_host()
+    t16 = oracle_sample_4b(K, 16, w)
+    n_steps = args.steps + args.warmup
+    per_step_budget = max(2.0, 150.0 / n_steps)
+    n = int(max(16, min(HEAD_T, 16 * per_step_budget / t16)))
+    times = []
+    for i in range(n_steps):
+        t = oracle_sample_4b(K, n, w)
+        if i >= args.warmup:
+            times.append(t)
+    ms = 1e3 * sum(times) / len(times)
+    val = n / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
+           "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded uniform tokens, random unit-norm bf16 weights)",
+           "config": {"workload": f"4B-class looped nGPT prefill at k={K}, last-loop KV cache "
+                                  f"(bounded sample: first {n} tokens of the 1x{HEAD_T} prompt "
+                                  f"per step)",
+                      "batch": 1, "seq_len": n, "k": K, "cache_mode": "last_loop"},
+           "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "kind": "oracle",
+                            "cores": _blas_threads(),
+                            "sample": f"1 sequence x {n} tokens prefill per step"},
+           "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -764,6 +1106,38 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_target_4b(args):
+    """The ncu target of the 4B-class line: one eager prefill of 1 x 8192 at
+    loop count --k and one decode step of --batch sequences (default 64) at
+    --ctx cached positions (default 32768; cache contents synthetic, written
+    by torch before any library launch).  --slim cuts the depth to 2/4/2."""
+    import torch
+
+    import synth
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+    _build.build()
+    sh = synth.DORY4B_SLIM if args.slim else synth.DORY4B
+    B, ctx = args.batch, args.ctx or HEAD_CTX
+    w = synth.make_weights_torch(sh)
+    w["layers"] = list(w["layers"])
+    md = dory.Model(sh, w, max_batch=B, max_ctx=ctx64(ctx + 1), max_chunk=1, k_max=4)
+    fill_cache_synthetic(md, sh)
+    md.set_length(B, ctx)
+    first = torch.tensor(synth.tokens(sh, B, 1, seed=5000)[:, 0], device="cuda")
+    n_pre = 0
+    if not args.decode_only:
+        mp = dory.Model(sh, w, max_batch=1, max_ctx=HEAD_T, max_chunk=HEAD_T, k_max=4)
+        mp.prefill(torch.tensor(synth.tokens(sh, 1, HEAD_T, seed=3000), device="cuda"), args.k)
+        n_pre = mp.launch_count()
+    md.decode(first, args.k)
+    torch.cuda.synchronize()
+    assert md.device_status() == 0
+    print(json.dumps({"profile_target": "ok", "shape": sh.name, "k": args.k,
+                      "launches_prefill": n_pre, "launches_decode": md.launch_count(),
+                      "decode_batch": B, "context": ctx}))
+
+
 def run_profile_target(args):
     """One eager prefill (4 x 2048, loop count --k) and one decode step of the
     benchmark workload, nothing else: the target for ncu launch lists and
@@ -790,7 +1164,7 @@ def run_profile_target(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["dory", "reference"], default="dory")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
@@ -798,20 +1172,34 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=4, help="loop count of the timed step")
     ap.add_argument("--decode", type=int, default=DECODE)
     ap.add_argument("--per-k", type=lambda s: [int(x) for x in s.split(",") if x],
-                    default=[1, 2, 4])
+                    default=[1, 2, 4], help="loop counts of the per-k prefill timings")
+    ap.add_argument("--decode-k", type=lambda s: [int(x) for x in s.split(",") if x],
+                    default=[1, 2, 3, 4], help="loop counts of the per-k decode timings "
+                                               "(4B-class line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--slim", action="store_true",
                     help="4B-class width with 2/4/2 layers (profiling targets)")
     ap.add_argument("--ctx", type=int, default=0, help="context of the decode workloads")
-    ap.add_argument("--workload", choices=["small", "prefill4b", "decode4b", "longctx4b",
-                                           "longprefill4b", "divergence4b"],
-                    default="small", help="small: the default benchmark line; the others time "
-                                          "the 4B-class workloads (one JSON line, not the contract)")
+    ap.add_argument("--batch", type=int, default=HEAD_B,
+                    help="decode sequences of the 4B-class profile target")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="4B-class profile target: skip the prefill")
+    ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
+                                           "longctx4b", "longprefill4b", "divergence4b"],
+                    default="headline4b",
+                    help="headline4b: the default benchmark line (4B-class prefill 1x8192 + "
+                         "decode 64x32768); small: the small looped nGPT line; the others time "
+                         "single 4B-class workloads (one JSON line each, not the contract)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 warm-up steps
     if args.impl == "reference":
-        run_reference(args)
+        run_reference_4b(args) if args.workload == "headline4b" else run_reference(args)
+    elif args.workload == "headline4b":
+        if args.mode == "profile":
+            run_profile_target_4b(args)
+        else:
+            run_gpu_headline(args)
     elif args.workload != "small":
         run_workload_4b(args)
     elif args.mode == "profile":

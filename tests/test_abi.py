@@ -188,3 +188,10 @@ def test_bench_work_models_match_the_closed_forms():
     for k, w in ((1, 18.2), (4, 47.6)):
         d = bench.decode_step_bytes(synth.DORY4B, 1, k, 262144)
         assert close((d["weights"] + d["kv"]) / 1e9, w), k
+    # the per-class split the roofline uses adds up to the same bytes
+    for B, k, P0 in ((64, 1, 32768), (64, 4, 32775), (1, 3, 100), (4, 2, 5000)):
+        d = bench.decode_step_bytes(synth.DORY4B, B, k, P0)
+        c = bench.decode_class_bytes(synth.DORY4B, B, k, P0)
+        assert sum(c.values()) == d["weights"] + d["kv"] and c["attention"] == d["kv"]
+    assert [bench.layer_apps(synth.DORY4B, k).count(20) for k in (1, 2, 4)] == [1, 2, 4]
+    assert len(bench.layer_apps(synth.DORY4B, 4)) == 192
