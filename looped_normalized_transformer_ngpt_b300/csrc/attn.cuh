@@ -529,6 +529,7 @@ struct DecAttnArgs {
   int P0, S, n_q, n_kv, window;
   float scale_log2;
   int chunk, n_splits;
+  int tpg;                        // TMA kernel: 64-key tiles per (sequence, kv head) group
   float* part_o;                  // [B, n_q, n_splits, dh]
   float* part_ml;                 // [B, n_q, n_splits, 2]
   int* counter;                   // [B * n_kv], zero between launches

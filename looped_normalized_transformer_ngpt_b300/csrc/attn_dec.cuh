@@ -2,14 +2,19 @@
 // head_dim 128 ("Dory1.0-4B: A Looped Normalized-GPT", Architecture;
 // Last-Loop KV Caching).
 //
-// Same operation and work split as attn_decode_kernel (attn.cuh): one new
-// token per sequence at position P0, its G query heads per kv head, the
-// cached keys of the sequence split into equal ranges; every (split, kv head,
-// sequence) item writes an unnormalised partial (o, max, sum) per head, and
-// the last CTA of the (sequence, kv head) group (atomic ticket) merges the
-// partials with the new token's own key / value, applies sigmoid(g) and
-// writes the gated output; split 0 stores the new k^ / v into ring slot
-// P0 mod S.
+// Same operation as attn_decode_kernel (attn.cuh): one new token per
+// sequence at position P0, its G query heads per kv head.  The work is
+// scheduled stream-K style: the 64-key tiles of all (sequence, kv head)
+// groups form one sequence of T = groups x tiles-per-group tiles, and CTA c
+// of n takes tiles [c T / n, (c + 1) T / n), so every CTA streams the same
+// number of bytes whatever the group count (no partly empty last round).  A
+// CTA's range may cross group boundaries; each (CTA, group) piece is one
+// split and writes an unnormalised partial (o, max, sum) per head.  The CTA
+// holding tile x is ((x + 1) n - 1) / T, which gives each piece its split
+// index and each group its number of splits.  The last CTA of the group
+// (atomic ticket) merges the partials with the new token's own key / value,
+// applies sigmoid(g) and writes the gated output; split 0 stores the new
+// k^ / v into ring slot P0 mod S.
 //
 // What differs is the key / value path, which carries nearly all of the
 // bytes of a long-context decode step:
@@ -84,8 +89,10 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
   const int P0 = a.P0;
   const int lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;   // first visible cached key
   const int lo_a = lo / kDecTile * kDecTile;
-  const int NS = a.n_splits;
-  const int n_items = NS * a.n_kv * a.B;
+  const int n_groups = a.n_kv * a.B;
+  const long long tpg = a.tpg;
+  const long long T = (long long)n_groups * tpg;
+  const long long ncta = gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < kDecTmaStages; ++s) {
@@ -99,14 +106,37 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
   }
   __syncthreads();
 
-  auto item_range = [&](int item, int& split, int& kvh, int& b, int& k0, int& k1, int& ntiles) {
-    split = item % NS;
-    kvh = (item / NS) % a.n_kv;
-    b = item / (NS * a.n_kv);
-    k0 = lo_a + split * a.chunk;                       // 64-aligned
-    k1 = min(k0 + a.chunk, P0);                        // cached keys only
-    ntiles = k1 > k0 ? (k1 - k0 + kDecTile - 1) / kDecTile : 0;
+  // This CTA's pieces in order.  With cached keys: its tile range cut at
+  // group boundaries; without (tpg == 0): groups blockIdx.x, + gridDim.x, ...
+  // as single pieces with no tiles.  `cur` is the piece's first global tile
+  // (or its group); returns false past the last piece.
+  const long long x_end = tpg > 0 ? ((long long)blockIdx.x + 1) * T / ncta : n_groups;
+  auto piece = [&](long long cur, int& grp, int& split, int& nseg, int& k0, int& k1,
+                   int& ntiles, long long& next) -> bool {
+    if (cur >= x_end) return false;
+    if (tpg == 0) {
+      grp = (int)cur;
+      split = 0;
+      nseg = 1;
+      k0 = k1 = lo_a;
+      ntiles = 0;
+      next = cur + ncta;
+      return true;
+    }
+    grp = (int)(cur / tpg);
+    const long long g0 = (long long)grp * tpg;
+    const long long e = min(x_end, g0 + tpg);
+    const long long c_first = ((g0 + 1) * ncta - 1) / T;
+    const long long c_last = ((g0 + tpg) * ncta - 1) / T;
+    split = (int)(blockIdx.x - c_first);
+    nseg = (int)(c_last - c_first + 1);
+    k0 = lo_a + (int)(cur - g0) * kDecTile;            // 64-aligned
+    k1 = min(lo_a + (int)(e - g0) * kDecTile, P0);      // cached keys only
+    ntiles = (int)(e - cur);
+    next = e;
+    return true;
   };
+  const long long x_begin = tpg > 0 ? (long long)blockIdx.x * T / ncta : blockIdx.x;
 
   if (warp == 4) {
     // ------------------------------------------------ TMA producer
@@ -116,10 +146,11 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
     // projections).
     if (lane == 0) {
       int g = 0;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
-        int split, kvh, b, k0, k1, ntiles;
-        item_range(item, split, kvh, b, k0, k1, ntiles);
-        const int row0 = (b * a.n_kv + kvh) * a.S;
+      int grp, split, nseg, k0, k1, ntiles;
+      long long nx;
+      for (long long cur = x_begin; !*abort_flag && piece(cur, grp, split, nseg, k0, k1, ntiles, nx);
+           cur = nx) {
+        const int row0 = grp * a.S;                    // group = b * n_kv + kv head
         for (int t = 0; t < ntiles; ++t, ++g) {
           const int st = g % kDecTmaStages;
           if (g >= kDecTmaStages &&
@@ -156,9 +187,11 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
   auto csync = [] { named_bar(1, 128); };
   bool first = true;
   int g = 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    int split, kvh, b, k0, k1, ntiles;
-    item_range(item, split, kvh, b, k0, k1, ntiles);
+  int grp, split, nseg, k0, k1, ntiles;
+  long long nx;
+  for (long long cur = x_begin; piece(cur, grp, split, nseg, k0, k1, ntiles, nx); cur = nx) {
+    const int kvh = grp % a.n_kv, b = grp / a.n_kv;
+    const int NS = nseg;                                 // splits of this group
     const int kv_lo = max(k0, lo);                       // visible keys [kv_lo, k1)
     if (first) {
       pdl_wait();
@@ -406,7 +439,7 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
         L += sL[w * 16 + r] * wt;
         acc += sO[(w * kDecMaxG + r) * DH + dd] * wt;
       }
-      const long long base = ((long long)b * a.n_q + kvh * G + r) * a.n_splits + split;
+      const long long base = ((long long)b * a.n_q + kvh * G + r) * a.n_splits + split;   // stride: max splits
       a.part_o[base * DH + dd] = acc;
       if (dd == 0) {
         a.part_ml[base * 2] = M;
@@ -419,7 +452,7 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
     csync();
     if (tid == 0) {
       const int prev = atomicAdd(&a.counter[b * a.n_kv + kvh], 1);
-      *sFlag = prev == a.n_splits - 1;
+      *sFlag = prev == NS - 1;
     }
     csync();
     if (!*sFlag) continue;
@@ -437,15 +470,15 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
     for (int r = warp; r < G; r += 4) {
       const long long bh = (long long)b * a.n_q + kvh * G + r;
       float mx = sCur[r];
-      for (int sp = lane; sp < NS; sp += 32) mx = fmaxf(mx, __ldcg(a.part_ml + (bh * NS + sp) * 2));
+      for (int sp = lane; sp < NS; sp += 32) mx = fmaxf(mx, __ldcg(a.part_ml + (bh * a.n_splits + sp) * 2));
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
       float L = 0.f;
       for (int sp = lane; sp < NS; sp += 32) {
-        const float ms = __ldcg(a.part_ml + (bh * NS + sp) * 2);
+        const float ms = __ldcg(a.part_ml + (bh * a.n_splits + sp) * 2);
         const float wt = ms == -INFINITY ? 0.f : ex2_ftz(ms - mx);
         sW[r * (NS + 1) + sp] = wt;
-        L += __ldcg(a.part_ml + (bh * NS + sp) * 2 + 1) * wt;
+        L += __ldcg(a.part_ml + (bh * a.n_splits + sp) * 2 + 1) * wt;
       }
       L = warp_sum(L);
       if (lane == 0) {
@@ -460,7 +493,7 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
       const long long bh = (long long)b * a.n_q + kvh * G + r;
       const float* wr = sW + r * (NS + 1);
       float acc = wr[NS] * sVc[dd];
-      const float* po = a.part_o + bh * NS * DH + dd;
+      const float* po = a.part_o + bh * a.n_splits * DH + dd;
       // 16 partials in flight per round
       for (int sp0 = 0; sp0 < NS; sp0 += 16) {
         float ov[16];

@@ -530,33 +530,39 @@ int launch_dec_attn_tma(DecAttnArgs a, int B, cudaStream_t st) {
   const int lo = a.window > 0 ? (a.P0 - a.window + 1 > 0 ? a.P0 - a.window + 1 : 0) : 0;
   const int lo_a = lo / kDecTile * kDecTile;
   const int n_cache = a.P0 - lo_a;                    // cached keys from the aligned start
-  const int groups = B * a.n_kv;
-  const int cap = num_sms();
-  const int max_sp = (n_cache + kDecMinTiles * kDecTile - 1) / (kDecMinTiles * kDecTile);
-  int best_sp = 1;
-  double best = -1.0;
-  for (int sp = 1; sp <= kDecMaxSplits && sp <= (max_sp > 0 ? max_sp : 1); ++sp) {
-    const long long items = (long long)groups * sp;
-    const long long rounds = (items + cap - 1) / cap;
-    const int keys = ((n_cache + sp - 1) / sp + kDecTile - 1) / kDecTile * kDecTile;
-    const double per = (double)rounds * (double)(keys + kDecTile);
-    if (best < 0 || per < best * 0.98) {
-      best = per;
-      best_sp = sp;
+  const long long groups = (long long)B * a.n_kv;
+  // stream-K schedule (attn_dec.cuh): T tiles cut into `grid` equal ranges,
+  // at least kDecMinTiles tiles each; a group spans at most
+  // ceil(tpg / floor(T / grid)) + 1 ranges, which must stay within the
+  // kDecMaxSplits partials per head that the workspace holds
+  const long long tpg = n_cache > 0 ? (n_cache + kDecTile - 1) / kDecTile : 0;
+  const long long T = groups * tpg;
+  long long grid = num_sms();
+  int max_seg = 1;
+  if (tpg == 0) {
+    if (grid > groups) grid = groups;
+  } else {
+    const long long by_min = (T + kDecMinTiles - 1) / kDecMinTiles;
+    if (grid > by_min) grid = by_min;
+    for (;; --grid) {
+      const long long per = T / grid;
+      const long long segs = (tpg + per - 1) / per + 1;
+      if (segs <= kDecMaxSplits || grid == 1) {
+        max_seg = (int)(segs < kDecMaxSplits ? segs : kDecMaxSplits);
+        break;
+      }
     }
   }
-  int chunk = n_cache > 0 ? (n_cache + best_sp - 1) / best_sp : kDecTile;
-  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
-  a.chunk = chunk;
-  a.n_splits = n_cache > 0 ? (n_cache + chunk - 1) / chunk : 1;
+  a.tpg = (int)tpg;
+  a.n_splits = max_seg;
+  a.chunk = 0;
   CUtensorMap tkc, tvc;
   if (!encode_bf16(&tkc, a.k_cache, (uint64_t)a.cache_rows, 128, 128, kDecTile) ||
       !encode_bf16(&tvc, a.v_cache, (uint64_t)a.cache_rows, 128, 128, kDecTile))
     return DORY_EUNSUPPORTED;
-  const long long items = (long long)groups * a.n_splits;
-  const int grid = items < cap ? (int)items : cap;
   a.B = B;
-  return launch_k(attn_decode_tma_kernel<RAW>, dim3(grid), dim3(kDecTmaThreads), DecTmaCfg::SMEM,
+  return launch_k(attn_decode_tma_kernel<RAW>, dim3((unsigned)grid), dim3(kDecTmaThreads),
+                  DecTmaCfg::SMEM,
                   st, tkc, tvc, a) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
@@ -869,10 +875,22 @@ int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n
   g.part_stride = (long long)rows * n_out;
   const int units = ((n_out + 127) / 128) * ((rows + kSwapBN - 1) / kSwapBN);
   const int kb = (K + 63) / 64;
-  int sp = (num_sms() + units - 1) / units;
-  if (sp > kSwapMaxParts) sp = kSwapMaxParts;
-  if (sp > kb / 2) sp = kb / 2;
-  if (sp < 1) sp = 1;
+  // K splits: the persistent CTAs take units (tile, split) round-robin, so a
+  // CTA's time is (its units) x (k blocks per unit + a fixed cost per unit
+  // for the pipeline fill and the partial-sum store, about two k blocks).
+  // Take the split count with the smallest such time; on ties the fewer
+  // partial sums.
+  const int cap = num_sms();
+  int sp = 1;
+  long long best = -1;
+  for (int c = 1; c <= kSwapMaxParts && c <= (kb / 2 > 1 ? kb / 2 : 1); ++c) {
+    const long long rounds = ((long long)units * c + cap - 1) / cap;
+    const long long t = rounds * ((kb + c - 1) / c + 2);
+    if (best < 0 || t < best) {
+      best = t;
+      sp = c;
+    }
+  }
   g.k_splits = sp;
   n_parts = sp;
   return launch_gemm<kSwapBN, EPI_PARTS>(tw, tx, g, st);
