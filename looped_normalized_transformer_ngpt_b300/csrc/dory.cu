@@ -544,6 +544,13 @@ int launch_dec_attn_tma(DecAttnArgs a, int B, cudaStream_t st) {
   } else {
     const long long by_min = (T + kDecMinTiles - 1) / kDecMinTiles;
     if (grid > by_min) grid = by_min;
+    // With few groups a grid that is a multiple of the group count cuts the
+    // ranges at group boundaries (no CTA pays a second prologue and merge);
+    // taken when the ranges are short (latency-bound launches) or it keeps
+    // nearly every SM busy.
+    const long long per_group = grid / groups;
+    if (per_group >= 1 && (tpg / per_group < 32 || groups * per_group * 10 >= grid * 9))
+      grid = groups * per_group;
     for (;; --grid) {
       const long long per = T / grid;
       const long long segs = (tpg + per - 1) / per + 1;
@@ -866,6 +873,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
 int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int rows,
               int K, float* parts, int& n_parts, cudaStream_t st) {
   GemmArgs g{};
+  g.w_pre = 1;   // weight operand: loads may start before the wait
   g.M = n_out;
   g.N = rows;
   g.K = K;
@@ -980,6 +988,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
 
   // QKV + gate projection with RoPE / q-k normalisation / sigmoid fused
   GemmArgs ga{};
+  ga.w_pre = 1;   // weight operand: loads may start before the wait
   ga.M = M;
   ga.N = (2 * c.n_q + 2 * c.n_kv) * c.head_dim;
   ga.K = c.d;
@@ -1096,6 +1105,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
 
   // output projection + nGPT step
   GemmArgs go{};
+  go.w_pre = 1;   // weight operand: loads may start before the wait
   go.M = M;
   go.N = c.d;
   go.K = hq;
@@ -1134,6 +1144,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
 
   // SwiGLU MLP + nGPT step
   GemmArgs gu{};
+  gu.w_pre = 1;   // weight operand: loads may start before the wait
   gu.M = M;
   gu.N = 2 * c.ffn;
   gu.K = c.d;
@@ -1160,6 +1171,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     DORY_TRY(pe(m, st, launch_gemm<kGemmBN, EPI_SWIGLU>(tm_hb, m->tm_upgate[l], gu, st, &emm)));
   }
   GemmArgs gd{};
+  gd.w_pre = 1;   // weight operand: loads may start before the wait
   gd.M = M;
   gd.N = c.d;
   gd.K = c.ffn;
@@ -1343,6 +1355,7 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     // LM head on the selected rows: per sequence, rows C - n .. C-1 of hb
     const int first = C - n_logit_rows;
     GemmArgs gl{};
+    gl.w_pre = 1;   // weight operand: loads may start before the wait
     gl.N = c.vocab;
     gl.K = c.d;
     gl.status = status;

@@ -82,6 +82,11 @@ struct GemmArgs {
   // tiles_n (N / 256 <= 8)
   const float* h32;
   const float* alpha;
+  // 1: the weight operand (A for EPI_PARTS, else B) never changes during the
+  // forward pass, so the producer issues the weight loads of the first ring
+  // stages before waiting on the previous kernel (programmatic launch); the
+  // activation loads follow the wait.  0: every load after the wait.
+  int w_pre;
 };
 
 template <int BN, int EPI = 0>
@@ -711,7 +716,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (C::NGPT) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // set-up above overlaps the previous kernel; global memory only from here
+
+  // (tile, k block) -> operand coordinates, in the producer's order
+  auto coords = [&](int tile, int& m0, int& nb0, int& nb1) {
+    const int tt = tile % (args.tiles_m * args.tiles_n);
+    // EPI_NGPT: the cluster's CTAs take the tiles_n column tiles of a row block
+    const int tm = C::NGPT ? tt / args.tiles_n : tt % args.tiles_m;
+    const int tn = C::NGPT ? tt % args.tiles_n : tt / args.tiles_m;
+    m0 = tm * BM;
+    if (EPI == EPI_SWIGLU) {
+      nb0 = tn * (BN / 2);
+      nb1 = args.b_second + tn * (BN / 2);
+    } else {
+      nb0 = tn * BN;
+      nb1 = tn * BN + BN / 2;
+    }
+  };
+  // weights of the first ring stages, before the wait on the previous kernel
+  // (each stage's barrier expects the whole stage; the activations complete it)
+  int n_pre = 0;
+  if (args.w_pre && warp == 0 && lane == 0) {
+    for (int tile = blockIdx.x; tile < num_tiles && n_pre < STAGES; tile += gridDim.x) {
+      int m0, nb0, nb1, kb_lo, kb_hi;
+      coords(tile, m0, nb0, nb1);
+      kb_range(tile, kb_lo, kb_hi);
+      for (int kb = kb_lo; kb < kb_hi && n_pre < STAGES; ++kb, ++n_pre) {
+        uint8_t* a_dst = smem + n_pre * C::STAGE_BYTES;
+        uint8_t* b_dst = a_dst + C::A_BYTES;
+        mbar_arrive_expect_tx(&full_bar[n_pre], C::STAGE_BYTES);
+        if (EPI == EPI_PARTS) {
+          tma_load_2d(a_dst, &tmA, &full_bar[n_pre], kb * BK, m0);
+        } else {
+          tma_load_2d(b_dst, &tmB, &full_bar[n_pre], kb * BK, nb0);
+          tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[n_pre], kb * BK, nb1);
+        }
+      }
+    }
+  }
+  // set-up above overlaps the previous kernel; global memory it may have
+  // written only from here
   pdl_wait();
   pdl_trigger();
 
@@ -720,33 +763,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int g = 0;                                    // k blocks issued so far
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int tt = tile % (args.tiles_m * args.tiles_n);
-        // EPI_NGPT: the cluster's CTAs take the tiles_n column tiles of a row block
-        const int tm = C::NGPT ? tt / args.tiles_n : tt % args.tiles_m;
-        const int tn = C::NGPT ? tt % args.tiles_n : tt / args.tiles_m;
-        const int m0 = tm * BM;
-        int kb_lo, kb_hi;
+        int m0, nb0, nb1, kb_lo, kb_hi;
+        coords(tile, m0, nb0, nb1);
         kb_range(tile, kb_lo, kb_hi);
-        int nb0, nb1;
-        if (EPI == EPI_SWIGLU) {
-          nb0 = tn * (BN / 2);
-          nb1 = args.b_second + tn * (BN / 2);
-        } else {
-          nb0 = tn * BN;
-          nb1 = tn * BN + BN / 2;
-        }
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++g) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, args.status, DEV_GEMM_PRODUCER)) {
             *abort_flag = 1;
             break;
           }
           uint8_t* a_dst = smem + stage * C::STAGE_BYTES;
           uint8_t* b_dst = a_dst + C::A_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, &full_bar[stage], kb * BK, m0);
-          tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
-          tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
+          if (g < n_pre) {                          // weights already on their way
+            if (EPI == EPI_PARTS) {
+              tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
+              tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
+            } else {
+              tma_load_2d(a_dst, &tmA, &full_bar[stage], kb * BK, m0);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+            tma_load_2d(a_dst, &tmA, &full_bar[stage], kb * BK, m0);
+            tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
+            tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
