@@ -172,6 +172,7 @@ class Oracle:
         self.mode_bound = None
         self.cache = {}            # (layer, slice) -> _Cache
         self.written = {}          # (layer, slice) -> list of positions
+        self.window_slack = 0      # extra window positions kept (speculative verification)
 
     def _slice(self, layer, loop, mode):
         if loop is not None and mode == PER_LOOP:
@@ -253,8 +254,9 @@ class Oracle:
         first = c.first
         if not self.shape.is_full(l):
             # keep the last W positions: a query at position t >= P0 + C sees
-            # keys j > t - W only, so older keys are never read again
-            drop = max(0, P0 + C - self.shape.window - first)
+            # keys j > t - W only, so older keys are never read again (unless
+            # the length is rolled back, for which window_slack keeps more)
+            drop = max(0, P0 + C - self.shape.window - self.window_slack - first)
             k, v, first = k[:, :, drop:], v[:, :, drop:], first + drop
         self.cache[(l, sl)] = _Cache(k, v, first)
         self.written.setdefault((l, sl), set()).update(range(P0, P0 + C))
@@ -281,9 +283,12 @@ class Oracle:
             self.written[(l, sl)] = set(range(first, length))
 
     # --------------------------------------------------------------- forward
-    def step(self, tokens: np.ndarray, k: int, mode: int):
+    def step(self, tokens: np.ndarray, k: int, mode: int, draft: bool = False):
         """Process tokens [B, C] at positions length .. length+C-1.
-        Returns the final hidden states [B, C, d] (input to the LM head)."""
+        Returns the final hidden states [B, C, d] (input to the LM head).
+        draft=True: a shallower drafting pass of self-speculative decoding
+        under per-loop caching (k at most the bound k; it reads and writes
+        the slices of loops 1..k only)."""
         sh = self.shape
         tokens = np.asarray(tokens)
         B, C = tokens.shape
@@ -293,12 +298,13 @@ class Oracle:
             self.batch = B
         elif B != self.batch:
             raise ValueError("batch size changed")
-        if mode == PER_LOOP and self.k_bound is not None and self.k_bound != k:
+        if mode == PER_LOOP and self.k_bound is not None and self.k_bound != k and not (
+                draft and k < self.k_bound):
             raise ValueError("per-loop caching needs the same k for every step")
         if self.mode_bound is not None and self.mode_bound != mode:
             raise ValueError("cache mode changed")
         self.mode_bound = mode
-        if mode == PER_LOOP:
+        if mode == PER_LOOP and not draft:
             self.k_bound = k
         pos = np.arange(self.length, self.length + C)
         h = l2n(self.w["embed_in"][tokens])
@@ -333,6 +339,52 @@ class Oracle:
         h = self.step(np.asarray(tokens).reshape(-1, 1), k, mode)[:, 0, :]
         z = self.logits(h)
         return {"hidden": h, "logits": z, "next": np.argmax(z, axis=-1).astype(np.int32)}
+
+    def speculative_step(self, token, k_draft: int, k_verify: int, gamma: int):
+        """One step of greedy self-speculative decoding (Self-Speculative
+        Decoding): the same weights draft gamma tokens autoregressively at
+        k_draft, then verify them in one forward pass at k_verify over the
+        last emitted token and the drafts; drafts are accepted while each
+        equals the verifier's greedy token at the position before it, and the
+        verifier's token at the first mismatch (or after the last draft) is
+        emitted too.  Per-loop caching: drafting reads and writes only the
+        slices of loops 1..k_draft, which the verifier shares; the verifier
+        rewrites every slice of the positions it processes.  The batch
+        advances by the smallest accepted count over its sequences plus one
+        (a sequence that accepted more would emit the same token there).
+        token: [B] the last emitted tokens (not yet in the cache).  Returns
+        emitted tokens [B, n] and n."""
+        if self.mode_bound != PER_LOOP or self.k_bound != k_verify or not (
+                1 <= k_draft <= k_verify) or gamma < 1:
+            raise ValueError("self-speculative decoding needs per-loop caching bound at k_verify")
+        token = np.asarray(token).reshape(-1)
+        L = self.length
+        # drafting may not change what the verifier sees at positions < L:
+        # keep the cache state and return to it before verifying (the
+        # verifier recomputes and stores every slice of the positions it
+        # processes; cached arrays are never modified in place)
+        saved = (dict(self.cache), {key: set(v) for key, v in self.written.items()})
+        drafts, cur = [], token
+        for _ in range(gamma):
+            h = self.step(cur.reshape(-1, 1), k_draft, PER_LOOP, draft=True)[:, 0]
+            cur = np.argmax(self.logits(h), axis=-1)
+            drafts.append(cur)
+        drafts = np.stack(drafts, axis=1)                                  # [B, gamma]
+        self.cache, self.written = saved
+        self.length = L
+        # the verifier stores positions L .. L + gamma; only L .. L + n - 1
+        # stay, so window layers must keep gamma + 1 more positions than a
+        # query at L + gamma + 1 would need
+        self.window_slack = gamma + 1
+        h = self.step(np.concatenate([token[:, None], drafts], axis=1), k_verify, PER_LOOP)
+        self.window_slack = 0
+        g = np.argmax(self.logits(h), axis=-1)                             # [B, gamma + 1]
+        match = drafts == g[:, :gamma]
+        accepted = np.where(match.all(axis=1), gamma, np.argmin(match, axis=1))
+        n = int(accepted.min()) + 1
+        out = np.concatenate([drafts[:, :n - 1], g[:, n - 1:n]], axis=1)
+        self.length = L + n
+        return out, n
 
     def stack_forward(self, tokens):
         """The same layers run once each as a plain (non-looped) stack,

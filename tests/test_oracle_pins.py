@@ -7,6 +7,7 @@ normalisations, gate, GQA, 3:1 interleave), Training with Loops (schedule,
 32 + 40k layer applications), Last-Loop KV Caching (cache policies, their
 coincidence at k = 1, memory growth), Long-Context Extension (RoPE bases).
 """
+import copy
 import math
 
 import numpy as np
@@ -561,3 +562,68 @@ def test_restore_replays_the_next_step(mode):
     assert np.array_equal(a.prefill(chunk, k, mode)["logits"], b.prefill(chunk, k, mode)["logits"])
     with pytest.raises(ValueError):
         b.restore(a.length + 1, mode, k, saved)
+
+
+def _greedy_decode(o, first, k, n, mode, draft=False):
+    out, cur = [], np.asarray(first)
+    for _ in range(n):
+        h = o.step(cur.reshape(-1, 1), k, mode, draft=draft)[:, 0]
+        cur = np.argmax(o.logits(h), axis=-1)
+        out.append(cur)
+    return np.stack(out, axis=1)
+
+
+@pytest.mark.parametrize("k_draft,gamma", [(1, 4), (2, 3), (1, 1)])
+def test_speculative_greedy_equals_plain_greedy_at_k_verify(k_draft, gamma):
+    """Self-Speculative Decoding: whatever the drafts, the emitted tokens are
+    those of plain greedy decoding at the verifier's loop count (the
+    verifier decides every emitted token), and the caches the step leaves
+    behind are those plain decoding of the emitted tokens leaves."""
+    sh, kv = synth.TINY_LOOPFULL, 4
+    w = synth.make_weights(sh)
+    prompt = synth.tokens(sh, 2, 21)
+    ref = oracle.Oracle(sh, w)
+    first = np.argmax(ref.prefill(prompt, kv, PER_LOOP)["logits"][:, -1], axis=-1)
+    spec = oracle.Oracle(sh, w)
+    spec.prefill(prompt, kv, PER_LOOP)
+    emitted, cur, counts = [], first, []
+    while sum(e.shape[1] for e in emitted) < 12:
+        # the count by brute force from copies of the state: greedy drafts at
+        # k_draft against greedy tokens at the verifier's depth
+        d = _greedy_decode(copy.deepcopy(spec), cur, k_draft, gamma, PER_LOOP, draft=True)
+        v = _greedy_decode(copy.deepcopy(spec), cur, kv, gamma + 1, PER_LOOP)
+        lead = np.cumprod(d == v[:, :gamma], axis=1).sum(axis=1)
+        out, n = spec.speculative_step(cur, k_draft, kv, gamma)
+        assert n == int(lead.min()) + 1 and out.shape == (2, n)
+        assert np.array_equal(out, v[:, :n])
+        emitted.append(out)
+        counts.append(n)
+        cur = out[:, -1]
+    assert max(counts) > 1                     # some drafts were accepted
+    emitted = np.concatenate(emitted, axis=1)
+    plain = _greedy_decode(ref, first, kv, emitted.shape[1], PER_LOOP)
+    assert np.array_equal(emitted, plain)
+    # the state after the steps continues exactly like plain decoding
+    assert spec.length == ref.length
+    np.testing.assert_allclose(spec.decode(emitted[:, -1], kv, PER_LOOP)["logits"],
+                               ref.decode(plain[:, -1], kv, PER_LOOP)["logits"], atol=1e-12)
+
+
+def test_speculative_draft_at_verify_depth_accepts_everything():
+    """With the drafter as deep as the verifier every draft is the verifier's
+    own greedy token, so all gamma drafts are accepted."""
+    sh = synth.TINY_LOOPFULL
+    w = synth.make_weights(sh)
+    o = oracle.Oracle(sh, w)
+    first = np.argmax(o.prefill(synth.tokens(sh, 2, 17), 2, PER_LOOP)["logits"][:, -1], axis=-1)
+    out, n = o.speculative_step(first, 2, 2, 5)
+    assert n == 6
+    assert len(set(out[1].tolist())) == 6     # six different tokens: no fixed point
+
+
+def test_speculative_step_needs_per_loop_caching():
+    sh = synth.TINY_LOOPFULL
+    o = oracle.Oracle(sh, synth.make_weights(sh))
+    o.prefill(synth.tokens(sh, 1, 5), 4, LAST_LOOP)
+    with pytest.raises(ValueError):
+        o.speculative_step(np.array([1]), 1, 4, 4)
