@@ -161,6 +161,42 @@ DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k,
 DORY_API int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                      float* logits, int32_t* next, void* stream);
 
+/* ---- self-speculative decoding ---------------------------------------- */
+
+/* One greedy self-speculative decoding step ("Dory1.0-4B: A Looped
+ * Normalized-GPT", Self-Speculative Decoding): the same weights draft gamma
+ * tokens, one decode step at a time at loop count k_draft, then verify them
+ * in one forward pass at k_verify over the last emitted token and the
+ * drafts; drafts are accepted while each equals the verifier's greedy token
+ * at the position before it, and the verifier's token after the last
+ * accepted draft is emitted as well.  The emitted tokens are those of plain
+ * greedy decoding at k_verify.
+ *   Per-loop caching bound with k_max == k_verify is required
+ * (DORY_EKMISMATCH otherwise): drafting reads and writes the slices of loops
+ * 1..k_draft, which the verifier shares, and the verifier rewrites every
+ * slice of the positions it processes.  The sliding-window ring slots that
+ * drafting and the rejected positions overwrite are saved and put back.
+ *   tokens: device int32 [B], the last emitted token of each sequence (not
+ * yet in the cache).  out: device int32 [B, gamma + 1]; row b receives the
+ * emitted tokens in its first *n_out entries (-1 after).  n_out: host; the
+ * same count for every sequence, 1 .. gamma + 1: the smallest accepted count
+ * of the batch plus one (a sequence that accepted more would emit the same
+ * token there).  The sequences' length grows by *n_out; the last emitted
+ * token is the next call's input.
+ *   scratch: device memory, 256-byte aligned, of at least
+ * dory_speculative_scratch_bytes(m, B, gamma) bytes (verifier logits, drafts,
+ * saved ring slots).  Requires 1 <= k_draft <= k_verify, 1 <= gamma <= 16,
+ * gamma + 1 <= max_chunk and length + gamma + 1 <= max_ctx.
+ *   Unlike the other compute calls this one synchronises `stream` once, to
+ * read the accepted count. */
+DORY_API int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft,
+                                   int k_verify, int gamma, void* scratch, size_t scratch_bytes,
+                                   int32_t* out, int* n_out, void* stream);
+
+/* Scratch bytes dory_speculative_step needs for B sequences and gamma drafts
+ * with the handle's current binding; 0 on bad arguments or before dory_bind. */
+DORY_API size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma);
+
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
 

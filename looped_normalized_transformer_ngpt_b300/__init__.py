@@ -85,6 +85,9 @@ _SIGS = {
     "dory_debug_kv_offset": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_I)]),
     "dory_debug_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "dory_debug_expire_wait": (_I, [_P, _I, _P]),
+    "dory_speculative_step": (_I, [_P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P,
+                                   ctypes.POINTER(_I), _P]),
+    "dory_speculative_scratch_bytes": (ctypes.c_size_t, [_P, _I, _I]),
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -234,6 +237,23 @@ class Model:
                                                           _ptr(logits), _ptr(next_tokens),
                                                           _stream_ptr(stream)))
         return logits, next_tokens
+
+    def speculative_step(self, tokens, k_draft, k_verify, gamma, stream=None):
+        """One greedy self-speculative step: tokens int32 device [B] (the last
+        emitted tokens).  Returns (emitted int32 device [B, n], n)."""
+        import torch
+        B = tokens.shape[0]
+        nb = int(lib().dory_speculative_scratch_bytes(self.handle, B, gamma))
+        if nb == 0:
+            raise DoryError("dory_speculative_scratch_bytes", DORY_EINVAL)
+        if getattr(self, "_spec_scratch", None) is None or self._spec_scratch.numel() < nb:
+            self._spec_scratch = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        out = torch.empty((B, gamma + 1), dtype=torch.int32, device=self.device)
+        n = ctypes.c_int()
+        _check("dory_speculative_step", lib().dory_speculative_step(
+            self.handle, _ptr(tokens), B, k_draft, k_verify, gamma, _ptr(self._spec_scratch), nb,
+            _ptr(out), ctypes.byref(n), _stream_ptr(stream)))
+        return out[:, :n.value], n.value
 
     def hidden(self, rows, stream=None):
         """Final hidden states (LM-head input) of the last chunk, [rows, d] fp32."""

@@ -1587,6 +1587,154 @@ int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_m
   return DORY_OK;
 }
 
+// ---------------------------------------------------------------- speculative
+}  // extern "C"
+
+namespace {
+constexpr int kSpecMaxGamma = 16;
+
+// Sliding-window blocks of the bound KV region (every slice): the ring slots
+// a speculative step overwrites and may have to put back.
+std::vector<SpecRing> spec_rings(const dory_model* m) {
+  std::vector<SpecRing> r;
+  const dory_config& c = m->cfg;
+  for (int l = 0; l < n_layers(c); ++l) {
+    if (layer_full(c, l)) continue;
+    for (int sl = 0; sl < mult_of(c, l, m->k_max, m->cache_mode); ++sl) {
+      SpecRing g{};
+      g.k_off = (long long)kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, sl, 0);
+      g.v_off = (long long)kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, sl, 1);
+      g.slots = slots_of(c, l, m->max_ctx);
+      r.push_back(g);
+    }
+  }
+  return r;
+}
+
+struct SpecScratch {
+  size_t logits, drafts, vin, g, n, table, backup, total;
+};
+
+SpecScratch spec_layout(const dory_model* m, int B, int gamma, size_t n_rings) {
+  const dory_config& c = m->cfg;
+  SpecScratch L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  L.logits = take((size_t)B * (gamma + 1) * c.vocab * 4);
+  L.drafts = take((size_t)gamma * B * 4);
+  L.vin = take((size_t)B * (gamma + 1) * 4);
+  L.g = take((size_t)B * (gamma + 1) * 4);
+  L.n = take(4);
+  L.table = take(n_rings * sizeof(SpecRing));
+  L.backup = take(n_rings * 2 * (size_t)B * c.n_kv * (gamma + 1) * c.head_dim * 2);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+extern "C" {
+
+size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma) {
+  if (!m || !m->bound || B <= 0 || gamma < 1 || gamma > kSpecMaxGamma) return 0;
+  return spec_layout(m, B, gamma, spec_rings(m).size()).total;
+}
+
+int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k_verify,
+                          int gamma, void* scratch, size_t scratch_bytes, int32_t* out, int* n_out,
+                          void* stream) {
+  if (!m || !tokens || !scratch || !out || !n_out) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (gamma < 1 || gamma > kSpecMaxGamma || k_draft < 1 || k_draft > k_verify) return DORY_EINVAL;
+  if (m->cache_mode != DORY_CACHE_PER_LOOP || k_verify != m->k_max) return DORY_EKMISMATCH;
+  if (reinterpret_cast<uintptr_t>(scratch) & 255) return DORY_EINVAL;
+  // the verifying pass is one chunk of gamma + 1 tokens per sequence
+  int rc = check_call(m, B, gamma + 1, k_verify, DORY_CACHE_PER_LOOP);
+  if (rc != DORY_OK) return rc;
+  if (gamma + 1 > m->max_chunk) return DORY_ECAPACITY;
+  const std::vector<SpecRing> rings = spec_rings(m);
+  const SpecScratch S = spec_layout(m, B, gamma, rings.size());
+  if (scratch_bytes < S.total) return DORY_ENOMEM;
+  const dory_config& c = m->cfg;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  float* logits = reinterpret_cast<float*>(sc + S.logits);
+  int32_t* drafts = reinterpret_cast<int32_t*>(sc + S.drafts);
+  int32_t* vin = reinterpret_cast<int32_t*>(sc + S.vin);
+  int32_t* g = reinterpret_cast<int32_t*>(sc + S.g);
+  int* n_dev = reinterpret_cast<int*>(sc + S.n);
+  SpecRing* table = reinterpret_cast<SpecRing*>(sc + S.table);
+  uint4* backup = reinterpret_cast<uint4*>(sc + S.backup);
+  const int L = m->len;
+  const int nr = (int)rings.size();
+  m->launches = 0;
+  m->batch = B;
+  auto ring_copy = [&](int dir, const int* i0) -> int {
+    if (nr == 0) return DORY_OK;
+    const long long chunks = (long long)nr * 2 * B * c.n_kv * (gamma + 1) * (c.head_dim / 8);
+    long long blocks = (chunks + 255) / 256;
+    if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+    return launch_k(spec_ring_copy_kernel, dim3((unsigned)blocks), dim3(256), 0, st, m->kv,
+                    (const SpecRing*)table, nr, B, c.n_kv, c.head_dim, L, gamma + 1, backup, dir,
+                    i0) == cudaSuccess
+               ? DORY_OK
+               : DORY_ECUDA;
+  };
+  if (nr > 0 &&
+      cudaMemcpyAsync(table, rings.data(), rings.size() * sizeof(SpecRing), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return DORY_ECUDA;
+  // the window-ring slots of positions L .. L + gamma, which drafting and
+  // verifying overwrite (slot p mod W held position p - W, still visible)
+  DORY_TRY(ring_copy(0, nullptr));
+  // drafts: gamma greedy decode steps at k_draft (per-loop slices 1..k_draft)
+  for (int i = 0; i < gamma; ++i) {
+    const int32_t* in = i == 0 ? tokens : drafts + (i - 1) * B;
+    DORY_TRY(run_step(m, in, 1, B, 1, k_draft, logits, 1, 0, 1, st, drafts + i * B));
+    if (!m->next_done) {
+      pb(m, DORY_K_ARGMAX, st);
+      DORY_TRY(pe(m, st,
+                  launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits, c.vocab,
+                           drafts + i * B) == cudaSuccess
+                      ? DORY_OK
+                      : DORY_ECUDA));
+    }
+  }
+  // back to the state before drafting; one verifying pass over the last
+  // emitted token and the drafts at k_verify, logits at every position
+  DORY_TRY(ring_copy(1, nullptr));
+  m->len = L;
+  DORY_TRY(launch_k(spec_gather_kernel, dim3(1), dim3(256), 0, st, tokens, (const int32_t*)drafts,
+                    B, gamma, vin) == cudaSuccess
+               ? DORY_OK
+               : DORY_ECUDA);
+  DORY_TRY(run_step(m, vin, gamma + 1, B, gamma + 1, k_verify, logits, gamma + 1, 0, gamma + 1,
+                    st));
+  pb(m, DORY_K_ARGMAX, st);
+  DORY_TRY(pe(m, st,
+              launch_k(argmax_kernel, dim3(B * (gamma + 1)), dim3(1024), 0, st,
+                       (const float*)logits, c.vocab, g) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA));
+  DORY_TRY(launch_k(spec_accept_kernel, dim3(1), dim3(256), 0, st, (const int32_t*)drafts,
+                    (const int32_t*)g, B, gamma, out, n_dev) == cudaSuccess
+               ? DORY_OK
+               : DORY_ECUDA);
+  // positions past the accepted ones go back to what the rings held
+  DORY_TRY(ring_copy(1, n_dev));
+  int n = 0;
+  if (cudaMemcpyAsync(&n, n_dev, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DORY_ECUDA;
+  if (n < 1 || n > gamma + 1) return DORY_EDEVICE;
+  m->len = L + n;
+  *n_out = n;
+  return DORY_OK;
+}
+
 int dory_length(const dory_t* m, int* out) {
   if (!m || !out) return DORY_EINVAL;
   *out = m->len;

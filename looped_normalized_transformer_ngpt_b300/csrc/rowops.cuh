@@ -433,4 +433,90 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V
   }
 }
 
+// ------------------------------------------------------------------------
+// Self-speculative decoding ("Dory1.0-4B: A Looped Normalized-GPT",
+// Self-Speculative Decoding): drafts at a shallow loop count, one verifying
+// forward pass at the deep one, greedy acceptance.
+
+// One sliding-window cache block of the KV region: byte offsets of its K and
+// V arrays ([max_batch][n_kv][slots][head_dim] bf16) and its ring size.
+struct SpecRing {
+  long long k_off, v_off;
+  int slots, pad;
+};
+
+// Ring slots of positions L .. L + n_pos - 1 of every window block, for B
+// sequences: dir 0 copies them from the KV region to `backup`, dir 1 back
+// for the positions L + i with i >= *i0 (i0 null: all of them).  One
+// 16-byte chunk per thread; rows are head_dim bf16.
+__global__ void spec_ring_copy_kernel(uint8_t* kv, const SpecRing* blocks, int n_blocks, int B,
+                                      int n_kv, int dh, int L, int n_pos, uint4* backup, int dir,
+                                      const int* i0) {
+  pdl_wait();
+  pdl_trigger();
+  const int cpr = dh / 8;                                        // 16-byte chunks per row
+  const long long rows = (long long)n_blocks * 2 * B * n_kv * n_pos;
+  const int first = i0 ? *i0 : 0;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < rows * cpr;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(t % cpr);
+    long long r = t / cpr;
+    const int i = (int)(r % n_pos);
+    r /= n_pos;
+    const int kvh = (int)(r % n_kv);
+    r /= n_kv;
+    const int b = (int)(r % B);
+    r /= B;
+    const int which = (int)(r % 2);
+    const int blk = (int)(r / 2);
+    const SpecRing g = blocks[blk];
+    uint4* row = reinterpret_cast<uint4*>(kv + (which ? g.v_off : g.k_off)) +
+                 (((long long)b * n_kv + kvh) * g.slots + (L + i) % g.slots) * cpr + c;
+    uint4* bk = backup + t;
+    if (dir == 0)
+      *bk = *row;
+    else if (i >= first)
+      *row = *bk;
+  }
+}
+
+// The verifying pass's tokens: [B, gamma + 1] = the last emitted token, then
+// the gamma drafts (drafts[j * B + b]).
+__global__ void spec_gather_kernel(const int32_t* tokens, const int32_t* drafts, int B, int gamma,
+                                   int32_t* vin) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = B * (gamma + 1);
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n; t += gridDim.x * blockDim.x) {
+    const int b = t / (gamma + 1), j = t % (gamma + 1);
+    vin[t] = j == 0 ? tokens[b] : drafts[(j - 1) * B + b];
+  }
+}
+
+// Greedy acceptance (one block): sequence b accepts a_b leading drafts, each
+// equal to the verifier's greedy token at the position before it (g[b][j]:
+// the verifier's token after position L + j).  The batch advances by
+// n = min_b a_b + 1: out[b][j] = drafts[j][b] for j < n - 1, g[b][n - 1] at
+// j = n - 1 (the verifier's token), -1 after; *n_out = n.
+__global__ void spec_accept_kernel(const int32_t* drafts, const int32_t* g, int B, int gamma,
+                                   int32_t* out, int* n_out) {
+  __shared__ int s_min;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) s_min = gamma;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int a = 0;
+    while (a < gamma && drafts[a * B + b] == g[b * (gamma + 1) + a]) ++a;
+    atomicMin(&s_min, a);
+  }
+  __syncthreads();
+  const int n = s_min + 1;
+  for (int t = threadIdx.x; t < B * (gamma + 1); t += blockDim.x) {
+    const int b = t / (gamma + 1), j = t % (gamma + 1);
+    out[t] = j < n - 1 ? drafts[j * B + b] : (j == n - 1 ? g[t] : -1);
+  }
+  if (threadIdx.x == 0) *n_out = n;
+}
+
 }  // namespace dory
