@@ -877,6 +877,51 @@ def run_workload_4b(args):
                         "teacher_forcing": "both modes decode the per-loop run's greedy tokens",
                         "per_step": steps,
                         "greedy_agreement": sum(x["greedy_agree"] for x in steps[1:]) / D})
+        elif args.workload == "spec4b":
+            # greedy self-speculative decoding (draft k = 1, verify k = 4,
+            # gamma = 4, per-loop caches) against plain greedy decoding at
+            # k = 4, both after a real prefill of the prompt
+            B, T, N, G = args.batch if args.batch != HEAD_B else 1, args.ctx or 4096, 32, 4
+            weights = synth.make_weights_torch(sh)
+            weights["layers"] = list(weights["layers"])
+            res = {}
+            for mode_name, kd in (("plain", 0), ("speculative", 1), ("speculative_draft_k4", 4)):
+                m = dory.Model(sh, weights, max_batch=B, max_ctx=ctx64(T + N + 2 * G + 8),
+                               max_chunk=min(T, 4096), k_max=4, cache_mode=dory.PER_LOOP)
+                tok = torch.tensor(synth.tokens(sh, B, T, seed=9), device="cuda")
+                lg = m.prefill(tok, 4)
+                cur = torch.argmax(lg, dim=-1).to(torch.int32)
+                torch.cuda.synchronize()
+                emitted, steps = 0, 0
+                t0 = time.perf_counter()
+                while emitted < N:
+                    if mode_name == "plain":
+                        _, cur = m.decode(cur, 4)
+                        n = 1
+                    else:
+                        out, n = m.speculative_step(cur, kd, 4, G)
+                        cur = out[:, -1].contiguous()
+                    emitted += n
+                    steps += 1
+                torch.cuda.synchronize()
+                dt = time.perf_counter() - t0
+                assert m.device_status() == 0
+                res[mode_name] = {"tokens_per_sequence": emitted, "steps": steps,
+                                  "ms_per_token": round(1e3 * dt / emitted, 3),
+                                  "tokens_s": round(B * emitted / dt, 1)}
+                m.close()
+                del m
+                torch.cuda.empty_cache()
+            out.update({"batch": B, "prompt": T, "draft_k": 1, "verify_k": 4, "gamma": G,
+                        "per_mode": res,
+                        "speedup": round(res["plain"]["ms_per_token"] /
+                                         res["speculative"]["ms_per_token"], 3),
+                        "speedup_draft_k4": round(res["plain"]["ms_per_token"] /
+                                                  res["speculative_draft_k4"]["ms_per_token"], 3),
+                        "note": "random weights: greedy tokens at k = 1 and k = 4 rarely agree, "
+                                "so few drafts are accepted; drafting at k = 4 accepts every "
+                                "draft and bounds what the step can gain; eager calls, "
+                                "host-timed"})
         elif args.workload == "prefill4b":
             T = 8192
             m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,
@@ -1186,7 +1231,8 @@ def main(argv=None):
     ap.add_argument("--decode-only", action="store_true",
                     help="4B-class profile target: skip the prefill")
     ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
-                                           "longctx4b", "longprefill4b", "divergence4b"],
+                                           "longctx4b", "longprefill4b", "divergence4b",
+                                           "spec4b"],
                     default="headline4b",
                     help="headline4b: the default benchmark line (4B-class prefill 1x8192 + "
                          "decode 64x32768); small: the small looped nGPT line; the others time "
