@@ -152,8 +152,8 @@ DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k,
  * device fp32 [B, vocab] or NULL; next: device int32 [B] greedy tokens or
  * NULL (requires logits).
  * Decode steps of up to 16 sequences run five kernels per layer application
- * (see dory_set_persistent_decode for the single-kernel alternative); larger
- * batches run the tensor-core projections with K split over the SMs.  With
+ * (weight-streaming projections, one attention kernel); larger batches run
+ * the tensor-core projections with K split over the SMs.  With
  * head_dim 128 and ring sizes that are multiples of 64 (max_ctx and window,
  * as given to dory_bind / dory_create) the attention streams the cached K/V
  * with TMA through a 4-stage ring; otherwise a cp.async kernel does (same
@@ -197,6 +197,20 @@ DORY_API int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int 
  * with the handle's current binding; 0 on bad arguments or before dory_bind. */
 DORY_API size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma);
 
+/* Prefix caching: copies the cached keys and values of positions 0 .. len-1
+ * of sequence src into each sequence dst[i] (host array of n_dst distinct
+ * indices other than src, all below max_batch; n_dst <= 256), for every
+ * layer and every slice of the bound cache mode, so that those sequences can
+ * continue from the same prompt without recomputing it (the serving setup
+ * of "Dory1.0-4B: A Looped Normalized-GPT", Last-Loop KV Caching, reuses
+ * cached prompt prefixes).  Full-layer
+ * slots 0 .. len-1 are copied, and window-layer rings as they stand (slot
+ * p mod ring size).  Asynchronous on `stream`; host state is not changed:
+ * declare the new length with dory_set_length(B, len) before continuing all
+ * B sequences together.  Requires len <= max_ctx (DORY_ECAPACITY). */
+DORY_API int dory_copy_prefix(dory_t* m, int src, const int* dst, int n_dst, int len,
+                              void* stream);
+
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
 
@@ -222,15 +236,6 @@ DORY_API const char* dory_strerror(int status);
  * naming the kernel and wait that expired.  The word is cleared. */
 DORY_API int dory_device_status(dory_t* m, int* out, void* stream);
 
-/* enable = 1: decode steps of up to 16 sequences (d <= 2048) run as ONE
- * persistent kernel after the RoPE table, launched cooperatively (one CTA
- * per SM, grid barriers between the dependent steps; every barrier wait is
- * bounded: an expired wait sets the device status word and abandons the
- * step, and dory_bind must be called again before further use).
- * enable = 0 (the default): five kernels per layer application.  Both give
- * the same results up to rounding order.  Host state only. */
-DORY_API int dory_set_persistent_decode(dory_t* m, int enable);
-
 /* Number of kernels the last dory_prefill / dory_decode_step launched. */
 DORY_API int dory_last_launch_count(const dory_t* m, int* out);
 
@@ -250,8 +255,7 @@ typedef enum {
     DORY_K_BOUNDARY = 9,    /* loop-boundary re-injection / normalisation */
     DORY_K_LM_HEAD = 10,    /* logits */
     DORY_K_ARGMAX = 11,     /* greedy token */
-    DORY_K_DECODE_STEP = 12,/* whole decode step as one persistent kernel */
-    DORY_K_COUNT = 13
+    DORY_K_COUNT = 12
 } dory_kernel_class;
 
 /* Starts recording a CUDA-event pair around each of the next max_launches

@@ -32,7 +32,7 @@ LAST_LOOP = 0
 PER_LOOP = 1
 
 KERNEL_CLASSES = ("embed", "rope", "qkvg_gemm", "attention", "kv_write", "o_gemm", "ngpt_update",
-                  "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax", "decode_step")
+                  "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax")
 
 
 class DoryConfig(ctypes.Structure):
@@ -78,7 +78,6 @@ _SIGS = {
     "dory_strerror": (ctypes.c_char_p, [_I]),
     "dory_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "dory_last_launch_count": (_I, [_P, ctypes.POINTER(_I)]),
-    "dory_set_persistent_decode": (_I, [_P, _I]),
     "dory_set_tc_attention": (_I, [_P, _I]),
     "dory_set_fused_ngpt": (_I, [_P, _I]),
     "dory_debug_hidden": (_I, [_P, _P, _I, _P]),
@@ -88,6 +87,7 @@ _SIGS = {
     "dory_speculative_step": (_I, [_P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P,
                                    ctypes.POINTER(_I), _P]),
     "dory_speculative_scratch_bytes": (ctypes.c_size_t, [_P, _I, _I]),
+    "dory_copy_prefix": (_I, [_P, _I, ctypes.POINTER(_I), _I, _I, _P]),
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -238,6 +238,13 @@ class Model:
                                                           _stream_ptr(stream)))
         return logits, next_tokens
 
+    def copy_prefix(self, src, dst, length, stream=None):
+        """Copy the cached positions 0 .. length-1 of sequence src into the
+        sequences listed in dst (prefix caching); then set_length()."""
+        arr = (ctypes.c_int * len(dst))(*dst)
+        _check("dory_copy_prefix", lib().dory_copy_prefix(self.handle, src, arr, len(dst), length,
+                                                          _stream_ptr(stream)))
+
     def speculative_step(self, tokens, k_draft, k_verify, gamma, stream=None):
         """One greedy self-speculative step: tokens int32 device [B] (the last
         emitted tokens).  Returns (emitted int32 device [B, n], n)."""
@@ -300,12 +307,6 @@ class Model:
         after limit_us and sets the device status word (code 0x71)."""
         _check("dory_debug_expire_wait", lib().dory_debug_expire_wait(self.handle, limit_us,
                                                                       _stream_ptr(stream)))
-
-    def set_persistent_decode(self, enable: bool):
-        """Decode steps of <= 16 sequences as one persistent kernel (default)
-        or one kernel per step of the layer."""
-        _check("dory_set_persistent_decode",
-               lib().dory_set_persistent_decode(self.handle, 1 if enable else 0))
 
     def set_tc_attention(self, enable: bool):
         """Prefill attention on tcgen05 where its tile rules hold (default)

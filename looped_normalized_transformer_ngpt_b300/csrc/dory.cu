@@ -31,8 +31,8 @@
 #include "attn_dec.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "gemv_tma.cuh"
 #include "rowops.cuh"
-#include "decode_mk.cuh"
 
 using namespace dory;
 
@@ -46,7 +46,7 @@ constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 struct WsLayout {
   size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, ropet_swa,
       ropet_full, gy, dec_o,
-      dec_ml, dec_cnt, parts, mk_tab, mk_bar, total;
+      dec_ml, dec_cnt, parts, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -85,9 +85,6 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.dec_o = take((size_t)max_batch * c.n_q * kDecMaxSplits * c.head_dim * 4);
   L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
   L.dec_cnt = take((size_t)max_batch * c.n_kv * 4);   // split tickets, zero between launches
-  // persistent decode kernel: per-layer table, grid-barrier words + abort flag
-  L.mk_tab = take((size_t)(c.n_in + c.n_rec + c.n_out) * sizeof(MkLayer));
-  L.mk_bar = take(4 * sizeof(unsigned));
   // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
   if (max_batch > kGemvMaxM) {
     const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
@@ -372,7 +369,46 @@ cudaError_t gemv_j(const GemvArgs& a, int J, int grid, cudaStream_t st) {
   return gemv_go<MM, 8, false, PRE>(a, grid, st);
 }
 
-int launch_gemv(GemvArgs a, cudaStream_t st) {
+// One-row projection of a large matrix with the weights streamed by bulk
+// copies (gemv_tma.cuh): one CTA per SM, each owning a contiguous range of
+// features.  Returns DORY_EUNSUPPORTED outside the case where it measured
+// faster (one activation row, >= 8 MB of weights) or its limits (a
+// feature's rows above one 16 KB stage, unaligned weights).
+#ifndef DORY_GEMV_TMA
+#define DORY_GEMV_TMA 1
+#endif
+template <int MM, bool SW, bool PRE>
+int gemv_tma_go(const GemvArgs& a, int* status, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemv_tma_kernel<MM, SW, PRE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGvtSmem) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  const int grid = a.N < num_sms() ? a.N : num_sms();
+  return launch_k(gemv_tma_kernel<MM, SW, PRE>, dim3(grid), dim3(kGvtThreads), (size_t)kGvtSmem, st,
+                  a, status) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
+int launch_gemv_tma(const GemvArgs& a, int* status, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr;
+  const bool pre = a.h_in != nullptr;
+  const long long wbytes = (long long)(sw ? 2 : 1) * a.N * a.K * 2;
+  if (!DORY_GEMV_TMA || a.M != 1 || wbytes < (8ll << 20) || a.N <= 0 || a.K % 8 ||
+      (sw ? 2 : 1) * a.K * 2 > kGvtStageMax || (reinterpret_cast<uintptr_t>(a.W) & 15) ||
+      (pre && a.K > kGemvPreMaxD) || (!pre && (reinterpret_cast<uintptr_t>(a.X) & 15 || a.ldx % 8)))
+    return DORY_EUNSUPPORTED;
+  if (gvt_geom(a.M, a.K, sw, pre).stages < 2) return DORY_EUNSUPPORTED;
+  return sw ? (pre ? gemv_tma_go<1, true, true>(a, status, st) : gemv_tma_go<1, true, false>(a, status, st))
+            : (pre ? gemv_tma_go<1, false, true>(a, status, st) : gemv_tma_go<1, false, false>(a, status, st));
+}
+
+int launch_gemv(GemvArgs a, cudaStream_t st, int* status = nullptr) {
+  const int rt = launch_gemv_tma(a, status, st);
+  if (rt != DORY_EUNSUPPORTED) return rt;
   const bool sw = a.m_out != nullptr;
   const bool pre = a.h_in != nullptr;
   const int jmax = sw ? 4 : 8;
@@ -587,39 +623,6 @@ int dec_attn(const DecAttnArgs& a, int B, int head_dim, cudaStream_t st) {
   return DORY_EUNSUPPORTED;
 }
 
-// Persistent decode-step kernel (see decode_mk.cuh): cooperative launch of
-// one CTA per SM.  Returns DORY_EUNSUPPORTED when the kernel cannot be
-// co-resident on every SM (the caller then runs the per-kernel path).
-template <int MM, int DH>
-int launch_mk(const MkArgs& a, cudaStream_t st) {
-  constexpr int smem = MkAttnCfg<DH>::SMEM > kGemvMaxM * kMkMaxD * 2 ? MkAttnCfg<DH>::SMEM
-                                                                      : kGemvMaxM * kMkMaxD * 2;
-  static int ok = -1;
-  if (ok < 0) {
-    int per_sm = 0;
-    ok = cudaFuncSetAttribute(decode_step_kernel<MM, DH>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
-                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<MM, DH>,
-                                                               kMkThreads, smem) == cudaSuccess &&
-                 per_sm >= 1
-             ? 1
-             : 0;
-  }
-  if (!ok) return DORY_EUNSUPPORTED;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
-  cfg.blockDim = dim3(kMkThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_step_kernel<MM, DH>, a) == cudaSuccess ? DORY_OK
-                                                                                : DORY_ECUDA;
-}
-
 // Split-KV decode attention: partial kernel + combine.
 template <int DH>
 int launch_decode_attn(DecodeArgs a, int B, const __nv_bfloat16* gate, __nv_bfloat16* out,
@@ -665,7 +668,6 @@ struct dory_model {
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
   int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
-  bool use_mk = false; // decode steps of <= kGemvMaxM sequences as one persistent kernel
   bool use_tc_attn = true;  // prefill attention on tcgen05 where its tile rules hold
   bool use_ngpt_fused = true;   // nGPT step in the prefill O / down GEMM epilogues
   bool next_done = false;  // the last step also wrote the greedy tokens
@@ -796,7 +798,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gq.ldy = nqkvg;
   with_pending(gq);
   pb(m, DORY_K_QKVG_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemv(gq, st)));
+  DORY_TRY(pe(m, st, launch_gemv(gq, st, wsp<int>(m, m->L.status))));
 
   // attention over the cached keys + the new token, KV write fused
   DecAttnArgs da{};
@@ -835,7 +837,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   go.Y = y32;
   go.ldy = c.d;
   pb(m, DORY_K_O_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemv(go, st)));
+  DORY_TRY(pe(m, st, launch_gemv(go, st, wsp<int>(m, m->L.status))));
   s.pend = w.alpha_attn;
   if (!fuse) DORY_TRY(flush_pending(m, s, M, st));
 
@@ -850,7 +852,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gu.ldm = c.ffn;
   with_pending(gu);
   pb(m, DORY_K_UPGATE_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemv(gu, st)));
+  DORY_TRY(pe(m, st, launch_gemv(gu, st, wsp<int>(m, m->L.status))));
 
   // down projection; its nGPT step is owed
   GemvArgs gd{};
@@ -863,7 +865,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gd.Y = y32;
   gd.ldy = c.d;
   pb(m, DORY_K_DOWN_GEMM, st);
-  DORY_TRY(pe(m, st, launch_gemv(gd, st)));
+  DORY_TRY(pe(m, st, launch_gemv(gd, st, wsp<int>(m, m->L.status))));
   s.pend = w.alpha_mlp;
   return DORY_OK;
 }
@@ -1020,7 +1022,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.Y = gy;
     g.ldy = ga.N;
     pb(m, DORY_K_QKVG_GEMM, st);
-    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+    DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
     pb(m, DORY_K_QKVG_GEMM, st);
     const int nheads = 2 * c.n_q + 2 * c.n_kv;
     const int thr = c.head_dim / 2 > 32 ? c.head_dim / 2 : 32;
@@ -1124,7 +1126,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.K = hq;
     g.Y = go.out;
     g.ldy = c.d;
-    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+    DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else if (m->use_ngpt_fused) {
     // nGPT step fused into the GEMM epilogue (cluster over the d columns)
     EpiMaps eh = em;
@@ -1164,7 +1166,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.pair_off = c.ffn;
     g.m_out = gu.m_out;
     g.ldm = c.ffn;
-    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+    DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else {
     EpiMaps emm = em;                              // m is written through its load map
     emm.out = tm_m;
@@ -1189,7 +1191,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.K = c.ffn;
     g.Y = gd.out;
     g.ldy = c.d;
-    DORY_TRY(pe(m, st, launch_gemv(g, st)));
+    DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else if (m->use_ngpt_fused) {
     EpiMaps eh = em;
     eh.hb = tm_hb;
@@ -1266,62 +1268,6 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
                     ? DORY_OK
                     : DORY_ECUDA));
   }
-  if (decode && m->use_mk && c.d <= kMkMaxD) {
-    // one persistent kernel for the whole step (embedding .. greedy token)
-    MkArgs a{};
-    a.layers = wsp<MkLayer>(m, m->L.mk_tab);
-    a.n_in = c.n_in;
-    a.n_rec = c.n_rec;
-    a.n_out = c.n_out;
-    a.d = c.d;
-    a.n_q = c.n_q;
-    a.n_kv = c.n_kv;
-    a.ffn = c.ffn;
-    a.vocab = c.vocab;
-    a.window = c.window;
-    a.B = B;
-    a.P0 = P0;
-    a.k = k;
-    a.per_loop = m->cache_mode == DORY_CACHE_PER_LOOP ? 1 : 0;
-    a.scale_log2 = attn_scale_log2(c);
-    a.tokens = tokens;
-    a.embed_in = static_cast<const __nv_bfloat16*>(m->embed_in);
-    a.embed_out = static_cast<const __nv_bfloat16*>(m->embed_out);
-    a.s_z = m->s_z;
-    a.logits = n_logit_rows > 0 ? logits : nullptr;
-    a.next = a.logits ? next_tok : nullptr;
-    a.h0 = wsp<float>(m, m->L.h32);
-    a.h1 = wsp<float>(m, m->L.h32b);
-    a.x32 = wsp<float>(m, m->L.x32);
-    a.hb = wsp<__nv_bfloat16>(m, m->L.hb);
-    a.y32 = wsp<float>(m, m->L.y32);
-    a.gy = wsp<float>(m, m->L.gy);
-    a.att = wsp<__nv_bfloat16>(m, m->L.att);
-    a.mo = wsp<__nv_bfloat16>(m, m->L.m);
-    a.rope_swa = c.rope ? wsp<float2>(m, m->L.rope_swa) : nullptr;
-    a.rope_full = c.rope ? wsp<float2>(m, m->L.rope_full) : nullptr;
-    a.part_o = wsp<float>(m, m->L.dec_o);
-    a.part_ml = wsp<float>(m, m->L.dec_ml);
-    a.counter = wsp<int>(m, m->L.dec_cnt);
-    unsigned* bar = wsp<unsigned>(m, m->L.mk_bar);
-    a.bar = bar;
-    a.abort_flag = reinterpret_cast<int*>(bar + 2);
-    a.status = status;
-    int rc = DORY_EUNSUPPORTED;
-    pb(m, DORY_K_DECODE_STEP, st);
-    if (c.head_dim == 128) rc = M <= 4 ? launch_mk<4, 128>(a, st) : launch_mk<16, 128>(a, st);
-    if (c.head_dim == 64) rc = M <= 4 ? launch_mk<4, 64>(a, st) : launch_mk<16, 64>(a, st);
-    if (c.head_dim == 32) rc = M <= 4 ? launch_mk<4, 32>(a, st) : launch_mk<16, 32>(a, st);
-    if (rc != DORY_EUNSUPPORTED) {
-      DORY_TRY(pe(m, st, rc));
-      m->len += C;
-      m->last_rows = M;
-      m->hsel_last = 0;
-      m->next_done = a.next != nullptr;
-      return DORY_OK;
-    }
-    m->use_mk = false;                     // not co-resident here: per-kernel path
-  }
   StepState s;
   pb(m, DORY_K_EMBED, st);
   DORY_TRY(pe(m, st,
@@ -1373,7 +1319,7 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       g.ldy = (int)(ld_seq * c.vocab);
       g.col_scale = m->s_z;
       pb(m, DORY_K_LM_HEAD, st);
-      DORY_TRY(pe(m, st, launch_gemv(g, st)));
+      DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
     } else if (n_logit_rows == 1) {
       // one row per sequence: a strided view of hb (row stride C * d)
       CUtensorMap tm_last;
@@ -1503,31 +1449,10 @@ int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes, i
   m->batch = 0;
   m->last_rows = 0;
   m->hsel_last = 0;
-  // per-layer table of the persistent decode kernel
-  std::vector<MkLayer> tab(L);
-  for (int l = 0; l < L; ++l) {
-    const dory_layer_weights& w = m->layers[l];
-    MkLayer& t = tab[l];
-    t.w_qkvg = static_cast<const __nv_bfloat16*>(w.w_qkvg);
-    t.w_o = static_cast<const __nv_bfloat16*>(w.w_o);
-    t.w_upgate = static_cast<const __nv_bfloat16*>(w.w_upgate);
-    t.w_down = static_cast<const __nv_bfloat16*>(w.w_down);
-    t.alpha_attn = w.alpha_attn;
-    t.alpha_mlp = w.alpha_mlp;
-    t.s_qk = w.s_qk;
-    t.kv = reinterpret_cast<__nv_bfloat16*>(
-        m->kv + kv_offset(c, max_batch, max_ctx, k_max, cache_mode, l, 0, 0));
-    t.S = slots_of(c, l, max_ctx);
-    t.blk = (long long)t.S * c.n_kv * c.head_dim * max_batch;
-    t.full = layer_full(c, l) ? 1 : 0;
-  }
-  // status word, split tickets and barrier words start at zero (tickets and
-  // barrier arrivals return to zero after every launch that uses them)
-  if (cudaMemcpy(m->ws + m->L.mk_tab, tab.data(), tab.size() * sizeof(MkLayer),
-                 cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
+  // status word and split tickets start at zero (tickets return to zero
+  // after every launch that uses them)
+  if (cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
       cudaMemsetAsync(m->ws + m->L.dec_cnt, 0, (size_t)max_batch * c.n_kv * 4, 0) != cudaSuccess ||
-      cudaMemsetAsync(m->ws + m->L.mk_bar, 0, 4 * sizeof(unsigned), 0) != cudaSuccess ||
       cudaStreamSynchronize(0) != cudaSuccess)
     return DORY_ECUDA;
   return DORY_OK;
@@ -1735,6 +1660,43 @@ int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, 
   return DORY_OK;
 }
 
+int dory_copy_prefix(dory_t* m, int src, const int* dst, int n_dst, int len, void* stream) {
+  if (!m || !dst || n_dst <= 0 || n_dst > kKvCopyMaxDst || len <= 0) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (src < 0 || src >= m->max_batch) return DORY_EINVAL;
+  if (len > m->max_ctx) return DORY_ECAPACITY;
+  const dory_config& c = m->cfg;
+  KvCopyTable t;
+  t.n_dst = n_dst;
+  t.src = src;
+  t.max_batch = m->max_batch;
+  for (int i = 0; i < n_dst; ++i) {
+    if (dst[i] < 0 || dst[i] >= m->max_batch || dst[i] == src) return DORY_EINVAL;
+    t.dst[i] = dst[i];
+  }
+  int nb = 0, max_rows = 0;
+  for (int l = 0; l < n_layers(c); ++l) {
+    for (int sl = 0; sl < mult_of(c, l, m->k_max, m->cache_mode); ++sl) {
+      if (nb == kKvCopyMaxBlocks) return DORY_EUNSUPPORTED;
+      t.k_off[nb] = (long long)kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l,
+                                         sl, 0);
+      t.slots[nb] = slots_of(c, l, m->max_ctx);
+      // positions 0 .. len-1: slots 0 .. len-1 on full layers; on a window
+      // ring the whole ring once it has wrapped (slot p mod slots)
+      t.rows[nb] = len < t.slots[nb] ? len : t.slots[nb];
+      if (t.rows[nb] > max_rows) max_rows = t.rows[nb];
+      ++nb;
+    }
+  }
+  t.n_blocks = nb;
+  const long long chunks = 2ll * c.n_kv * max_rows * (c.head_dim / 8);
+  const dim3 grid((unsigned)((chunks + 255) / 256), (unsigned)nb, (unsigned)n_dst);
+  return launch_k(kv_copy_kernel, grid, dim3(256), 0, static_cast<cudaStream_t>(stream), m->kv, t,
+                  c.n_kv, c.head_dim) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
 int dory_length(const dory_t* m, int* out) {
   if (!m || !out) return DORY_EINVAL;
   *out = m->len;
@@ -1827,12 +1789,6 @@ int dory_device_status(dory_t* m, int* out, void* stream) {
     return DORY_ECUDA;
   if (cudaMemsetAsync(m->ws + m->L.status, 0, sizeof(int), st) != cudaSuccess) return DORY_ECUDA;
   *out = v;
-  return DORY_OK;
-}
-
-int dory_set_persistent_decode(dory_t* m, int enable) {
-  if (!m || (enable != 0 && enable != 1)) return DORY_EINVAL;
-  m->use_mk = enable != 0;
   return DORY_OK;
 }
 

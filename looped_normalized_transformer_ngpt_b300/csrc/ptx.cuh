@@ -24,6 +24,8 @@ enum : int {
   DEV_ATTN_ALIGN = 0x45,
   DEV_DEC_PRODUCER = 0x51,
   DEV_DEC_CONSUMER = 0x52,
+  DEV_GEMV_PRODUCER = 0x61,
+  DEV_GEMV_CONSUMER = 0x62,
   DEV_PROBE_WAIT = 0x71,   // the test-only kernel whose wait nobody completes
 };
 

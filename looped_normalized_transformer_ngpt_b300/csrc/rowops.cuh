@@ -519,4 +519,48 @@ __global__ void spec_accept_kernel(const int32_t* drafts, const int32_t* g, int 
   if (threadIdx.x == 0) *n_out = n;
 }
 
+// ------------------------------------------------------------------------
+// Prefix caching: the cached keys and values of one sequence copied into
+// other sequences of the same KV region.
+
+constexpr int kKvCopyMaxBlocks = 1024;   // (layer, slice) pairs
+constexpr int kKvCopyMaxDst = 256;
+
+// Byte offset of each (layer, slice) K block ([max_batch][n_kv][slots][dh]
+// bf16; the V block follows it), its ring size and the slots to copy.
+struct KvCopyTable {
+  int n_blocks, n_dst, src, max_batch;
+  long long k_off[kKvCopyMaxBlocks];
+  int slots[kKvCopyMaxBlocks];
+  int rows[kKvCopyMaxBlocks];
+  int dst[kKvCopyMaxDst];
+};
+
+// grid: x over (K/V, kv head, slot row, 16-byte chunk) of the largest block,
+// y = block, z = destination.  Slots 0 .. rows-1 of the source sequence go to
+// the same slots of the destination.
+__global__ void kv_copy_kernel(uint8_t* kv, const __grid_constant__ KvCopyTable t, int n_kv,
+                               int dh) {
+  pdl_wait();
+  pdl_trigger();
+  const int blk = blockIdx.y, d = blockIdx.z;
+  const int cpr = dh / 8;
+  const int rows = t.rows[blk], slots = t.slots[blk];
+  const long long total = 2ll * n_kv * rows * cpr;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int c = (int)(i % cpr);
+  long long r = i / cpr;
+  const int row = (int)(r % rows);
+  r /= rows;
+  const int kvh = (int)(r % n_kv);
+  const int which = (int)(r / n_kv);
+  const long long blk_bytes = (long long)t.max_batch * n_kv * slots * dh * 2;
+  const uint4* base = reinterpret_cast<const uint4*>(kv + t.k_off[blk] + which * blk_bytes);
+  uint4* dbase = reinterpret_cast<uint4*>(kv + t.k_off[blk] + which * blk_bytes);
+  const long long src = (((long long)t.src * n_kv + kvh) * slots + row) * cpr + c;
+  const long long dst = (((long long)t.dst[d] * n_kv + kvh) * slots + row) * cpr + c;
+  dbase[dst] = base[src];
+}
+
 }  // namespace dory

@@ -158,8 +158,6 @@ def test_path_switches_validate_arguments(L):
         assert L.dory_set_fused_ngpt(h, 1) == dory.DORY_OK
         assert L.dory_set_tc_attention(h, 3) == dory.DORY_EINVAL
         assert L.dory_set_tc_attention(h, 0) == dory.DORY_OK
-        assert L.dory_set_persistent_decode(h, -1) == dory.DORY_EINVAL
-        assert L.dory_set_persistent_decode(h, 0) == dory.DORY_OK
     finally:
         assert L.dory_destroy(h) == dory.DORY_OK
 

@@ -105,3 +105,27 @@ def test_4b_width_chunked_prefill_then_decode(dev, weights, mode):
         check_greedy(nxt.cpu().numpy(), r["logits"])
     assert m.device_status() == 0
     m.close()
+
+
+@pytest.mark.parametrize("B", [5, 16])
+def test_4b_width_few_row_decode(dev, weights, model_last, B):
+    """Decode batches of 5..16 sequences take the few-row projections (bulk-copy
+    weight streaming, activation rows held for up to 16 sequences): the
+    4B-width model at k = 2, two decode steps after a short prefill, against
+    the oracle."""
+    k, T, D = 2, 24, 2
+    prompt = synth.tokens(SHAPE, B, T, seed=60 + B)
+    dec = synth.tokens(SHAPE, B, D, seed=70 + B)
+    m = model_last
+    m.reset()
+    o = oracle.Oracle(SHAPE, weights, dtype=np.float32)
+    r = o.prefill(prompt, k, oracle.LAST_LOOP)
+    lg = m.prefill(_tok(prompt), k)
+    check_logits(lg.cpu().numpy(), r["logits"][:, -1])
+    for s in range(D):
+        r = o.decode(dec[:, s], k, oracle.LAST_LOOP)
+        lg, nxt = m.decode(_tok(dec[:, s]), k)
+        check_logits(lg.cpu().numpy(), r["logits"])
+        check_hidden(m.hidden(B).cpu().numpy(), r["hidden"])
+        check_greedy(nxt.cpu().numpy(), r["logits"])
+    assert m.device_status() == 0

@@ -59,15 +59,13 @@ def _tok(t):
 @pytest.mark.parametrize("shape", [synth.TINY, synth.TINY_LOOPFULL], ids=lambda s: s.name)
 @pytest.mark.parametrize("k", [1, 2, 4])
 @pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
-@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "perkernel"])
-def test_tiny_prefill_then_decode(dev, shape, k, mode, persistent):
+def test_tiny_prefill_then_decode(dev, shape, k, mode):
     w = synth.make_weights(shape)
     B, T, D = 2, 64, 8
     prompt = synth.tokens(shape, B, T)
     dec = synth.tokens(shape, B, D, seed=1)
     o = oracle.Oracle(shape, w)
     m = dev.Model(shape, w, max_batch=B, max_ctx=T + D, max_chunk=T, k_max=k, cache_mode=mode)
-    m.set_persistent_decode(persistent)
     ref = o.prefill(prompt, k, mode, all_logits=True)
     lg = m.prefill(_tok(prompt), k, mode, all_logits=True)
     hid = m.hidden(B * T)

@@ -5,9 +5,8 @@
   (4 x 2048 tokens, one chunk, last-loop cache): the GPU processes the whole
   batch; sequences are independent, so two sampled sequences are checked
   against the float32 oracle run on those sequences alone, at every position.
-* Decode steps after a short prefill, through the persistent decode-step
-  kernel and through the per-kernel path: few-row GEMVs with split K
-  segments and the fused SwiGLU pair, and the split-key decode attention.
+* Decode steps after a short prefill: few-row GEMVs with split K segments
+  and the fused SwiGLU pair, and the split-key decode attention.
 Tolerances as in test_gpu_parity."""
 import numpy as np
 import pytest
@@ -55,9 +54,8 @@ def test_full_size_prefill_sampled_sequences(dev, weights, k):
 
 
 @pytest.mark.parametrize("k,mode", [(2, oracle.LAST_LOOP), (3, oracle.PER_LOOP)])
-@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "perkernel"])
 @pytest.mark.parametrize("max_ctx", [99, 128], ids=["ring99", "ring128"])
-def test_decode_steps(dev, weights, k, mode, persistent, max_ctx):
+def test_decode_steps(dev, weights, k, mode, max_ctx):
     """A cache capacity of 99 positions runs the cp.async decode attention; 128
     (a multiple of 64) the TMA-fed one that the benchmark times."""
     sh = synth.SMALL
@@ -66,7 +64,6 @@ def test_decode_steps(dev, weights, k, mode, persistent, max_ctx):
     dec = synth.tokens(sh, B, D, seed=8)
     o = oracle.Oracle(sh, weights, dtype=np.float32)
     m = dev.Model(sh, weights, max_batch=B, max_ctx=max_ctx, max_chunk=T, k_max=k, cache_mode=mode)
-    m.set_persistent_decode(persistent)
     r = o.prefill(prompt, k, mode)
     lg = m.prefill(_tok(prompt), k, mode)
     check_logits(lg.cpu().numpy(), r["logits"][:, -1])
