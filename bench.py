@@ -94,6 +94,19 @@ def layer_params(sh):
             "down": sh.d * sh.ffn}
 
 
+def quant_weight_bytes(sh, fmt):
+    """Bytes of all layers' projection weights in format fmt (0 bf16, 1
+    MXFP8: a byte per weight + a scale byte per 32, 2 NVFP4: half a byte per
+    weight + a scale byte per 16 + a 4-byte scale per row)."""
+    hq, hk = sh.n_q * sh.head_dim, sh.n_kv * sh.head_dim
+    mats = [(2 * hq + 2 * hk, sh.d), (sh.d, hq), (2 * sh.ffn, sh.d), (sh.d, sh.ffn)]
+    per = 0
+    for rows, K in mats:
+        n = rows * K
+        per += 2 * n if fmt == 0 else (n + n // 32 if fmt == 1 else n // 2 + n // 16 + 4 * rows)
+    return per * sh.n_layers
+
+
 def visible_keys(sh, layer, P0, C):
     """Sum over the C query positions P0..P0+C-1 of the number of visible
     keys (closed form: t + 1 keys at position t, at most the window)."""
@@ -928,6 +941,61 @@ def run_workload_4b(args):
                                 "so few drafts are accepted; drafting at k = 4 accepts every "
                                 "draft and bounds what the step can gain; eager calls, "
                                 "host-timed"})
+        elif args.workload == "quant4b":
+            # weight-only quantised decode: the same decode steps with bf16,
+            # MXFP8 and NVFP4 projection weights (last-loop cache, synthetic
+            # contents), B sequences at ctx positions, k = 1 and 4
+            cases = [(1, 8192), (4, 8192), (16, 8192), (1, 262144)]
+            D = 4
+            weights = synth.make_weights_torch(sh)
+            weights["layers"] = list(weights["layers"])     # used by three models
+            res = {}
+            for fmt_name, fmt in (("bf16", 0), ("mxfp8", 1), ("nvfp4", 2)):
+                m = dory.Model(sh, weights, max_batch=1, max_ctx=64, max_chunk=1, k_max=4)
+                qs = None
+                if fmt:
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                    m.quantize(fmt)
+                    torch.cuda.synchronize()
+                    qs = round(time.perf_counter() - t0, 3)
+                wb = quant_weight_bytes(sh, fmt)
+                r = {"quantize_s": qs, "projection_weight_GB": round(wb / 1e9, 3)}
+                for B, ctx in cases:
+                    m.bind(B, ctx, 1, 4)
+                    fill_cache_synthetic(m, sh)
+                    tok = torch.tensor(synth.tokens(sh, B, 1, seed=4)[:, 0], device="cuda")
+                    lg = torch.empty((B, sh.vocab), device="cuda")
+                    nxt = torch.empty((B,), dtype=torch.int32, device="cuda")
+                    for k in (1, 4):
+                        P0 = ctx - D
+
+                        def fn(k=k):
+                            m.set_length(B, P0)
+                            for _ in range(D):
+                                m.decode(tok, k, logits=lg, next_tokens=nxt, stream=st)
+                        ms = _graph_time(fn, st, warm=1, reps=3) / D
+                        by = decode_step_bytes(sh, B, k, P0 + D // 2)
+                        na = len(layer_apps(sh, k))
+                        w = by["weights"] - 2 * sum(layer_params(sh).values()) * na \
+                            + wb * na // sh.n_layers
+                        gbs = (w + by["kv"]) / (ms / 1e3) / 1e9
+                        r[f"B{B}_ctx{ctx}_k{k}"] = {
+                            "decode_tok_s": round(B / (ms / 1e3), 1), "ms_per_step": round(ms, 3),
+                            "bytes_per_step_GB": round((w + by["kv"]) / 1e9, 2),
+                            "achieved_GBs": round(gbs, 1),
+                            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+                    assert m.device_status() == 0
+                res[fmt_name] = r
+                m.close()
+                del m
+                torch.cuda.empty_cache()
+            speed = {f: {c: round(res["bf16"][c]["ms_per_step"] / v["ms_per_step"], 3)
+                         for c, v in res[f].items() if isinstance(v, dict)}
+                     for f in ("mxfp8", "nvfp4")}
+            out.update({"per_format": res, "speedup_vs_bf16": speed,
+                        "note": "few-row projections stream the packed codes; embeddings and the "
+                                "LM head stay bf16; CUDA graphs of 4 decode steps"})
         elif args.workload == "prefill4b":
             T = 8192
             m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,
@@ -1238,7 +1306,7 @@ def main(argv=None):
                     help="4B-class profile target: skip the prefill")
     ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
                                            "longctx4b", "longprefill4b", "divergence4b",
-                                           "spec4b"],
+                                           "spec4b", "quant4b"],
                     default="headline4b",
                     help="headline4b: the default benchmark line (4B-class prefill 1x8192 + "
                          "decode 64x32768); small: the small looped nGPT line; the others time "

@@ -211,6 +211,73 @@ DORY_API size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma
 DORY_API int dory_copy_prefix(dory_t* m, int src, const int* dst, int n_dst, int len,
                               void* stream);
 
+/* ------------------------------------------------------------------------
+ * Weight-only quantised decode ("Dory1.0-4B: A Looped Normalized-GPT",
+ * Quantization: post-training quantisation of every weight matrix except
+ * the token embeddings and the LM head, weights only; MXFP8 with maximum
+ * scaling, NVFP4 with each block's E4M3 scale chosen to minimise the block's
+ * squared error over all 126 positive finite E4M3 values).
+ *
+ * Formats of a row-major [rows, K] matrix (blocks run along K):
+ *   DORY_QUANT_MXFP8: codes [rows][K] E4M3 (sign in bit 7); scales
+ *     [rows][K/32] E8M0 (value 2^(s - 127)); weight = code * 2^(s - 127).
+ *     The block exponent is floor(log2 max|x|) - 8, clamped to [-127, 127]
+ *     (-127 for a block whose maximum is 0 or subnormal); elements round to
+ *     nearest even, saturating at 448.
+ *   DORY_QUANT_NVFP4: codes [rows][K/2] E2M1 (element 2i in the low nibble,
+ *     sign in bit 3 of a nibble); scales [rows][K/16] E4M3 block scales s;
+ *     row_scale [rows] fp32, the tensor's scale s_g = max|x| / 2688 (1 for
+ *     an all-zero tensor) on every row; weight = code * s * s_g.  The block
+ *     scale is the first candidate, in increasing order, with the smallest
+ *     float32 error sum over the block of (x - q*d)^2, d = s*s_g, q = E2M1
+ *     rounding (nearest even, at most 6) of x/d, each operation rounded in
+ *     float32, elements in order.
+ * ---------------------------------------------------------------------- */
+typedef enum { DORY_QUANT_NONE = 0, DORY_QUANT_MXFP8 = 1, DORY_QUANT_NVFP4 = 2 } dory_quant_format;
+
+/* Bytes of the codes and block scales of a rows x K matrix in format fmt
+ * (pure host function).  K must be a multiple of 32.  DORY_EINVAL for a bad
+ * format or size. */
+DORY_API int dory_quant_bytes(int fmt, int rows, int K, size_t* codes_bytes,
+                              size_t* scales_bytes);
+
+/* Quantises the bf16 matrix W [rows, K] (device, 16-byte aligned, K a
+ * multiple of 32) as ONE tensor: codes and scales (device, sizes from
+ * dory_quant_bytes; codes 16-byte aligned) and row_scale (device fp32
+ * [rows]; NVFP4: required, receives s_g on every row; MXFP8: may be NULL,
+ * else receives 1.0).  deq (device bf16 [rows, K], may be NULL, may equal
+ * W) receives the dequantised weights rounded to bf16 (exact for MXFP8).
+ * Asynchronous on `stream`.  Sub-tensors that share one packed matrix (the
+ * q, k, v and gate rows of w_qkvg; the up and SiLU-gate rows of w_upgate)
+ * are quantised by one call each, at their row offsets. */
+DORY_API int dory_quantize_matrix(int fmt, const void* W, int rows, int K, void* codes,
+                                  void* scales, float* row_scale, void* deq, void* stream);
+
+/* The quantised form of one projection matrix (device pointers, layout as
+ * above; row_scale may be NULL for MXFP8). */
+typedef struct {
+    const void* codes;
+    const void* scales;
+    const float* row_scale;
+} dory_qmatrix;
+
+typedef struct {
+    dory_qmatrix qkvg, o, upgate, down;   /* same rows and K as the bf16 matrices */
+} dory_qlayer;
+
+/* From now on, every layer projection computed with at most 4 rows (the
+ * decode steps of up to 4 sequences, prefill chunks of up to 4 rows)
+ * streams these quantised weights instead of the bf16 ones; projections of
+ * more rows keep reading the bf16 matrices (with 5 or more rows, decoding
+ * the codes once per row makes the projection compute-bound), which should
+ * then hold the dequantised values (dory_quantize_matrix's deq) so that
+ * every path computes with the same weights.  The LM head and the embeddings are never
+ * quantised.  layers: HOST array of n_layers entries (copied); fmt
+ * DORY_QUANT_NONE switches back to the bf16 weights (layers may be NULL).
+ * DORY_EINVAL for null pointers, misaligned codes (16 bytes) or NVFP4
+ * scales (2 bytes), or d, n_q*head_dim or ffn not multiples of 32. */
+DORY_API int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* layers);
+
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
 

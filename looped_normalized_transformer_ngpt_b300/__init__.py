@@ -31,6 +31,10 @@ DORY_EUNSUPPORTED = -8
 LAST_LOOP = 0
 PER_LOOP = 1
 
+QUANT_NONE = 0
+QUANT_MXFP8 = 1
+QUANT_NVFP4 = 2
+
 KERNEL_CLASSES = ("embed", "rope", "qkvg_gemm", "attention", "kv_write", "o_gemm", "ngpt_update",
                   "upgate_gemm", "down_gemm", "boundary", "lm_head", "argmax")
 
@@ -53,6 +57,16 @@ class DoryLayerWeights(ctypes.Structure):
 class DoryWeights(ctypes.Structure):
     _fields_ = [("embed_in", ctypes.c_void_p), ("embed_out", ctypes.c_void_p),
                 ("s_z", ctypes.c_void_p), ("layers", ctypes.POINTER(DoryLayerWeights))]
+
+
+class DoryQMatrix(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("row_scale", ctypes.c_void_p)]
+
+
+class DoryQLayer(ctypes.Structure):
+    _fields_ = [("qkvg", DoryQMatrix), ("o", DoryQMatrix), ("upgate", DoryQMatrix),
+                ("down", DoryQMatrix)]
 
 
 class DoryError(RuntimeError):
@@ -88,6 +102,10 @@ _SIGS = {
                                    ctypes.POINTER(_I), _P]),
     "dory_speculative_scratch_bytes": (ctypes.c_size_t, [_P, _I, _I]),
     "dory_copy_prefix": (_I, [_P, _I, ctypes.POINTER(_I), _I, _I, _P]),
+    "dory_quant_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t),
+                              ctypes.POINTER(ctypes.c_size_t)]),
+    "dory_quantize_matrix": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "dory_set_quantized_weights": (_I, [_P, _I, ctypes.POINTER(DoryQLayer)]),
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -146,6 +164,31 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def quant_bytes(fmt: int, rows: int, K: int):
+    """(codes bytes, block-scale bytes) of a rows x K matrix in format fmt."""
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("dory_quant_bytes", lib().dory_quant_bytes(fmt, rows, K, ctypes.byref(cb),
+                                                      ctypes.byref(sb)))
+    return cb.value, sb.value
+
+
+def quantize_matrix(fmt: int, W, codes=None, scales=None, row_scale=None, deq=None, stream=None):
+    """Quantises the bf16 device matrix W [rows, K] as one tensor
+    (dory_quantize_matrix); allocates the outputs that are not given.
+    Returns (codes uint8, scales uint8, row_scale fp32 [rows])."""
+    import torch
+    rows, K = W.shape
+    cb, sb = quant_bytes(fmt, rows, K)
+    dev = W.device
+    codes = torch.empty(cb, dtype=torch.uint8, device=dev) if codes is None else codes
+    scales = torch.empty(sb, dtype=torch.uint8, device=dev) if scales is None else scales
+    row_scale = torch.empty(rows, dtype=torch.float32, device=dev) if row_scale is None else row_scale
+    _check("dory_quantize_matrix",
+           lib().dory_quantize_matrix(fmt, _ptr(W), rows, K, _ptr(codes), _ptr(scales),
+                                      _ptr(row_scale), _ptr(deq), _stream_ptr(stream)))
+    return codes, scales, row_scale
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
@@ -168,7 +211,10 @@ class Model:
         L = lib()
 
         def bf(x):
-            return torch.as_tensor(x).to(self.device, torch.bfloat16).contiguous()
+            # always the model's own copy (quantize() rewrites it in place)
+            t = torch.as_tensor(x)
+            y = t.to(self.device, torch.bfloat16).contiguous()
+            return y.clone() if y.data_ptr() == t.data_ptr() else y
 
         def f32(x):
             return torch.as_tensor(x).to(self.device, torch.float32).contiguous()
@@ -237,6 +283,47 @@ class Model:
                                                           _ptr(logits), _ptr(next_tokens),
                                                           _stream_ptr(stream)))
         return logits, next_tokens
+
+    def quantize(self, fmt, stream=None):
+        """Weight-only quantisation of every projection matrix (not the
+        embeddings or the LM head), on the GPU: the few-row projections
+        (decode) then stream the packed codes and block scales, and the
+        model's bf16 matrices are overwritten with the dequantised values so
+        that the larger projections compute with the same weights.  Each of
+        W_q, W_k, W_v, W_g, W_o, W_up, W_sl, W_down is its own tensor (its
+        own NVFP4 scale).  fmt QUANT_NONE switches the decode projections
+        back to the bf16 matrices (which keep the dequantised values)."""
+        import torch
+        L = lib()
+        if fmt == QUANT_NONE:
+            _check("dory_set_quantized_weights", L.dory_set_quantized_weights(self.handle, 0, None))
+            self._q = None
+            return
+        sh = self.shape
+        hq, hk = sh.n_q * sh.head_dim, sh.n_kv * sh.head_dim
+        parts = {"qkvg": (hq, hk, hk, hq), "o": (sh.d,), "upg": (sh.ffn, sh.ffn), "down": (sh.d,)}
+        table = (DoryQLayer * sh.n_layers)()
+        keep = []
+        for l, t in enumerate(self._keep):
+            mats = {}
+            for name in ("qkvg", "o", "upg", "down"):
+                W = t[name]
+                rows, K = W.shape
+                cb, sb = quant_bytes(fmt, rows, K)
+                codes = torch.empty(cb, dtype=torch.uint8, device=self.device)
+                scales = torch.empty(sb, dtype=torch.uint8, device=self.device)
+                rs = torch.empty(rows, dtype=torch.float32, device=self.device)
+                r0 = 0
+                for nr in parts[name]:
+                    quantize_matrix(fmt, W[r0:r0 + nr], codes[r0 * cb // rows:(r0 + nr) * cb // rows],
+                                    scales[r0 * sb // rows:(r0 + nr) * sb // rows], rs[r0:r0 + nr],
+                                    deq=W[r0:r0 + nr], stream=stream)
+                    r0 += nr
+                mats[name] = DoryQMatrix(codes.data_ptr(), scales.data_ptr(), rs.data_ptr())
+                keep.append((codes, scales, rs))
+            table[l] = DoryQLayer(mats["qkvg"], mats["o"], mats["upg"], mats["down"])
+        _check("dory_set_quantized_weights", L.dory_set_quantized_weights(self.handle, fmt, table))
+        self._q = keep
 
     def copy_prefix(self, src, dst, length, stream=None):
         """Copy the cached positions 0 .. length-1 of sequence src into the

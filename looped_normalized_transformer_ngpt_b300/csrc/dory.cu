@@ -32,6 +32,7 @@
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
 #include "gemv_tma.cuh"
+#include "quant.cuh"
 #include "rowops.cuh"
 
 using namespace dory;
@@ -406,7 +407,126 @@ int launch_gemv_tma(const GemvArgs& a, int* status, cudaStream_t st) {
             : (pre ? gemv_tma_go<1, false, true>(a, status, st) : gemv_tma_go<1, false, false>(a, status, st));
 }
 
+// Projection of 1-4 rows with weight-only quantised weights (quant.cuh),
+// register form: the geometry of launch_gemv with 16 (MXFP8) or 32 (NVFP4)
+// weights per 16-byte chunk.  Used where the bulk-copy form does not apply
+// (scale rows that are not a multiple of 16 bytes).
+template <int FMT, int MM, int J, bool SW, bool PRE>
+cudaError_t gemv_q_go(const GemvArgs& a, int grid, cudaStream_t st) {
+  const size_t smem = (PRE || a.stage_x) ? (size_t)a.M * a.K * 2 : 0;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(gemv_q_kernel<FMT, MM, J, SW, PRE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemvStageMax) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_q_kernel<FMT, MM, J, SW, PRE>,
+                                                      kGemvThreads, kGemvStageMax) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+  }
+  const int cap = per_sm * num_sms();
+  return launch_k(gemv_q_kernel<FMT, MM, J, SW, PRE>, dim3(grid < cap ? grid : cap),
+                  dim3(kGemvThreads), smem, st, a);
+}
+
+template <int FMT, int MM, bool SW, bool PRE>
+cudaError_t gemv_q_j(const GemvArgs& a, int J, int grid, cudaStream_t st) {
+  if (J <= 2) return gemv_q_go<FMT, MM, 2, SW, PRE>(a, grid, st);
+  if (J <= 4) return gemv_q_go<FMT, MM, 4, SW, PRE>(a, grid, st);
+  if (SW) return cudaErrorInvalidValue;
+  if (J <= 6) return gemv_q_go<FMT, MM, 6, false, PRE>(a, grid, st);
+  return gemv_q_go<FMT, MM, 8, false, PRE>(a, grid, st);
+}
+
+template <int FMT>
+cudaError_t gemv_q_fmt(const GemvArgs& a, int J, int grid, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr, pre = a.h_in != nullptr;
+  return sw ? (pre ? gemv_q_j<FMT, 4, true, true>(a, J, grid, st)
+                   : gemv_q_j<FMT, 4, true, false>(a, J, grid, st))
+            : (pre ? gemv_q_j<FMT, 4, false, true>(a, J, grid, st)
+                   : gemv_q_j<FMT, 4, false, false>(a, J, grid, st));
+}
+
+int launch_gemv_q(GemvArgs a, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr;
+  const bool pre = a.h_in != nullptr;
+  const int E = a.qfmt == QF_MXFP8 ? 16 : 32;
+  const int jmax = sw ? 4 : 8;
+  const int kc = (a.K + 32 * E - 1) / (32 * E);   // chunk columns per row
+  int S = 1;
+  while ((kc + S - 1) / S > jmax && S < kGemvWarps) S *= 2;
+  const int J = (kc + S - 1) / S;
+  if (J > jmax || a.M > 4 || a.M <= 0 || a.K % 32 || !a.Wq || !a.Ws ||
+      (a.qfmt != QF_MXFP8 && a.qfmt != QF_NVFP4))
+    return DORY_EUNSUPPORTED;
+  if (pre && a.K > kGemvPreMaxD) return DORY_EUNSUPPORTED;
+  a.S = S;
+  const int fpi = kGemvWarps / S;
+  a.n_iters = (a.N + fpi - 1) / fpi;
+  a.stage_x = (!pre && (size_t)a.M * a.K * 2 <= (size_t)kGemvStageMax) ? 1 : 0;
+  const cudaError_t e = a.qfmt == QF_MXFP8 ? gemv_q_fmt<QF_MXFP8>(a, J, a.n_iters, st)
+                                           : gemv_q_fmt<QF_NVFP4>(a, J, a.n_iters, st);
+  return e == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
+// Projection of 1-4 rows with quantised weights, bulk-copy form (quant.cuh
+// gemv_tma_q_kernel): one CTA per SM, packed code and scale rows streamed by
+// cp.async.bulk.  Needs 16-byte multiples for the rows of codes and scales.
+template <int FMT, int MM, bool SW, bool PRE>
+int gemv_tma_q_go(const GemvArgs& a, int* status, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemv_tma_q_kernel<FMT, MM, SW, PRE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGvtSmem) != cudaSuccess)
+      return DORY_ECUDA;
+    attr = true;
+  }
+  const int grid = a.N < num_sms() ? a.N : num_sms();
+  return launch_k(gemv_tma_q_kernel<FMT, MM, SW, PRE>, dim3(grid), dim3(kGvtThreads),
+                  (size_t)kGvtSmem, st, a, status) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
+}
+
+template <int FMT, int MM>
+int gemv_tma_q_mm(const GemvArgs& a, int* status, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr, pre = a.h_in != nullptr;
+  return sw ? (pre ? gemv_tma_q_go<FMT, MM, true, true>(a, status, st)
+                   : gemv_tma_q_go<FMT, MM, true, false>(a, status, st))
+            : (pre ? gemv_tma_q_go<FMT, MM, false, true>(a, status, st)
+                   : gemv_tma_q_go<FMT, MM, false, false>(a, status, st));
+}
+
+int launch_gemv_tma_q(const GemvArgs& a, int* status, cudaStream_t st) {
+  const bool sw = a.m_out != nullptr;
+  const bool pre = a.h_in != nullptr;
+  if (a.M < 1 || a.M > 4 || a.N <= 0 || a.K % 32 || !a.Wq || !a.Ws ||
+      (a.qfmt != QF_MXFP8 && a.qfmt != QF_NVFP4))
+    return DORY_EUNSUPPORTED;
+  const int sb = a.qfmt == QF_MXFP8 ? a.K / 32 : a.K / 16;
+  if (sb % 16 || (reinterpret_cast<uintptr_t>(a.Wq) & 15) || (reinterpret_cast<uintptr_t>(a.Ws) & 15))
+    return DORY_EUNSUPPORTED;
+  if (pre && a.K > kGemvPreMaxD) return DORY_EUNSUPPORTED;
+  if (!pre && ((reinterpret_cast<uintptr_t>(a.X) & 15) || a.ldx % 8)) return DORY_EUNSUPPORTED;
+  if (gvq_geom(a.qfmt, a.M, a.K, sw, pre).stages < 2) return DORY_EUNSUPPORTED;
+  if (a.qfmt == QF_MXFP8)
+    return a.M == 1 ? gemv_tma_q_mm<QF_MXFP8, 1>(a, status, st)
+                    : gemv_tma_q_mm<QF_MXFP8, 4>(a, status, st);
+  return a.M == 1 ? gemv_tma_q_mm<QF_NVFP4, 1>(a, status, st)
+                  : gemv_tma_q_mm<QF_NVFP4, 4>(a, status, st);
+}
+
 int launch_gemv(GemvArgs a, cudaStream_t st, int* status = nullptr) {
+  if (a.qfmt) {
+    if (a.M <= 4) {
+      const int rq = launch_gemv_tma_q(a, status, st);
+      if (rq != DORY_EUNSUPPORTED) return rq;
+      return launch_gemv_q(a, st);
+    }
+    // 5-16 rows: decoding the codes for every row makes the projection
+    // compute-bound; the bf16 matrix holds the dequantised weights
+    a.qfmt = 0;
+  }
   const int rt = launch_gemv_tma(a, status, st);
   if (rt != DORY_EUNSUPPORTED) return rt;
   const bool sw = a.m_out != nullptr;
@@ -652,6 +772,8 @@ int launch_decode_attn(DecodeArgs a, int B, const __nv_bfloat16* gate, __nv_bflo
 struct dory_model {
   dory_config cfg;
   std::vector<dory_layer_weights> layers;
+  int qfmt = 0;                          // DORY_QUANT_* of the few-row projections
+  std::vector<dory_qlayer> qlayers;
   const void* embed_in = nullptr;
   const void* embed_out = nullptr;
   const float* s_z = nullptr;
@@ -678,6 +800,19 @@ struct dory_model {
   std::vector<cudaEvent_t> prof_ev;   // 2 per launch
   std::vector<int> prof_cls;
 };
+
+// Points a layer projection at the layer's quantised weights, if any
+// (which: 0 QKV+gate, 1 output, 2 up+gate, 3 down).
+void use_quant(const dory_model* m, int l, int which, GemvArgs& g) {
+  if (!m->qfmt) return;
+  const dory_qlayer& q = m->qlayers[l];
+  const dory_qmatrix& x = which == 0 ? q.qkvg : which == 1 ? q.o : which == 2 ? q.upgate : q.down;
+  g.qfmt = m->qfmt;
+  g.Wq = static_cast<const uint8_t*>(x.codes);
+  g.Ws = static_cast<const uint8_t*>(x.scales);
+  g.Wr = x.row_scale;
+}
+
 
 namespace {
 
@@ -797,6 +932,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gq.Y = gy;
   gq.ldy = nqkvg;
   with_pending(gq);
+  use_quant(m, l, 0, gq);
   pb(m, DORY_K_QKVG_GEMM, st);
   DORY_TRY(pe(m, st, launch_gemv(gq, st, wsp<int>(m, m->L.status))));
 
@@ -836,6 +972,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   go.K = hq;
   go.Y = y32;
   go.ldy = c.d;
+  use_quant(m, l, 1, go);
   pb(m, DORY_K_O_GEMM, st);
   DORY_TRY(pe(m, st, launch_gemv(go, st, wsp<int>(m, m->L.status))));
   s.pend = w.alpha_attn;
@@ -851,6 +988,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gu.m_out = mo;
   gu.ldm = c.ffn;
   with_pending(gu);
+  use_quant(m, l, 2, gu);
   pb(m, DORY_K_UPGATE_GEMM, st);
   DORY_TRY(pe(m, st, launch_gemv(gu, st, wsp<int>(m, m->L.status))));
 
@@ -864,6 +1002,7 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   gd.K = c.ffn;
   gd.Y = y32;
   gd.ldy = c.d;
+  use_quant(m, l, 3, gd);
   pb(m, DORY_K_DOWN_GEMM, st);
   DORY_TRY(pe(m, st, launch_gemv(gd, st, wsp<int>(m, m->L.status))));
   s.pend = w.alpha_mlp;
@@ -1021,6 +1160,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.K = c.d;
     g.Y = gy;
     g.ldy = ga.N;
+    use_quant(m, l, 0, g);
     pb(m, DORY_K_QKVG_GEMM, st);
     DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
     pb(m, DORY_K_QKVG_GEMM, st);
@@ -1126,6 +1266,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.K = hq;
     g.Y = go.out;
     g.ldy = c.d;
+    use_quant(m, l, 1, g);
     DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else if (m->use_ngpt_fused) {
     // nGPT step fused into the GEMM epilogue (cluster over the d columns)
@@ -1166,6 +1307,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.pair_off = c.ffn;
     g.m_out = gu.m_out;
     g.ldm = c.ffn;
+    use_quant(m, l, 2, g);
     DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else {
     EpiMaps emm = em;                              // m is written through its load map
@@ -1191,6 +1333,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     g.K = c.ffn;
     g.Y = gd.out;
     g.ldy = c.d;
+    use_quant(m, l, 3, g);
     DORY_TRY(pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status))));
   } else if (m->use_ngpt_fused) {
     EpiMaps eh = em;
@@ -1695,6 +1838,71 @@ int dory_copy_prefix(dory_t* m, int src, const int* dst, int n_dst, int len, voi
                   c.n_kv, c.head_dim) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
+}
+
+int dory_quant_bytes(int fmt, int rows, int K, size_t* codes_bytes, size_t* scales_bytes) {
+  if ((fmt != DORY_QUANT_MXFP8 && fmt != DORY_QUANT_NVFP4) || rows <= 0 || K <= 0 || K % 32 ||
+      !codes_bytes || !scales_bytes)
+    return DORY_EINVAL;
+  const size_t n = (size_t)rows * K;
+  *codes_bytes = fmt == DORY_QUANT_MXFP8 ? n : n / 2;
+  *scales_bytes = fmt == DORY_QUANT_MXFP8 ? n / 32 : n / 16;
+  return DORY_OK;
+}
+
+int dory_quantize_matrix(int fmt, const void* W, int rows, int K, void* codes, void* scales,
+                         float* row_scale, void* deq, void* stream) {
+  size_t cb = 0, sb = 0;
+  if (dory_quant_bytes(fmt, rows, K, &cb, &sb) != DORY_OK || !W || !codes || !scales)
+    return DORY_EINVAL;
+  if (fmt == DORY_QUANT_NVFP4 && !row_scale) return DORY_EINVAL;
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (!al(W, 16) || !al(codes, 16) || (deq && !al(deq, 16)) || (row_scale && !al(row_scale, 4)))
+    return DORY_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long n = (long long)rows * K;
+  const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(W);
+  __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(deq);
+  // plain launches: these kernels do not take part in programmatic
+  // dependent launch, so each waits for all earlier work on the stream
+  if (fmt == DORY_QUANT_MXFP8) {
+    const long long nb = n / 32;
+    quant_mxfp8_kernel<<<(unsigned)((nb + 127) / 128), 128, 0, st>>>(
+        w, nb, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), dq, row_scale, K);
+  } else {
+    const long long nb = n / 16;
+    if (cudaMemsetAsync(row_scale, 0, sizeof(float), st) != cudaSuccess) return DORY_ECUDA;
+    long long g = (n / 8 + 255) / 256;
+    if (g > 4ll * num_sms()) g = 4ll * num_sms();
+    quant_amax_kernel<<<(unsigned)g, 256, 0, st>>>(w, n, reinterpret_cast<unsigned*>(row_scale));
+    quant_gscale_kernel<<<1, 256, 0, st>>>(row_scale, rows);
+    quant_nvfp4_kernel<<<(unsigned)((nb + 127) / 128), 128, 0, st>>>(
+        w, nb, K, row_scale, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), dq);
+  }
+  return cudaGetLastError() == cudaSuccess ? DORY_OK : DORY_ECUDA;
+}
+
+int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* layers) {
+  if (!m) return DORY_EINVAL;
+  if (fmt == DORY_QUANT_NONE) {
+    m->qfmt = 0;
+    m->qlayers.clear();
+    return DORY_OK;
+  }
+  if ((fmt != DORY_QUANT_MXFP8 && fmt != DORY_QUANT_NVFP4) || !layers) return DORY_EINVAL;
+  const dory_config& c = m->cfg;
+  if (c.d % 32 || (c.n_q * c.head_dim) % 32 || c.ffn % 32) return DORY_EINVAL;
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  for (int l = 0; l < n_layers(c); ++l) {
+    const dory_qmatrix* q[4] = {&layers[l].qkvg, &layers[l].o, &layers[l].upgate, &layers[l].down};
+    for (const dory_qmatrix* x : q) {
+      if (!x->codes || !x->scales || !al(x->codes, 16)) return DORY_EINVAL;
+      if (fmt == DORY_QUANT_NVFP4 && (!x->row_scale || !al(x->scales, 2))) return DORY_EINVAL;
+    }
+  }
+  m->qlayers.assign(layers, layers + n_layers(c));
+  m->qfmt = fmt;
+  return DORY_OK;
 }
 
 int dory_length(const dory_t* m, int* out) {

@@ -55,6 +55,11 @@ struct GemvArgs {
   const float* alpha;
   float* h_out;             // written by CTA 0 (a different buffer from h_in)
   int stage_x;              // not PRE: copy X to shared memory first (M * K * 2 bytes)
+  // weight-only quantised weights (quant.cuh) instead of W when qfmt != 0
+  int qfmt;
+  const uint8_t* Wq;        // codes
+  const uint8_t* Ws;        // block scales
+  const float* Wr;          // per-row scales (may be null)
 };
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
