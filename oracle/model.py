@@ -41,6 +41,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from .sampling import sample_weights, softmax_t, speculative_accept
+
 LAST_LOOP = 0
 PER_LOOP = 1
 
@@ -385,6 +387,43 @@ class Oracle:
         out = np.concatenate([drafts[:, :n - 1], g[:, n - 1:n]], axis=1)
         self.length = L + n
         return out, n
+
+    def speculative_sample_step(self, token, k_draft: int, k_verify: int, gamma: int,
+                                temperature: float, u):
+        """One step of self-speculative decoding with rejection sampling
+        (Self-Speculative Decoding; the rule is written out in
+        oracle/sampling.py): gamma drafts drawn at k_draft from softmax(z / T),
+        one verifying pass at k_verify, each draft kept with probability
+        min(1, p / q), the first rejected position redrawn from the residual
+        max(0, p - q), a last token from the verifier when every draft is kept.
+        Cache handling as in speculative_step.  u [B, 2 gamma + 1]: uniforms,
+        columns 0 .. gamma - 1 draw the drafts, gamma .. 2 gamma - 1 decide
+        acceptance, 2 gamma draws the residual or last token.  Returns
+        (tokens [B, n], n, kept drafts per sequence [B])."""
+        if self.mode_bound != PER_LOOP or self.k_bound != k_verify or not (
+                1 <= k_draft <= k_verify) or gamma < 1 or temperature <= 0:
+            raise ValueError("self-speculative sampling needs per-loop caching bound at k_verify")
+        token = np.asarray(token).reshape(-1)
+        u = np.asarray(u, np.float64)
+        B, L = token.shape[0], self.length
+        saved = (dict(self.cache), {key: set(v) for key, v in self.written.items()})
+        drafts, qs, cur = [], [], token
+        for i in range(gamma):
+            h = self.step(cur.reshape(-1, 1), k_draft, PER_LOOP, draft=True)[:, 0]
+            q = softmax_t(self.logits(h), temperature)
+            cur = np.array([sample_weights(q[b], u[b, i]) for b in range(B)], np.int64)
+            drafts.append(cur)
+            qs.append(q)
+        drafts, q = np.stack(drafts, axis=1), np.stack(qs, axis=1)
+        self.cache, self.written = saved
+        self.length = L
+        self.window_slack = gamma + 1
+        h = self.step(np.concatenate([token[:, None], drafts], axis=1), k_verify, PER_LOOP)
+        self.window_slack = 0
+        p = softmax_t(self.logits(h), temperature)                         # [B, gamma + 1, V]
+        out, n, kept = speculative_accept(p, q, drafts, u[:, gamma:2 * gamma], u[:, 2 * gamma])
+        self.length = L + n
+        return out, n, kept
 
     def stack_forward(self, tokens):
         """The same layers run once each as a plain (non-looped) stack,
