@@ -898,28 +898,39 @@ def run_workload_4b(args):
             weights = synth.make_weights_torch(sh)
             weights["layers"] = list(weights["layers"])
             res = {}
-            for mode_name, kd in (("plain", 0), ("speculative", 1), ("speculative_draft_k4", 4)):
+            TEMP = 1.0
+            gen = torch.Generator(device="cuda").manual_seed(12)
+            modes = (("plain", 0, 0.0), ("speculative", 1, 0.0), ("speculative_draft_k4", 4, 0.0),
+                     ("plain_sampled", 0, TEMP), ("speculative_sampled", 1, TEMP),
+                     ("speculative_sampled_draft_k4", 4, TEMP))
+            for mode_name, kd, temp in modes:
                 m = dory.Model(sh, weights, max_batch=B, max_ctx=ctx64(T + N + 5 * (G + 1) + 8),
                                max_chunk=min(T, 4096), k_max=4, cache_mode=dory.PER_LOOP)
                 tok = torch.tensor(synth.tokens(sh, B, T, seed=9), device="cuda")
                 lg = m.prefill(tok, 4)
                 cur = torch.argmax(lg, dim=-1).to(torch.int32)
-                for _ in range(3):                   # untimed: first launches load kernels
-                    if mode_name == "plain":
-                        _, cur = m.decode(cur, 4)
+
+                def advance(cur):
+                    if kd == 0:
+                        lgd, nxt = m.decode(cur, 4)
+                        if temp > 0:
+                            u = torch.rand((B,), device="cuda", generator=gen)
+                            nxt = dory.sample_tokens(lgd, temp, u)
+                        return nxt, 1
+                    if temp > 0:
+                        u = torch.rand((B, 2 * G + 1), device="cuda", generator=gen)
+                        emit, n, _ = m.speculative_sample_step(cur, kd, 4, G, temp, u)
                     else:
-                        emit, _ = m.speculative_step(cur, kd, 4, G)
-                        cur = emit[:, -1].contiguous()
+                        emit, n = m.speculative_step(cur, kd, 4, G)
+                    return emit[:, -1].contiguous(), n
+
+                for _ in range(3):                   # untimed: first launches load kernels
+                    cur, _ = advance(cur)
                 torch.cuda.synchronize()
                 emitted, steps = 0, 0
                 t0 = time.perf_counter()
                 while emitted < N:
-                    if mode_name == "plain":
-                        _, cur = m.decode(cur, 4)
-                        n = 1
-                    else:
-                        emit, n = m.speculative_step(cur, kd, 4, G)
-                        cur = emit[:, -1].contiguous()
+                    cur, n = advance(cur)
                     emitted += n
                     steps += 1
                 torch.cuda.synchronize()
@@ -937,6 +948,12 @@ def run_workload_4b(args):
                                          res["speculative"]["ms_per_token"], 3),
                         "speedup_draft_k4": round(res["plain"]["ms_per_token"] /
                                                   res["speculative_draft_k4"]["ms_per_token"], 3),
+                        "temperature_sampled": TEMP,
+                        "speedup_sampled": round(res["plain_sampled"]["ms_per_token"] /
+                                                 res["speculative_sampled"]["ms_per_token"], 3),
+                        "speedup_sampled_draft_k4": round(
+                            res["plain_sampled"]["ms_per_token"] /
+                            res["speculative_sampled_draft_k4"]["ms_per_token"], 3),
                         "note": "random weights: greedy tokens at k = 1 and k = 4 rarely agree, "
                                 "so few drafts are accepted; drafting at k = 4 accepts every "
                                 "draft and bounds what the step can gain; eager calls, "

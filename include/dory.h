@@ -184,8 +184,8 @@ DORY_API int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, in
  * token there).  The sequences' length grows by *n_out; the last emitted
  * token is the next call's input.
  *   scratch: device memory, 256-byte aligned, of at least
- * dory_speculative_scratch_bytes(m, B, gamma) bytes (verifier logits, drafts,
- * saved ring slots).  Requires 1 <= k_draft <= k_verify, 1 <= gamma <= 16,
+ * dory_speculative_scratch_bytes(m, B, gamma) bytes (verifier and drafter
+ * logits, drafts, saved ring slots).  Requires 1 <= k_draft <= k_verify, 1 <= gamma <= 16,
  * gamma + 1 <= max_chunk and length + gamma + 1 <= max_ctx.
  *   Unlike the other compute calls this one synchronises `stream` once, to
  * read the accepted count. */
@@ -193,9 +193,49 @@ DORY_API int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int 
                                    int k_verify, int gamma, void* scratch, size_t scratch_bytes,
                                    int32_t* out, int* n_out, void* stream);
 
-/* Scratch bytes dory_speculative_step needs for B sequences and gamma drafts
- * with the handle's current binding; 0 on bad arguments or before dory_bind. */
+/* The same step with rejection sampling instead of greedy acceptance
+ * ("Dory1.0-4B: A Looped Normalized-GPT", Self-Speculative Decoding: the
+ * shallow loop count drafts, the full count verifies in one pass, and
+ * rejection sampling keeps the verifier's distribution).  Distributions are
+ * softmax(logits / temperature), temperature > 0.  A draw from weights w
+ * with uniform v is the smallest index whose running sum (vocabulary order)
+ * exceeds v * sum(w).  Draft i of sequence b is drawn with u[b][i] from the
+ * drafter's distribution q; it is kept iff u[b][gamma + i] * q(x) < p(x) (p:
+ * the verifier's distribution at that position), and only while every
+ * earlier draft was kept.  The batch advances by n = (fewest kept drafts) +
+ * 1; at the last emitted position a sequence emits its kept draft, else a
+ * draw with u[b][2 gamma] from max(0, p - q) (its first rejected position)
+ * or, when every draft was kept, from the verifier's distribution after the
+ * last draft.  Every emitted token then follows the verifier's conditional
+ * distribution.
+ *   u: device fp32 [B][2 gamma + 1] uniforms in [0, 1) (the caller's random
+ * numbers).  out, n_out, scratch, requirements and the synchronisation as
+ * for dory_speculative_step; kept (device int32 [B], may be NULL) receives
+ * each sequence's count of leading kept drafts.  DORY_EINVAL for u NULL or
+ * temperature <= 0. */
+DORY_API int dory_speculative_sample_step(dory_t* m, const int32_t* tokens, int B, int k_draft,
+                                          int k_verify, int gamma, float temperature,
+                                          const float* u, void* scratch, size_t scratch_bytes,
+                                          int32_t* out, int* n_out, int32_t* kept, void* stream);
+
+/* Scratch bytes dory_speculative_step and dory_speculative_sample_step need
+ * for B sequences and gamma drafts with the handle's current binding; 0 on
+ * bad arguments or before dory_bind. */
 DORY_API size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma);
+
+/* Test-only: byte offsets inside the speculative scratch of the verifier
+ * logits (fp32 [B][gamma + 1][V]), the drafter logits (fp32 [gamma][B][V],
+ * written by the sampled step) and the drafts (int32 [gamma][B]):
+ * offsets[0..2].  DORY_EINVAL on bad arguments or before dory_bind. */
+DORY_API int dory_debug_speculative_layout(const dory_t* m, int B, int gamma, size_t* offsets);
+
+/* One token per row of logits (device fp32 [rows][V]) drawn from
+ * softmax(logits / temperature) with the uniform u[row] (device fp32 [rows],
+ * in [0, 1)), by the rule of dory_speculative_sample_step; out: device int32
+ * [rows].  Asynchronous on `stream`.  DORY_EINVAL for null pointers,
+ * rows or V <= 0, temperature <= 0. */
+DORY_API int dory_sample_tokens(const float* logits, int rows, int V, float temperature,
+                                const float* u, int32_t* out, void* stream);
 
 /* Prefix caching: copies the cached keys and values of positions 0 .. len-1
  * of sequence src into each sequence dst[i] (host array of n_dst distinct

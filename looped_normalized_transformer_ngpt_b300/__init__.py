@@ -101,6 +101,10 @@ _SIGS = {
     "dory_speculative_step": (_I, [_P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P,
                                    ctypes.POINTER(_I), _P]),
     "dory_speculative_scratch_bytes": (ctypes.c_size_t, [_P, _I, _I]),
+    "dory_speculative_sample_step": (_I, [_P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                                          ctypes.c_size_t, _P, ctypes.POINTER(_I), _P, _P]),
+    "dory_sample_tokens": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "dory_debug_speculative_layout": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "dory_copy_prefix": (_I, [_P, _I, ctypes.POINTER(_I), _I, _I, _P]),
     "dory_quant_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                               ctypes.POINTER(ctypes.c_size_t)]),
@@ -187,6 +191,17 @@ def quantize_matrix(fmt: int, W, codes=None, scales=None, row_scale=None, deq=No
            lib().dory_quantize_matrix(fmt, _ptr(W), rows, K, _ptr(codes), _ptr(scales),
                                       _ptr(row_scale), _ptr(deq), _stream_ptr(stream)))
     return codes, scales, row_scale
+
+
+def sample_tokens(logits, temperature, u, out=None, stream=None):
+    """One token per row of fp32 device logits [rows, V] drawn from
+    softmax(logits / T) with the uniforms u (fp32 device [rows])."""
+    import torch
+    rows, V = logits.shape
+    out = torch.empty((rows,), dtype=torch.int32, device=logits.device) if out is None else out
+    _check("dory_sample_tokens", lib().dory_sample_tokens(_ptr(logits), rows, V, float(temperature),
+                                                          _ptr(u), _ptr(out), _stream_ptr(stream)))
+    return out
 
 
 def _ptr(t):
@@ -348,6 +363,27 @@ class Model:
             self.handle, _ptr(tokens), B, k_draft, k_verify, gamma, _ptr(self._spec_scratch), nb,
             _ptr(out), ctypes.byref(n), _stream_ptr(stream)))
         return out[:, :n.value], n.value
+
+    def speculative_sample_step(self, tokens, k_draft, k_verify, gamma, temperature, u,
+                                stream=None):
+        """One self-speculative step with rejection sampling: tokens int32
+        device [B]; u fp32 device [B, 2 gamma + 1] uniforms.  Returns
+        (emitted int32 device [B, n], n, kept drafts int32 device [B])."""
+        import torch
+        B = tokens.shape[0]
+        nb = int(lib().dory_speculative_scratch_bytes(self.handle, B, gamma))
+        if nb == 0:
+            raise DoryError("dory_speculative_scratch_bytes", DORY_EINVAL)
+        if getattr(self, "_spec_scratch", None) is None or self._spec_scratch.numel() < nb:
+            self._spec_scratch = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        out = torch.empty((B, gamma + 1), dtype=torch.int32, device=self.device)
+        kept = torch.empty((B,), dtype=torch.int32, device=self.device)
+        n = ctypes.c_int()
+        _check("dory_speculative_sample_step", lib().dory_speculative_sample_step(
+            self.handle, _ptr(tokens), B, k_draft, k_verify, gamma, float(temperature), _ptr(u),
+            _ptr(self._spec_scratch), nb, _ptr(out), ctypes.byref(n), _ptr(kept),
+            _stream_ptr(stream)))
+        return out[:, :n.value], n.value, kept
 
     def hidden(self, rows, stream=None):
         """Final hidden states (LM-head input) of the last chunk, [rows, d] fp32."""

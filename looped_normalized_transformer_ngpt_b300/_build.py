@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libdory.so")
 SOURCES = ["dory.cu"]
-HEADERS = ["ptx.cuh", "gemm_tc.cuh", "gemv.cuh", "gemv_tma.cuh", "quant.cuh", "attn.cuh", "rowops.cuh", "attn_tc.cuh", "attn_dec.cuh"]
+HEADERS = ["ptx.cuh", "gemm_tc.cuh", "gemv.cuh", "gemv_tma.cuh", "quant.cuh", "sample.cuh", "attn.cuh", "rowops.cuh", "attn_tc.cuh", "attn_dec.cuh"]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-lineinfo",

@@ -33,6 +33,7 @@
 #include "gemv.cuh"
 #include "gemv_tma.cuh"
 #include "quant.cuh"
+#include "sample.cuh"
 #include "rowops.cuh"
 
 using namespace dory;
@@ -1680,7 +1681,7 @@ std::vector<SpecRing> spec_rings(const dory_model* m) {
 }
 
 struct SpecScratch {
-  size_t logits, drafts, vin, g, n, table, backup, total;
+  size_t logits, drafts, vin, g, n, table, backup, dlogits, stats, kept, total;
 };
 
 SpecScratch spec_layout(const dory_model* m, int B, int gamma, size_t n_rings) {
@@ -1699,6 +1700,10 @@ SpecScratch spec_layout(const dory_model* m, int B, int gamma, size_t n_rings) {
   L.n = take(4);
   L.table = take(n_rings * sizeof(SpecRing));
   L.backup = take(n_rings * 2 * (size_t)B * c.n_kv * (gamma + 1) * c.head_dim * 2);
+  // sampling only: the drafter's logits, softmax statistics, kept counts
+  L.dlogits = take((size_t)gamma * B * c.vocab * 4);
+  L.stats = take((size_t)(2 * gamma + 1) * B * sizeof(float2));
+  L.kept = take((size_t)B * 4);
   L.total = off;
   return L;
 }
@@ -1711,9 +1716,14 @@ size_t dory_speculative_scratch_bytes(const dory_t* m, int B, int gamma) {
   return spec_layout(m, B, gamma, spec_rings(m).size()).total;
 }
 
-int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k_verify,
-                          int gamma, void* scratch, size_t scratch_bytes, int32_t* out, int* n_out,
-                          void* stream) {
+}  // extern "C"
+
+namespace {
+// Greedy (temperature 0, u null) or sampled self-speculative step.
+int speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k_verify,
+                     int gamma, float temperature, const float* u, void* scratch,
+                     size_t scratch_bytes, int32_t* out, int* n_out, int32_t* kept_out,
+                     void* stream) {
   if (!m || !tokens || !scratch || !out || !n_out) return DORY_EINVAL;
   if (!m->bound) return DORY_EUNBOUND;
   if (gamma < 1 || gamma > kSpecMaxGamma || k_draft < 1 || k_draft > k_verify) return DORY_EINVAL;
@@ -1736,6 +1746,11 @@ int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, 
   int* n_dev = reinterpret_cast<int*>(sc + S.n);
   SpecRing* table = reinterpret_cast<SpecRing*>(sc + S.table);
   uint4* backup = reinterpret_cast<uint4*>(sc + S.backup);
+  float* dlogits = reinterpret_cast<float*>(sc + S.dlogits);
+  float2* stats = reinterpret_cast<float2*>(sc + S.stats);
+  int32_t* kept = reinterpret_cast<int32_t*>(sc + S.kept);
+  const bool sampled = u != nullptr;
+  const float inv_t = sampled ? 1.0f / temperature : 0.0f;
   const int L = m->len;
   const int nr = (int)rings.size();
   m->launches = 0;
@@ -1758,9 +1773,19 @@ int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, 
   // the window-ring slots of positions L .. L + gamma, which drafting and
   // verifying overwrite (slot p mod W held position p - W, still visible)
   DORY_TRY(ring_copy(0, nullptr));
-  // drafts: gamma greedy decode steps at k_draft (per-loop slices 1..k_draft)
+  // drafts: gamma decode steps at k_draft (per-loop slices 1..k_draft),
+  // greedy or drawn from softmax(z / T) with uniform column i
   for (int i = 0; i < gamma; ++i) {
     const int32_t* in = i == 0 ? tokens : drafts + (i - 1) * B;
+    if (sampled) {
+      float* dl = dlogits + (size_t)i * B * c.vocab;
+      DORY_TRY(run_step(m, in, 1, B, 1, k_draft, dl, 1, 0, 1, st));
+      DORY_TRY(launch_k(sample_kernel, dim3(B), dim3(kSampleThreads), 0, st, (const float*)dl,
+                        c.vocab, inv_t, u + i, 2 * gamma + 1, drafts + i * B) == cudaSuccess
+                   ? DORY_OK
+                   : DORY_ECUDA);
+      continue;
+    }
     DORY_TRY(run_step(m, in, 1, B, 1, k_draft, logits, 1, 0, 1, st, drafts + i * B));
     if (!m->next_done) {
       pb(m, DORY_K_ARGMAX, st);
@@ -1781,16 +1806,45 @@ int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, 
                : DORY_ECUDA);
   DORY_TRY(run_step(m, vin, gamma + 1, B, gamma + 1, k_verify, logits, gamma + 1, 0, gamma + 1,
                     st));
-  pb(m, DORY_K_ARGMAX, st);
-  DORY_TRY(pe(m, st,
-              launch_k(argmax_kernel, dim3(B * (gamma + 1)), dim3(1024), 0, st,
-                       (const float*)logits, c.vocab, g) == cudaSuccess
-                  ? DORY_OK
-                  : DORY_ECUDA));
-  DORY_TRY(launch_k(spec_accept_kernel, dim3(1), dim3(256), 0, st, (const int32_t*)drafts,
-                    (const int32_t*)g, B, gamma, out, n_dev) == cudaSuccess
-               ? DORY_OK
-               : DORY_ECUDA);
+  if (sampled) {
+    // softmax statistics of the verifier's and the drafter's rows, kept
+    // drafts, emitted tokens (rejection sampling)
+    float2* sp = stats;
+    float2* sq = stats + (size_t)B * (gamma + 1);
+    DORY_TRY(launch_k(row_stats_kernel, dim3(B * (gamma + 1)), dim3(kSampleThreads), 0, st,
+                      (const float*)logits, c.vocab, inv_t, sp) == cudaSuccess
+                 ? DORY_OK
+                 : DORY_ECUDA);
+    DORY_TRY(launch_k(row_stats_kernel, dim3(B * gamma), dim3(kSampleThreads), 0, st,
+                      (const float*)dlogits, c.vocab, inv_t, sq) == cudaSuccess
+                 ? DORY_OK
+                 : DORY_ECUDA);
+    DORY_TRY(launch_k(spec_keep_kernel, dim3(1), dim3(256), 0, st, (const float*)logits,
+                      (const float2*)sp, (const float*)dlogits, (const float2*)sq,
+                      (const int32_t*)drafts, u, B, gamma, c.vocab, inv_t, kept) == cudaSuccess
+                 ? DORY_OK
+                 : DORY_ECUDA);
+    DORY_TRY(launch_k(spec_emit_kernel, dim3(B), dim3(kSampleThreads), 0, st,
+                      (const float*)logits, (const float2*)sp, (const float*)dlogits,
+                      (const float2*)sq, (const int32_t*)drafts, u, (const int32_t*)kept, B, gamma,
+                      c.vocab, inv_t, out, n_dev) == cudaSuccess
+                 ? DORY_OK
+                 : DORY_ECUDA);
+    if (kept_out && cudaMemcpyAsync(kept_out, kept, (size_t)B * 4, cudaMemcpyDeviceToDevice, st) !=
+                        cudaSuccess)
+      return DORY_ECUDA;
+  } else {
+    pb(m, DORY_K_ARGMAX, st);
+    DORY_TRY(pe(m, st,
+                launch_k(argmax_kernel, dim3(B * (gamma + 1)), dim3(1024), 0, st,
+                         (const float*)logits, c.vocab, g) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
+    DORY_TRY(launch_k(spec_accept_kernel, dim3(1), dim3(256), 0, st, (const int32_t*)drafts,
+                      (const int32_t*)g, B, gamma, out, n_dev) == cudaSuccess
+                 ? DORY_OK
+                 : DORY_ECUDA);
+  }
   // positions past the accepted ones go back to what the rings held
   DORY_TRY(ring_copy(1, n_dev));
   int n = 0;
@@ -1801,6 +1855,46 @@ int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, 
   m->len = L + n;
   *n_out = n;
   return DORY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dory_speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k_verify,
+                          int gamma, void* scratch, size_t scratch_bytes, int32_t* out, int* n_out,
+                          void* stream) {
+  return speculative_step(m, tokens, B, k_draft, k_verify, gamma, 0.0f, nullptr, scratch,
+                          scratch_bytes, out, n_out, nullptr, stream);
+}
+
+int dory_speculative_sample_step(dory_t* m, const int32_t* tokens, int B, int k_draft,
+                                 int k_verify, int gamma, float temperature, const float* u,
+                                 void* scratch, size_t scratch_bytes, int32_t* out, int* n_out,
+                                 int32_t* kept, void* stream) {
+  if (!u || !(temperature > 0.0f)) return DORY_EINVAL;
+  return speculative_step(m, tokens, B, k_draft, k_verify, gamma, temperature, u, scratch,
+                          scratch_bytes, out, n_out, kept, stream);
+}
+
+int dory_debug_speculative_layout(const dory_t* m, int B, int gamma, size_t* offsets) {
+  if (!m || !offsets || !m->bound || B <= 0 || gamma < 1 || gamma > kSpecMaxGamma)
+    return DORY_EINVAL;
+  const SpecScratch S = spec_layout(m, B, gamma, spec_rings(m).size());
+  offsets[0] = S.logits;
+  offsets[1] = S.dlogits;
+  offsets[2] = S.drafts;
+  return DORY_OK;
+}
+
+int dory_sample_tokens(const float* logits, int rows, int V, float temperature, const float* u,
+                       int32_t* out, void* stream) {
+  if (!logits || !u || !out || rows <= 0 || V <= 0 || !(temperature > 0.0f)) return DORY_EINVAL;
+  return launch_k(sample_kernel, dim3(rows), dim3(kSampleThreads), 0,
+                  static_cast<cudaStream_t>(stream), logits, V, 1.0f / temperature, u, 1,
+                  out) == cudaSuccess
+             ? DORY_OK
+             : DORY_ECUDA;
 }
 
 int dory_copy_prefix(dory_t* m, int src, const int* dst, int n_dst, int len, void* stream) {

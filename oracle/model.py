@@ -389,7 +389,7 @@ class Oracle:
         return out, n
 
     def speculative_sample_step(self, token, k_draft: int, k_verify: int, gamma: int,
-                                temperature: float, u):
+                                temperature: float, u, margins=None):
         """One step of self-speculative decoding with rejection sampling
         (Self-Speculative Decoding; the rule is written out in
         oracle/sampling.py): gamma drafts drawn at k_draft from softmax(z / T),
@@ -399,7 +399,8 @@ class Oracle:
         Cache handling as in speculative_step.  u [B, 2 gamma + 1]: uniforms,
         columns 0 .. gamma - 1 draw the drafts, gamma .. 2 gamma - 1 decide
         acceptance, 2 gamma draws the residual or last token.  Returns
-        (tokens [B, n], n, kept drafts per sequence [B])."""
+        (tokens [B, n], n, kept drafts per sequence [B]); margins (optional
+        list) collects the decision margins of oracle/sampling.py."""
         if self.mode_bound != PER_LOOP or self.k_bound != k_verify or not (
                 1 <= k_draft <= k_verify) or gamma < 1 or temperature <= 0:
             raise ValueError("self-speculative sampling needs per-loop caching bound at k_verify")
@@ -411,7 +412,7 @@ class Oracle:
         for i in range(gamma):
             h = self.step(cur.reshape(-1, 1), k_draft, PER_LOOP, draft=True)[:, 0]
             q = softmax_t(self.logits(h), temperature)
-            cur = np.array([sample_weights(q[b], u[b, i]) for b in range(B)], np.int64)
+            cur = np.array([sample_weights(q[b], u[b, i], margins) for b in range(B)], np.int64)
             drafts.append(cur)
             qs.append(q)
         drafts, q = np.stack(drafts, axis=1), np.stack(qs, axis=1)
@@ -421,7 +422,8 @@ class Oracle:
         h = self.step(np.concatenate([token[:, None], drafts], axis=1), k_verify, PER_LOOP)
         self.window_slack = 0
         p = softmax_t(self.logits(h), temperature)                         # [B, gamma + 1, V]
-        out, n, kept = speculative_accept(p, q, drafts, u[:, gamma:2 * gamma], u[:, 2 * gamma])
+        out, n, kept = speculative_accept(p, q, drafts, u[:, gamma:2 * gamma], u[:, 2 * gamma],
+                                          margins)
         self.length = L + n
         return out, n, kept
 

@@ -37,14 +37,20 @@ def softmax_t(z: np.ndarray, temperature: float) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def sample_weights(w: np.ndarray, u: float) -> int:
-    """Inverse-CDF draw from non-negative weights w [V] with uniform u."""
+def sample_weights(w: np.ndarray, u: float, margins=None) -> int:
+    """Inverse-CDF draw from non-negative weights w [V] with uniform u.
+    margins (a list, optional) receives the distance of u * sum(w) to the
+    nearest edge of the chosen interval, relative to sum(w): a draw whose
+    margin is below another implementation's rounding may go either way."""
     w = np.asarray(w, np.float64)
     c = np.cumsum(w)
-    hit = np.nonzero(c > u * c[-1])[0]
-    if len(hit):
-        return int(hit[0])
-    return int(np.nonzero(w > 0)[0][-1])
+    t = u * c[-1]
+    hit = np.nonzero(c > t)[0]
+    x = int(hit[0]) if len(hit) else int(np.nonzero(w > 0)[0][-1])
+    if margins is not None:
+        lo = c[x - 1] if x > 0 else 0.0
+        margins.append(min(abs(t - lo), abs(c[x] - t)) / c[-1])
+    return x
 
 
 def sample_tokens(z: np.ndarray, temperature: float, u: np.ndarray) -> np.ndarray:
@@ -54,19 +60,23 @@ def sample_tokens(z: np.ndarray, temperature: float, u: np.ndarray) -> np.ndarra
 
 
 def speculative_accept(p: np.ndarray, q: np.ndarray, drafts: np.ndarray, u_acc: np.ndarray,
-                       u_res: np.ndarray):
+                       u_res: np.ndarray, margins=None):
     """The acceptance step for a batch.
 
     p [B, gamma + 1, V]: verifier probabilities at the positions of the last
     emitted token and of each draft; q [B, gamma, V]: drafter probabilities
     the drafts were drawn from; drafts [B, gamma]; u_acc [B, gamma]; u_res
-    [B].  Returns (tokens [B, n], n, kept [B] = leading kept drafts)."""
+    [B].  Returns (tokens [B, n], n, kept [B] = leading kept drafts).
+    margins (optional list) receives |u q - p| / p of every acceptance test
+    and the margins of the draws (see sample_weights)."""
     B, G = drafts.shape
     kept = np.zeros(B, np.int64)
     for b in range(B):
         while kept[b] < G:
             i = kept[b]
             x = drafts[b, i]
+            if margins is not None:
+                margins.append(abs(u_acc[b, i] * q[b, i, x] - p[b, i, x]) / p[b, i, x])
             if u_acc[b, i] * q[b, i, x] < p[b, i, x]:
                 kept[b] += 1
             else:
@@ -79,7 +89,7 @@ def speculative_accept(p: np.ndarray, q: np.ndarray, drafts: np.ndarray, u_acc: 
         if kept[b] > j:
             out[b, j] = drafts[b, j]                 # a kept draft
         elif j < G:
-            out[b, j] = sample_weights(np.maximum(p[b, j] - q[b, j], 0.0), u_res[b])
+            out[b, j] = sample_weights(np.maximum(p[b, j] - q[b, j], 0.0), u_res[b], margins)
         else:
-            out[b, j] = sample_weights(p[b, G], u_res[b])
+            out[b, j] = sample_weights(p[b, G], u_res[b], margins)
     return out, n, kept
