@@ -1246,7 +1246,9 @@ def run_profile_target_4b(args):
     """The ncu target of the 4B-class line: one eager prefill of 1 x 8192 at
     loop count --k and one decode step of --batch sequences (default 64) at
     --ctx cached positions (default 32768; cache contents synthetic, written
-    by torch before any library launch).  --slim cuts the depth to 2/4/2."""
+    by torch before any library launch).  --slim cuts the depth to 2/4/2;
+    --quant 1 / 2 quantises the decode model's projections (MXFP8 / NVFP4)
+    first."""
     import torch
 
     import synth
@@ -1258,6 +1260,8 @@ def run_profile_target_4b(args):
     w = synth.make_weights_torch(sh)
     w["layers"] = list(w["layers"])
     md = dory.Model(sh, w, max_batch=B, max_ctx=ctx64(ctx + 1), max_chunk=1, k_max=4)
+    if args.quant:
+        md.quantize(args.quant)
     fill_cache_synthetic(md, sh)
     md.set_length(B, ctx)
     first = torch.tensor(synth.tokens(sh, B, 1, seed=5000)[:, 0], device="cuda")
@@ -1319,6 +1323,8 @@ def main(argv=None):
     ap.add_argument("--ctx", type=int, default=0, help="context of the decode workloads")
     ap.add_argument("--batch", type=int, default=HEAD_B,
                     help="decode sequences of the 4B-class profile target")
+    ap.add_argument("--quant", type=int, default=0, choices=[0, 1, 2],
+                    help="profile target: quantise the decode model (1 MXFP8, 2 NVFP4)")
     ap.add_argument("--decode-only", action="store_true",
                     help="4B-class profile target: skip the prefill")
     ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
