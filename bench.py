@@ -939,6 +939,16 @@ def run_workload_4b(args):
                 res[mode_name] = {"tokens_per_sequence": emitted, "steps": steps,
                                   "ms_per_token": round(1e3 * dt / emitted, 3),
                                   "tokens_s": round(B * emitted / dt, 1)}
+                # one more step with every model launch event-timed by class
+                m.profile_begin(1 << 14)
+                t1 = time.perf_counter()
+                cur, n = advance(cur)
+                torch.cuda.synchronize()
+                wall = time.perf_counter() - t1
+                prof = m.profile_end()
+                res[mode_name]["profiled_step"] = {
+                    "tokens": n, "wall_ms": round(1e3 * wall, 3),
+                    "classes": {k: [round(v[0], 3), v[1]] for k, v in prof.items() if v[1]}}
                 m.close()
                 del m
                 torch.cuda.empty_cache()

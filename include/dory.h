@@ -409,7 +409,10 @@ DORY_API int dory_debug_gemm(const void* A, const void* B, float* C, int M, int 
  * means full causal; scale <= 0 means sqrt(head_dim).  All bf16, device.
  * With C == 1 the split-key decode kernels run and need `scratch`: device
  * memory of at least dory_debug_attention_scratch_bytes(B, n_q, head_dim)
- * bytes (ignored otherwise). */
+ * bytes.  With C > 1 a scratch (256-byte aligned, may be NULL) lets the
+ * mma.sync kernel split the key range of a short chunk over more CTAs, as
+ * the forward pass does with its workspace: up to scratch_bytes /
+ * (B*C*n_q*(head_dim + 2)*4 + 512) splits, merged by a second kernel. */
 DORY_API int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur,
                                   const void* k_cache, const void* v_cache, const void* gate,
                                   void* out, int B, int C, int P0, int S, int n_q, int n_kv,

@@ -495,8 +495,11 @@ def debug_attention(q, k_cur, v_cur, k_cache, v_cache, gate, out, B, C, P0, S, n
     """The library's attention step alone (all tensors bf16 on the device);
     one-token calls run the split-key decode kernels on a torch scratch buffer."""
     import torch
-    nbytes = int(lib().dory_debug_attention_scratch_bytes(B, n_q, head_dim))
-    scratch = torch.empty(nbytes, dtype=torch.uint8, device=out.device) if C == 1 else None
+    if C == 1:
+        nbytes = int(lib().dory_debug_attention_scratch_bytes(B, n_q, head_dim))
+    else:                               # room for 64 key-range splits
+        nbytes = 64 * (B * C * n_q * (head_dim + 2) * 4 + 512)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=out.device)
     _check("dory_debug_attention", lib().dory_debug_attention(
         _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(k_cache), _ptr(v_cache), _ptr(gate), _ptr(out),
         B, C, P0, S, n_q, n_kv, head_dim, window, scale, _ptr(scratch), nbytes,

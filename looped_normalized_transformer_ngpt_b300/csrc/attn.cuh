@@ -20,7 +20,9 @@
 //
 // One CTA = (sequence b, kv head, block of 64/G query positions); its 64
 // rows are (position, head-in-group) pairs so every K/V tile staged in shared
-// memory serves all G heads.  4 warps x 16 rows, mma.sync m16n8k16 bf16 with
+// memory serves all G heads.  With few such CTAs (a short chunk over a long
+// cache: the speculative verifier's gamma + 1 tokens) the key blocks are
+// split over n_split CTAs whose partial results a second kernel merges.  4 warps x 16 rows, mma.sync m16n8k16 bf16 with
 // fp32 accumulation, online softmax in fp32 (exp2), K/V tiles of 64 keys
 // double-buffered with cp.async, XOR-swizzled 16-byte chunks for ldmatrix.
 #pragma once
@@ -40,6 +42,13 @@ struct AttnArgs {
   int n_q, n_kv;
   int window;                    // 0 = full causal
   float scale_log2;              // softmax scale * log2(e)
+  // key-range splits (n_split > 1): each CTA covers one split of its key
+  // blocks and writes un-normalised partials; attn_split_combine_kernel
+  // merges them, normalises and applies the gate
+  int n_split;
+  float* part_o;                 // [B*C, n_q, n_split, dh]
+  float* part_ml;                // [B*C, n_q, n_split, 2]: running max (log2 units), sum
+  int part_cap;                  // launcher input: most splits the partial buffers hold
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -104,13 +113,16 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv, BQ = BR / G;
   const int qb = gridDim.x - 1 - blockIdx.x;    // longest rows first
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int n_split = a.n_split > 1 ? a.n_split : 1;
+  const int kvh = blockIdx.y, b = blockIdx.z / n_split, split = blockIdx.z % n_split;
   const int q0 = qb * BQ;
   const int nqv = min(BQ, a.C - q0);
   const int p_lo = a.P0 + q0, p_hi = a.P0 + q0 + nqv - 1;
   const int k_lo = a.window > 0 ? max(0, p_lo - a.window + 1) : 0;
   const int k_hi = p_hi;
-  const int nblk = (k_hi - k_lo) / BKEY + 1;
+  const int nblk_all = (k_hi - k_lo) / BKEY + 1;
+  const int blk0 = (int)((long long)split * nblk_all / n_split);
+  const int blk1 = (int)((long long)(split + 1) * nblk_all / n_split);
 
   // ---- Q tile: row r = (position i = r / G, head hg = r % G)
   for (int idx = tid; idx < BR * CH; idx += 128) {
@@ -145,7 +157,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
       cp_async16(sVa + o, vs, ok);
     }
   };
-  load_kv(0, 0);
+  if (blk0 < blk1) load_kv(blk0, 0);
   cp_async_commit();
 
   const int g = lane >> 2, t4 = lane & 3;
@@ -165,9 +177,9 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
     qpos[h] = a.P0 + q0 + i;
   }
 
-  for (int blk = 0; blk < nblk; ++blk) {
-    const int buf = blk & 1;
-    if (blk + 1 < nblk) {
+  for (int blk = blk0; blk < blk1; ++blk) {
+    const int buf = (blk - blk0) & 1;
+    if (blk + 1 < blk1) {
       load_kv(blk + 1, buf ^ 1);
       cp_async_commit();
       cp_async_wait<1>();
@@ -175,7 +187,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
       cp_async_wait<0>();
     }
     __syncthreads();
-    if (blk == 0) {
+    if (blk == blk0) {
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
         const int r = warp * 16 + (lane & 15);
@@ -267,6 +279,27 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
     __syncthreads();
   }
 
+  cp_async_wait<0>();
+  if (n_split > 1) {
+    // ---- un-normalised partials of this split (an empty split: m = -inf, l = 0)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float l = l_run[h];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (!qok[h]) continue;
+      const int r = warp * 16 + g + 8 * h;
+      const int i = r / G, hg = r % G;
+      const long long slot =
+          (((long long)b * a.C + q0 + i) * a.n_q + kvh * G + hg) * n_split + split;
+      float* po = a.part_o + slot * DH;
+#pragma unroll
+      for (int nt = 0; nt < DH / 8; ++nt)
+        *reinterpret_cast<float2*>(po + 8 * nt + 2 * t4) = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+      if (t4 == 0) *reinterpret_cast<float2*>(a.part_ml + slot * 2) = make_float2(m_run[h], l);
+    }
+    return;
+  }
   // ---- normalise, gate, store
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -288,6 +321,29 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const AttnArgs a) {
       *reinterpret_cast<uint32_t*>(a.out + base + dim) = pk;
     }
   }
+}
+
+// Merge of the key-range splits: one CTA of DH threads per (row, head);
+// out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, times the gate.
+template <int DH>
+__global__ void __launch_bounds__(DH) attn_split_combine_kernel(const AttnArgs a, int rows) {
+  pdl_wait();
+  pdl_trigger();
+  const long long rh = blockIdx.x;                     // row * n_q + head
+  const int n_split = a.n_split;
+  const float* ml = a.part_ml + rh * n_split * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < n_split; ++s) M = fmaxf(M, ml[2 * s]);
+  float acc = 0.f, l = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const float w = ml[2 * s] == -INFINITY ? 0.f : exp2f(ml[2 * s] - M);
+    acc += w * a.part_o[(rh * n_split + s) * DH + threadIdx.x];
+    l += w * ml[2 * s + 1];
+  }
+  const long long idx = rh * DH + threadIdx.x;
+  const float gt = __bfloat162float(a.gate[idx]);
+  const float inv = l > 0.f ? 1.0f / l : 0.f;         // as the one-pass epilogue
+  a.out[idx] = __float2bfloat16_rn(acc * inv * gt);
 }
 
 }  // namespace dory

@@ -276,9 +276,28 @@ int launch_attn(const AttnArgs& a, int B, cudaStream_t st) {
     attr = true;
   }
   const int G = a.n_q / a.n_kv, BQ = AttnCfg<DH>::BR / G;
-  dim3 grid((a.C + BQ - 1) / BQ, a.n_kv, B);
-  return launch_k(attn_prefill_kernel<DH>, grid, dim3(128), AttnCfg<DH>::SMEM, st, a) ==
-                 cudaSuccess
+  const int qblocks = (a.C + BQ - 1) / BQ;
+  const int base = qblocks * a.n_kv * B;
+  // few CTAs over many key blocks (a short chunk after a long cache): split
+  // the key blocks so that about two CTAs per SM stream them, within the
+  // partial buffers (part_cap splits of every (row, head) when given)
+  AttnArgs aa = a;
+  aa.n_split = 1;
+  if (a.part_o && a.part_ml && a.part_cap > 0 && base < num_sms()) {
+    const int keys = a.window > 0 ? std::min(a.P0 + a.C, a.window + BQ) : a.P0 + a.C;
+    const int nblk = keys / AttnCfg<DH>::BKEY;
+    int ns = (2 * num_sms() + base - 1) / base;
+    ns = std::min(ns, nblk / 2);
+    ns = std::min(ns, a.part_cap);
+    if (ns >= 2) aa.n_split = ns;
+  }
+  dim3 grid(qblocks, a.n_kv, B * aa.n_split);
+  if (launch_k(attn_prefill_kernel<DH>, grid, dim3(128), AttnCfg<DH>::SMEM, st, aa) != cudaSuccess)
+    return DORY_ECUDA;
+  if (aa.n_split == 1) return DORY_OK;
+  const long long rh = (long long)B * a.C * a.n_q;
+  return launch_k(attn_split_combine_kernel<DH>, dim3((unsigned)rh), dim3(DH), 0, st, aa,
+                  (int)(B * a.C)) == cudaSuccess
              ? DORY_OK
              : DORY_ECUDA;
 }
@@ -548,6 +567,9 @@ int launch_gemv(GemvArgs a, cudaStream_t st, int* status = nullptr) {
   if (a.M <= 4)
     e = sw ? (pre ? gemv_j<4, true, true>(a, J, grid, st) : gemv_j<4, true, false>(a, J, grid, st))
            : (pre ? gemv_j<4, false, true>(a, J, grid, st) : gemv_j<4, false, false>(a, J, grid, st));
+  else if (a.M <= 8)   // e.g. the speculative verifier's gamma + 1 rows
+    e = sw ? (pre ? gemv_j<8, true, true>(a, J, grid, st) : gemv_j<8, true, false>(a, J, grid, st))
+           : (pre ? gemv_j<8, false, true>(a, J, grid, st) : gemv_j<8, false, false>(a, J, grid, st));
   else
     e = sw ? (pre ? gemv_j<16, true, true>(a, J, grid, st) : gemv_j<16, true, false>(a, J, grid, st))
            : (pre ? gemv_j<16, false, true>(a, J, grid, st)
@@ -1223,6 +1245,10 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     aa.n_kv = c.n_kv;
     aa.window = full ? 0 : c.window;
     aa.scale_log2 = attn_scale_log2(c);
+    // key-range split partials live in the decode attention's buffers
+    aa.part_o = wsp<float>(m, m->L.dec_o);
+    aa.part_ml = wsp<float>(m, m->L.dec_ml);
+    aa.part_cap = (int)((long long)kDecMaxSplits * m->max_batch / ((long long)B * C));
     int arc = m->use_tc_attn ? launch_attn_tc(aa, B, c.head_dim,
                                               (long long)m->max_batch * c.n_kv * S, status, st)
                              : DORY_EUNSUPPORTED;
@@ -2234,6 +2260,18 @@ int dory_debug_attention(const void* q, const void* k_cur, const void* v_cur, co
   if (g_debug_tc_attn) {
     const int rc = launch_attn_tc(a, B, head_dim, (long long)B * n_kv * a.S, nullptr, st);
     if (rc != DORY_EUNSUPPORTED) return rc;
+  }
+  if (scratch && !((uintptr_t)scratch & 255)) {
+    // key-range splits of the mma.sync kernel, with partials in the scratch
+    const size_t per = (size_t)B * C * n_q * (head_dim + 2) * 4;   // bytes per split
+    const size_t cap = scratch_bytes / (per + 512);
+    if (cap >= 2) {
+      a.part_cap = cap > kDecMaxSplits ? kDecMaxSplits : (int)cap;
+      uint8_t* sc = static_cast<uint8_t*>(scratch);
+      a.part_o = reinterpret_cast<float*>(sc);
+      a.part_ml = reinterpret_cast<float*>(
+          sc + align256((size_t)B * C * n_q * a.part_cap * head_dim * 4));
+    }
   }
   if (head_dim == 32) return launch_attn<32>(a, B, st);
   if (head_dim == 64) return launch_attn<64>(a, B, st);

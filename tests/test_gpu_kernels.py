@@ -105,7 +105,9 @@ def _attn_case(dev, B, C, P0, W, nq, nkv, dh, seed, uniform=False, S=None):
 @pytest.mark.parametrize("dh", [32, 128])
 @pytest.mark.parametrize("W,P0,C", [(16, 0, 64), (16, 40, 37), (5, 10, 1), (0, 0, 100),
                                     (0, 71, 1), (1, 3, 20), (512, 0, 130), (0, 300, 1),
-                                    (64, 200, 1), (0, 0, 1)])
+                                    (64, 200, 1), (0, 0, 1),
+                                    # short chunks after long caches: key-range splits
+                                    (0, 2000, 5), (300, 2000, 3), (0, 1500, 17)])
 def test_attention_mask_is_exact(dev, dh, W, P0, C):
     """Equal scores and one-hot values e_(j mod dh): every output is
     count / n with n = |visible keys|, so the bf16 result equals the value
@@ -130,7 +132,9 @@ def test_attention_mask_is_exact(dev, dh, W, P0, C):
 
 @pytest.mark.parametrize("dh,nq,nkv", [(32, 4, 2), (128, 8, 2), (128, 16, 4), (64, 4, 4)])
 @pytest.mark.parametrize("W,P0,C", [(16, 0, 64), (24, 50, 30), (0, 0, 130), (0, 33, 1),
-                                    (512, 600, 1), (8, 9, 17), (0, 1000, 1), (512, 3000, 1)])
+                                    (512, 600, 1), (8, 9, 17), (0, 1000, 1), (512, 3000, 1),
+                                    # short chunks after long caches: key-range splits
+                                    (0, 3000, 5), (512, 3000, 5), (0, 1000, 17), (2048, 5001, 3)])
 def test_attention_matches_oracle(dev, dh, nq, nkv, W, P0, C):
     B = 2
     out, q, k_all, v_all, gate = _attn_case(dev, B, C, P0, W, nq, nkv, dh, 1)
