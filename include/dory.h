@@ -46,7 +46,8 @@
  *     Device-side failures (a bounded wait that expired) set a status word
  *     that dory_device_status reads.  No call aborts or throws.
  *   - All sequences of one call share the same current length (they are
- *     prefilled and decoded together).
+ *     prefilled and decoded together), except in the ragged-batch calls
+ *     (dory_prefill_slot, dory_decode_step_ragged) below.
  */
 #ifndef DORY_H
 #define DORY_H
@@ -317,6 +318,43 @@ typedef struct {
  * DORY_EINVAL for null pointers, misaligned codes (16 bytes) or NVFP4
  * scales (2 bytes), or d, n_q*head_dim or ffn not multiples of 32. */
 DORY_API int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* layers);
+
+/* ------------------------------------------------------------------------
+ * Ragged batches: sequences of different lengths in one decode step (the
+ * serving setting of "Dory1.0-4B: A Looped Normalized-GPT", Last-Loop KV
+ * Caching; each sequence computes exactly what it computes alone).  The
+ * handle then keeps one length per batch slot.  The uniform calls
+ * (dory_prefill, dory_decode_step, dory_speculative_step /
+ * _sample_step) return DORY_EINVAL while the lengths are per sequence;
+ * dory_set_length or dory_reset returns to one shared length.
+ * ---------------------------------------------------------------------- */
+
+/* Declares per-sequence lengths: batch slots 0 .. B-1 hold lengths[b]
+ * positions (host array; host state only, as dory_set_length).  Requires
+ * B <= max_batch and lengths <= max_ctx (DORY_ECAPACITY). */
+DORY_API int dory_set_lengths(dory_t* m, int B, const int* lengths);
+
+/* The lengths of batch slots 0 .. B-1 (host array out; no CUDA call). */
+DORY_API int dory_get_lengths(const dory_t* m, int B, int* out);
+
+/* Prefill of ONE sequence in batch slot `slot` (< max_batch), continuing from
+ * that slot's own length: T tokens (device int32), loop count k, logits of
+ * the last position [V] or, with all_logits, of every position [T][V].
+ * The other slots are untouched.  Asynchronous on `stream`.  From the
+ * uniform state, every slot keeps its length and the handle switches to
+ * per-sequence lengths. */
+DORY_API int dory_prefill_slot(dory_t* m, int slot, const int32_t* tokens, int T, int k,
+                               int cache_mode, float* logits, int all_logits, void* stream);
+
+/* One decode step of batch slots 0 .. B-1 (B <= 128), each at its own
+ * length: token b is the next token of slot b; RoPE, the visible keys, the
+ * window and the ring slot of its new key and value follow its own
+ * position.  Arguments and outputs as for dory_decode_step.  Each slot's
+ * length grows by one.  The decode attention's schedule gives every
+ * (sequence, kv head) group as many key tiles as the longest sequence has,
+ * so a batch costs about what the same batch at its longest length costs. */
+DORY_API int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, int k,
+                                     int cache_mode, float* logits, int32_t* next, void* stream);
 
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);

@@ -106,6 +106,10 @@ _SIGS = {
     "dory_sample_tokens": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
     "dory_debug_speculative_layout": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "dory_copy_prefix": (_I, [_P, _I, ctypes.POINTER(_I), _I, _I, _P]),
+    "dory_set_lengths": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "dory_get_lengths": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "dory_prefill_slot": (_I, [_P, _I, _P, _I, _I, _I, _P, _I, _P]),
+    "dory_decode_step_ragged": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "dory_quant_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                               ctypes.POINTER(ctypes.c_size_t)]),
     "dory_quantize_matrix": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P]),
@@ -339,6 +343,48 @@ class Model:
             table[l] = DoryQLayer(mats["qkvg"], mats["o"], mats["upg"], mats["down"])
         _check("dory_set_quantized_weights", L.dory_set_quantized_weights(self.handle, fmt, table))
         self._q = keep
+
+    def set_lengths(self, lengths):
+        """Per-sequence lengths of batch slots 0 .. len(lengths) - 1."""
+        arr = (ctypes.c_int * len(lengths))(*[int(x) for x in lengths])
+        _check("dory_set_lengths", lib().dory_set_lengths(self.handle, len(lengths), arr))
+
+    def lengths(self, B):
+        arr = (ctypes.c_int * B)()
+        _check("dory_get_lengths", lib().dory_get_lengths(self.handle, B, arr))
+        return list(arr)
+
+    def prefill_slot(self, slot, tokens, k, cache_mode=None, all_logits=False, logits=None,
+                     stream=None):
+        """Prefill of one sequence (tokens int32 device [T]) in batch slot
+        `slot`, from that slot's own length.  Returns fp32 logits [V] (last
+        position) or [T, V]."""
+        import torch
+        T = tokens.shape[-1]
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        if logits is None:
+            shp = (T, self.shape.vocab) if all_logits else (self.shape.vocab,)
+            logits = torch.empty(shp, dtype=torch.float32, device=self.device)
+        _check("dory_prefill_slot", lib().dory_prefill_slot(
+            self.handle, slot, _ptr(tokens), T, k, mode, _ptr(logits), 1 if all_logits else 0,
+            _stream_ptr(stream)))
+        return logits
+
+    def decode_ragged(self, tokens, k, cache_mode=None, logits=None, next_tokens=None,
+                      stream=None):
+        """One decode step of slots 0 .. B-1 at their own lengths.  Returns
+        (logits [B, V], next [B])."""
+        import torch
+        B = tokens.shape[0]
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        if logits is None:
+            logits = torch.empty((B, self.shape.vocab), dtype=torch.float32, device=self.device)
+        if next_tokens is None:
+            next_tokens = torch.empty((B,), dtype=torch.int32, device=self.device)
+        _check("dory_decode_step_ragged", lib().dory_decode_step_ragged(
+            self.handle, _ptr(tokens), B, k, mode, _ptr(logits), _ptr(next_tokens),
+            _stream_ptr(stream)))
+        return logits, next_tokens
 
     def copy_prefix(self, src, dst, length, stream=None):
         """Copy the cached positions 0 .. length-1 of sequence src into the

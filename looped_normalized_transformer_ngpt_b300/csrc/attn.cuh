@@ -574,7 +574,8 @@ struct DecAttnArgs {
   int ldy, n_parts;
   long long part_stride;
   const float* s_qk;              // RAW: [dh]
-  const float2* rope;             // RAW: [dh / 2] (cos, sin) of position P0, or null
+  const float2* rope;             // RAW: [dh / 2] (cos, sin) of position P0 ([B][dh / 2] of
+                                  // each sequence's position when p0s is set), or null
   const __nv_bfloat16* q;         // READY: [B, n_q, dh]
   const __nv_bfloat16* k_cur;     // READY: [B, n_kv, dh]
   const __nv_bfloat16* v_cur;
@@ -582,7 +583,9 @@ struct DecAttnArgs {
   __nv_bfloat16* k_cache;         // [., n_kv, S, dh] of this layer / slice
   __nv_bfloat16* v_cache;
   int store;
-  int P0, S, n_q, n_kv, window;
+  int P0, S, n_q, n_kv, window;   // P0: the position of every sequence's new token, or
+                                  // (ragged batches) the largest one
+  const int* p0s;                 // ragged batches: [B] each sequence's position (device), or null
   float scale_log2;
   int chunk, n_splits;
   int tpg;                        // TMA kernel: 64-key tiles per (sequence, kv head) group
@@ -623,16 +626,21 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv;
-  const int P0 = a.P0;
-  const int lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;
   const int NS = a.n_splits;
   const int n_items = NS * a.n_kv * a.B;
 
+  // ragged batches: the positions were written by an earlier kernel of the
+  // step, so wait for the previous kernel before the first tile loads
+  if (a.p0s) pdl_wait();
   // Work items (split, kv head, sequence) of equal size; the CTAs of the grid
   // (no more than are resident) stride over them.
   bool first = true;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int split = item % NS, kvh = (item / NS) % a.n_kv, b = item / (NS * a.n_kv);
+    // this sequence's position (ragged batches: its own; trailing splits of
+    // shorter sequences are empty)
+    const int P0 = a.p0s ? a.p0s[b] : a.P0;
+    const int lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;
     const int k0 = lo + split * a.chunk;
     const int k1 = min(k0 + a.chunk, P0);                    // cached keys only
     const int ntiles = k1 > k0 ? (k1 - k0 + kDecTile - 1) / kDecTile : 0;
@@ -716,7 +724,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
             if (i < HALF) {
               float c1 = x1[e], c2 = x2[e];
               if (a.rope) {
-                const float2 cs = a.rope[i];
+                const float2 cs = a.rope[(a.p0s ? b * HALF : 0) + i];
                 c1 = x1[e] * cs.x - x2[e] * cs.y;
                 c2 = x2[e] * cs.x + x1[e] * cs.y;
               }

@@ -86,9 +86,6 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv;
-  const int P0 = a.P0;
-  const int lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;   // first visible cached key
-  const int lo_a = lo / kDecTile * kDecTile;
   const int n_groups = a.n_kv * a.B;
   const long long tpg = a.tpg;
   const long long T = (long long)n_groups * tpg;
@@ -105,17 +102,26 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
     tma_prefetch_desc(&tm_vc);
   }
   __syncthreads();
+  // ragged batches: the positions were written by an earlier kernel of the
+  // step, so every warp waits for the previous kernel before using them
+  if (a.p0s) pdl_wait();
 
   // This CTA's pieces in order.  With cached keys: its tile range cut at
   // group boundaries; without (tpg == 0): groups blockIdx.x, + gridDim.x, ...
   // as single pieces with no tiles.  `cur` is the piece's first global tile
-  // (or its group); returns false past the last piece.
+  // (or its group); returns false past the last piece.  Every group spans
+  // tpg tiles of the schedule; in a ragged batch a shorter sequence's group
+  // has fewer real tiles, and its pieces past them carry none.  P0 / lo:
+  // the group's sequence position and first visible cached key.
   const long long x_end = tpg > 0 ? ((long long)blockIdx.x + 1) * T / ncta : n_groups;
   auto piece = [&](long long cur, int& grp, int& split, int& nseg, int& k0, int& k1,
-                   int& ntiles, long long& next) -> bool {
+                   int& ntiles, long long& next, int& P0, int& lo) -> bool {
     if (cur >= x_end) return false;
+    grp = (int)(tpg == 0 ? cur : cur / tpg);
+    P0 = a.p0s ? a.p0s[grp / a.n_kv] : a.P0;
+    lo = a.window > 0 ? max(0, P0 - a.window + 1) : 0;
+    const int lo_a = lo / kDecTile * kDecTile;
     if (tpg == 0) {
-      grp = (int)cur;
       split = 0;
       nseg = 1;
       k0 = k1 = lo_a;
@@ -123,16 +129,16 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
       next = cur + ncta;
       return true;
     }
-    grp = (int)(cur / tpg);
     const long long g0 = (long long)grp * tpg;
     const long long e = min(x_end, g0 + tpg);
     const long long c_first = ((g0 + 1) * ncta - 1) / T;
     const long long c_last = ((g0 + tpg) * ncta - 1) / T;
     split = (int)(blockIdx.x - c_first);
     nseg = (int)(c_last - c_first + 1);
+    const long long real = P0 > lo_a ? (P0 - lo_a + kDecTile - 1) / kDecTile : 0;   // <= tpg
     k0 = lo_a + (int)(cur - g0) * kDecTile;            // 64-aligned
     k1 = min(lo_a + (int)(e - g0) * kDecTile, P0);      // cached keys only
-    ntiles = (int)(e - cur);
+    ntiles = (int)max(0ll, min(e, g0 + real) - cur);
     next = e;
     return true;
   };
@@ -146,10 +152,10 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
     // projections).
     if (lane == 0) {
       int g = 0;
-      int grp, split, nseg, k0, k1, ntiles;
+      int grp, split, nseg, k0, k1, ntiles, p0g, log;
       long long nx;
-      for (long long cur = x_begin; !*abort_flag && piece(cur, grp, split, nseg, k0, k1, ntiles, nx);
-           cur = nx) {
+      for (long long cur = x_begin;
+           !*abort_flag && piece(cur, grp, split, nseg, k0, k1, ntiles, nx, p0g, log); cur = nx) {
         const int row0 = grp * a.S;                    // group = b * n_kv + kv head
         for (int t = 0; t < ntiles; ++t, ++g) {
           const int st = g % kDecTmaStages;
@@ -187,12 +193,18 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
   auto csync = [] { named_bar(1, 128); };
   bool first = true;
   int g = 0;
-  int grp, split, nseg, k0, k1, ntiles;
+  int grp, split, nseg, k0, k1, ntiles, P0, lo;
   long long nx;
-  for (long long cur = x_begin; piece(cur, grp, split, nseg, k0, k1, ntiles, nx); cur = nx) {
+  for (long long cur = x_begin; piece(cur, grp, split, nseg, k0, k1, ntiles, nx, P0, lo);
+       cur = nx) {
     const int kvh = grp % a.n_kv, b = grp / a.n_kv;
     const int NS = nseg;                                 // splits of this group
     const int kv_lo = max(k0, lo);                       // visible keys [kv_lo, k1)
+    if (RAW && a.rope && a.p0s) {
+      // ragged batches: RoPE of this sequence's own position
+#pragma unroll
+      for (int e = 0; e < HALF / 32; ++e) rcs[e] = a.rope[b * HALF + lane + 32 * e];
+    }
     if (first) {
       pdl_wait();
       pdl_trigger();

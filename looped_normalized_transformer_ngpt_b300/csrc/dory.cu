@@ -48,7 +48,7 @@ constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 struct WsLayout {
   size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, ropet_swa,
       ropet_full, gy, dec_o,
-      dec_ml, dec_cnt, parts, total;
+      dec_ml, dec_cnt, parts, seq_pos, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -75,8 +75,10 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.g = take(M * hq * 2);
   L.att = take(M * hq * 2);
   L.m = take(M * (size_t)c.ffn * 2);
-  L.rope_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);
-  L.rope_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
+  // RoPE rows: the call's positions, or (ragged decode) each sequence's
+  const size_t rope_rows = max_chunk > max_batch ? max_chunk : max_batch;
+  L.rope_swa = take(rope_rows * (c.head_dim / 2) * 8);
+  L.rope_full = take(rope_rows * (c.head_dim / 2) * 8);
   L.ropet_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);    // transposed copies
   L.ropet_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
   // few-row projections (decode): fp32 output of the QKV+gate / up+gate GEMV
@@ -87,6 +89,7 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.dec_o = take((size_t)max_batch * c.n_q * kDecMaxSplits * c.head_dim * 4);
   L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
   L.dec_cnt = take((size_t)max_batch * c.n_kv * 4);   // split tickets, zero between launches
+  L.seq_pos = take((size_t)max_batch * 4);            // ragged decode: positions
   // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
   if (max_batch > kGemvMaxM) {
     const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
@@ -714,7 +717,9 @@ int launch_dec_attn_tma(DecAttnArgs a, int B, cudaStream_t st) {
   // at least kDecMinTiles tiles each; a group spans at most
   // ceil(tpg / floor(T / grid)) + 1 ranges, which must stay within the
   // kDecMaxSplits partials per head that the workspace holds
-  const long long tpg = n_cache > 0 ? (n_cache + kDecTile - 1) / kDecTile : 0;
+  // ragged batches: the caller's count, the most tiles of any sequence
+  const long long tpg =
+      a.p0s ? a.tpg : (n_cache > 0 ? (n_cache + kDecTile - 1) / kDecTile : 0);
   const long long T = groups * tpg;
   long long grid = num_sms();
   int max_seg = 1;
@@ -810,6 +815,13 @@ struct dory_model {
   CUtensorMap tm_embed_out{};
   // sequence state
   int len = 0;
+  // ragged batches: per-sequence lengths (seq_len[b] = len for every b < batch
+  // while `ragged` is false), the batch slot of a one-sequence call and
+  // whether the current step decodes at per-sequence positions
+  std::vector<int> seq_len;
+  bool ragged = false;
+  int slot = 0;
+  bool ragged_step = false;
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
   int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
@@ -902,9 +914,34 @@ int flush_pending(dory_model* m, StepState& s, int M, cudaStream_t st) {
 }
 
 // Cache block of (layer, slice): K (which = 0) or V (which = 1).
+// K or V block of (layer, slice), from the batch slot of a one-sequence
+// call (m->slot; 0 otherwise): [max_batch - slot][n_kv][slots][head_dim].
 __nv_bfloat16* kv_block(dory_model* m, int l, int slice, int which) {
+  const dory_config& c = m->cfg;
   return reinterpret_cast<__nv_bfloat16*>(
-      m->kv + kv_offset(m->cfg, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, slice, which));
+             m->kv + kv_offset(c, m->max_batch, m->max_ctx, m->k_max, m->cache_mode, l, slice,
+                               which)) +
+         (size_t)m->slot * c.n_kv * slots_of(c, l, m->max_ctx) * c.head_dim;
+}
+
+// Rows ([batch][n_kv][slots]) of a block as kv_block returns it.
+long long cache_rows(const dory_model* m, int slots) {
+  return (long long)(m->max_batch - m->slot) * m->cfg.n_kv * slots;
+}
+
+// Ragged decode: 64-key tiles per (sequence, kv head) group of the TMA decode
+// attention's schedule, the most over the step's sequences (window <= 0:
+// full layer).
+int ragged_tpg(const dory_model* m, int B, int window) {
+  int t = 0;
+  for (int b = 0; b < B; ++b) {
+    const int p0 = m->seq_len[b];
+    const int lo = window > 0 ? (p0 - window + 1 > 0 ? p0 - window + 1 : 0) : 0;
+    const int lo_a = lo / kDecTile * kDecTile;
+    const int n = p0 > lo_a ? (p0 - lo_a + kDecTile - 1) / kDecTile : 0;
+    if (n > t) t = n;
+  }
+  return t;
 }
 
 float attn_scale_log2(const dory_config& c) {
@@ -980,8 +1017,12 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   da.part_ml = wsp<float>(m, m->L.dec_ml);
   da.counter = wsp<int>(m, m->L.dec_cnt);
   da.out = att;
-  da.cache_rows = (long long)m->max_batch * c.n_kv * da.S;
+  da.cache_rows = cache_rows(m, da.S);
   da.status = wsp<int>(m, m->L.status);
+  if (m->ragged_step) {
+    da.p0s = wsp<int>(m, m->L.seq_pos);
+    da.tpg = ragged_tpg(m, B, da.window);
+  }
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
 
@@ -1110,8 +1151,12 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
   da.part_ml = wsp<float>(m, m->L.dec_ml);
   da.counter = wsp<int>(m, m->L.dec_cnt);
   da.out = att;
-  da.cache_rows = (long long)m->max_batch * c.n_kv * da.S;
+  da.cache_rows = cache_rows(m, da.S);
   da.status = wsp<int>(m, m->L.status);
+  if (m->ragged_step) {
+    da.p0s = wsp<int>(m, m->L.seq_pos);
+    da.tpg = ragged_tpg(m, B, da.window);
+  }
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
 
@@ -1226,7 +1271,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     da.part_ml = wsp<float>(m, m->L.dec_ml);
     da.counter = wsp<int>(m, m->L.dec_cnt);
     da.out = att;
-    da.cache_rows = (long long)m->max_batch * c.n_kv * S;
+    da.cache_rows = cache_rows(m, S);
     da.status = status;
     DORY_TRY(pe(m, st, dec_attn<false>(da, B, c.head_dim, st)));
   } else {
@@ -1250,7 +1295,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     aa.part_ml = wsp<float>(m, m->L.dec_ml);
     aa.part_cap = (int)((long long)kDecMaxSplits * m->max_batch / ((long long)B * C));
     int arc = m->use_tc_attn ? launch_attn_tc(aa, B, c.head_dim,
-                                              (long long)m->max_batch * c.n_kv * S, status, st)
+                                              cache_rows(m, S), status, st)
                              : DORY_EUNSUPPORTED;
     if (arc == DORY_EUNSUPPORTED) {
       if (c.head_dim == 32) arc = launch_attn<32>(aa, B, st);
@@ -1425,7 +1470,21 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       !encode_f32_out(&em.out, m->ws + m->L.y32, M, c.d, c.d))   // output / down projections
     return DORY_ECUDA;
 
-  if (c.rope) {
+  if (m->ragged_step) {
+    // each sequence's position: RoPE rows and the positions for the attention
+    SeqPos sp{};
+    for (int b = 0; b < B; ++b) sp.p[b] = m->seq_len[b];
+    const int n = 2 * B * (c.head_dim / 2);
+    pb(m, DORY_K_ROPE, st);
+    DORY_TRY(pe(m, st,
+                launch_k(rope_rows_kernel, dim3((n + 255) / 256), dim3(256), 0, st,
+                         c.rope ? wsp<float2>(m, m->L.rope_swa) : nullptr,
+                         c.rope ? wsp<float2>(m, m->L.rope_full) : nullptr, sp, B, c.head_dim,
+                         (double)c.rope_base_swa, (double)c.rope_base_full,
+                         wsp<int>(m, m->L.seq_pos)) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
+  } else if (c.rope) {
     const int n = 2 * C * (c.head_dim / 2);
     const int blocks = (n + 255) / 256;
     pb(m, DORY_K_ROPE, st);
@@ -1538,6 +1597,10 @@ int check_call(dory_model* m, int B, int n_new, int k, int cache_mode) {
   return DORY_OK;
 }
 
+
+int dory_prefill_body(dory_t* m, const int32_t* tokens, int B, int T, int k, float* logits,
+                      int all_logits, void* stream);
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -1619,6 +1682,9 @@ int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes, i
   m->batch = 0;
   m->last_rows = 0;
   m->hsel_last = 0;
+  m->seq_len.assign(max_batch, 0);
+  m->ragged = false;
+  m->slot = 0;
   // status word and split tickets start at zero (tickets return to zero
   // after every launch that uses them)
   if (cudaMemsetAsync(m->ws + m->L.status, 0, 256, 0) != cudaSuccess ||
@@ -1630,9 +1696,22 @@ int dory_bind(dory_t* m, void* kv, size_t kv_bytes, void* ws, size_t ws_bytes, i
 
 int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k, int cache_mode,
                  float* logits, int all_logits, void* stream) {
-  const int rc = check_call(m, B, T, k, cache_mode);
+  int rc = check_call(m, B, T, k, cache_mode);
   if (rc != DORY_OK) return rc;
   if (!tokens) return DORY_EINVAL;
+  if (m->ragged) return DORY_EINVAL;     // per-sequence lengths: dory_prefill_slot
+  rc = dory_prefill_body(m, tokens, B, T, k, logits, all_logits, stream);
+  if (rc == DORY_OK)
+    for (int b = 0; b < B; ++b) m->seq_len[b] = m->len;
+  return rc;
+}
+}  // extern "C"
+
+namespace {
+// The chunk loop of a prefill of B sequences at m->len (from batch slot
+// m->slot when B == 1).
+int dory_prefill_body(dory_t* m, const int32_t* tokens, int B, int T, int k, float* logits,
+                      int all_logits, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   m->launches = 0;
   m->batch = B;
@@ -1659,18 +1738,23 @@ int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k, int cach
   }
   return DORY_OK;
 }
+}  // namespace
+
+extern "C" {
 
 int dory_decode_step(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                      float* logits, int32_t* next, void* stream) {
   const int rc = check_call(m, B, 1, k, cache_mode);
   if (rc != DORY_OK) return rc;
   if (!tokens) return DORY_EINVAL;
+  if (m->ragged) return DORY_EINVAL;     // per-sequence lengths: dory_decode_step_ragged
   if (next && !logits) return DORY_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   m->launches = 0;
   m->batch = B;
   const int r = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st, next);
   if (r != DORY_OK) return r;
+  for (int b = 0; b < B; ++b) m->seq_len[b] = m->len;
   if (next && !m->next_done) {
     pb(m, DORY_K_ARGMAX, st);
     return pe(m, st,
@@ -1755,6 +1839,7 @@ int speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k
   if (gamma < 1 || gamma > kSpecMaxGamma || k_draft < 1 || k_draft > k_verify) return DORY_EINVAL;
   if (m->cache_mode != DORY_CACHE_PER_LOOP || k_verify != m->k_max) return DORY_EKMISMATCH;
   if (reinterpret_cast<uintptr_t>(scratch) & 255) return DORY_EINVAL;
+  if (m->ragged) return DORY_EINVAL;     // sequences of one length only
   // the verifying pass is one chunk of gamma + 1 tokens per sequence
   int rc = check_call(m, B, gamma + 1, k_verify, DORY_CACHE_PER_LOOP);
   if (rc != DORY_OK) return rc;
@@ -1879,6 +1964,7 @@ int speculative_step(dory_t* m, const int32_t* tokens, int B, int k_draft, int k
     return DORY_ECUDA;
   if (n < 1 || n > gamma + 1) return DORY_EDEVICE;
   m->len = L + n;
+  for (int b = 0; b < B; ++b) m->seq_len[b] = m->len;
   *n_out = n;
   return DORY_OK;
 }
@@ -2038,6 +2124,9 @@ int dory_set_length(dory_t* m, int B, int len) {
   if (B > m->max_batch || len > m->max_ctx) return DORY_ECAPACITY;
   m->len = len;
   m->batch = len > 0 ? B : 0;
+  m->ragged = false;
+  std::fill(m->seq_len.begin(), m->seq_len.end(), 0);
+  for (int b = 0; b < B; ++b) m->seq_len[b] = len;
   return DORY_OK;
 }
 
@@ -2046,7 +2135,100 @@ int dory_reset(dory_t* m) {
   m->len = 0;
   m->batch = 0;
   m->last_rows = 0;
+  m->ragged = false;
+  std::fill(m->seq_len.begin(), m->seq_len.end(), 0);
   return DORY_OK;
+}
+
+int dory_set_lengths(dory_t* m, int B, const int* lengths) {
+  if (!m || !lengths) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (B <= 0) return DORY_EINVAL;
+  if (B > m->max_batch) return DORY_ECAPACITY;
+  for (int b = 0; b < B; ++b) {
+    if (lengths[b] < 0) return DORY_EINVAL;
+    if (lengths[b] > m->max_ctx) return DORY_ECAPACITY;
+  }
+  std::fill(m->seq_len.begin(), m->seq_len.end(), 0);
+  for (int b = 0; b < B; ++b) m->seq_len[b] = lengths[b];
+  m->ragged = true;
+  m->batch = B;
+  m->len = 0;
+  return DORY_OK;
+}
+
+int dory_get_lengths(const dory_t* m, int B, int* out) {
+  if (!m || !out || B <= 0) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (B > m->max_batch) return DORY_ECAPACITY;
+  for (int b = 0; b < B; ++b) out[b] = m->ragged ? m->seq_len[b] : (b < m->batch ? m->len : 0);
+  return DORY_OK;
+}
+
+int dory_prefill_slot(dory_t* m, int slot, const int32_t* tokens, int T, int k, int cache_mode,
+                      float* logits, int all_logits, void* stream) {
+  if (!m || !tokens) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (slot < 0 || slot >= m->max_batch) return DORY_EINVAL;
+  if (!m->ragged) {
+    // from the uniform state: every sequence of the batch keeps its length
+    for (int b = 0; b < m->max_batch; ++b) m->seq_len[b] = b < m->batch ? m->len : 0;
+    m->ragged = true;
+  }
+  const int saved_len = m->len, saved_batch = m->batch;
+  m->len = m->seq_len[slot];
+  m->batch = 0;
+  m->slot = slot;
+  int rc = check_call(m, 1, T, k, cache_mode);
+  if (rc == DORY_OK) rc = dory_prefill_body(m, tokens, 1, T, k, logits, all_logits, stream);
+  if (rc == DORY_OK) m->seq_len[slot] = m->len;
+  m->slot = 0;
+  m->len = saved_len;
+  m->batch = saved_batch > slot + 1 ? saved_batch : slot + 1;
+  return rc;
+}
+
+int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
+                            float* logits, int32_t* next, void* stream) {
+  if (!m || !tokens) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (B <= 0) return DORY_EINVAL;
+  if (B > kRaggedMax) return DORY_EUNSUPPORTED;
+  if (next && !logits) return DORY_EINVAL;
+  if (B > m->max_batch) return DORY_ECAPACITY;
+  if (!m->ragged) {
+    for (int b = 0; b < m->max_batch; ++b) m->seq_len[b] = b < m->batch ? m->len : 0;
+    m->ragged = true;
+  }
+  int pmax = 0;
+  for (int b = 0; b < B; ++b) {
+    if (m->seq_len[b] + 1 > m->max_ctx) return DORY_ECAPACITY;
+    if (m->seq_len[b] > pmax) pmax = m->seq_len[b];
+  }
+  const int saved_len = m->len, saved_batch = m->batch;
+  m->len = pmax;                        // the step's largest position (schedules)
+  m->batch = 0;
+  int rc = check_call(m, B, 1, k, cache_mode);
+  if (rc == DORY_OK) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    m->launches = 0;
+    m->ragged_step = true;
+    rc = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st, next);
+    m->ragged_step = false;
+    if (rc == DORY_OK && next && !m->next_done) {
+      pb(m, DORY_K_ARGMAX, st);
+      rc = pe(m, st,
+              launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits,
+                       m->cfg.vocab, next) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA);
+    }
+    if (rc == DORY_OK)
+      for (int b = 0; b < B; ++b) m->seq_len[b] += 1;
+  }
+  m->len = saved_len;
+  m->batch = saved_batch > B ? saved_batch : B;
+  return rc;
 }
 
 int dory_destroy(dory_t* m) {

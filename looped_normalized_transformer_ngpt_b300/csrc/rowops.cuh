@@ -371,6 +371,40 @@ __global__ void rope_table_kernel(float2* tab0, float2* tab1, float2* tabt0, flo
   }
 }
 
+// Ragged batches: the position of each sequence's new token (host values
+// carried in the launch parameters).
+constexpr int kRaggedMax = 128;
+struct SeqPos {
+  int p[kRaggedMax];
+};
+
+// RoPE (cos, sin) rows of B sequences at their own positions (tab0: base0,
+// tab1: base1, [B][dh / 2]; null tables when RoPE is off) and the positions
+// themselves into pos_out [B] for the decode attention.
+__global__ void rope_rows_kernel(float2* tab0, float2* tab1, const __grid_constant__ SeqPos sp,
+                                 int B, int dh, double base0, double base1, int* pos_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int half = dh / 2;
+  const long long n = (long long)B * half;
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) pos_out[b] = sp.p[b];
+  if (!tab0) return;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < 2 * n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int which = idx >= n;
+    const long long e = idx - which * n;
+    const int b = (int)(e / half), i = (int)(e % half);
+    const double inv_freq = pow(which ? base1 : base0, -2.0 * i / dh);
+    double ang = (double)sp.p[b] * inv_freq;
+    const double two_pi = 6.283185307179586476925286766559;
+    ang -= floor(ang / two_pi) * two_pi;
+    double s, c;
+    sincos(ang, &s, &c);
+    (which ? tab1 : tab0)[e] = make_float2((float)c, (float)s);
+  }
+}
+
 // Greedy token per row: argmax of logits[row, 0..V), lowest index on ties.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V, int32_t* next) {
   __shared__ float bv[32];

@@ -1,0 +1,126 @@
+"""Ragged batches through the C ABI: sequences of different lengths prefilled
+slot by slot (dory_prefill_slot) and decoded together at their own
+positions (dory_decode_step_ragged).  Every sequence must compute exactly
+what it computes alone, so each is compared with its own oracle run
+(prompt + decode steps, one sequence), in both cache modes, with window
+rings that wrap, on the tiny shape (cp.async decode attention) and at the
+4B-class width (TMA decode attention, ring sizes of 64-multiples).  Equal
+lengths through the ragged path must give the uniform path's results bit
+for bit.  Tolerances as in test_gpu_parity."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from test_gpu_parity import check_greedy, check_hidden, check_logits, _tok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import looped_normalized_transformer_ngpt_b300 as dory
+    from looped_normalized_transformer_ngpt_b300 import _build
+    _build.build()
+    dory.lib()
+    return dory
+
+
+def _run(dev, shape, w, lens, mode, k, steps, max_ctx, extend=None, seed=0):
+    B = len(lens)
+    dt = np.float64 if shape.d <= 256 else np.float32
+    m = dev.Model(shape, w, max_batch=B + 1, max_ctx=max_ctx, max_chunk=max(lens), k_max=k,
+                  cache_mode=mode)
+    oracles, nxt = [], []
+    for b, T in enumerate(lens):
+        prompt = synth.tokens(shape, 1, T, seed=seed + b)
+        o = oracle.Oracle(shape, w, dtype=dt)
+        z = o.prefill(prompt, k, mode)["logits"][0, -1]
+        lg = m.prefill_slot(b, _tok(prompt[0]), k, mode).cpu().numpy()
+        check_logits(lg, z)
+        oracles.append(o)
+        nxt.append(int(np.argmax(z)))
+    assert m.lengths(B) == list(lens)
+    cur = np.array(nxt, np.int32)
+    for s in range(steps):
+        if extend is not None and s == extend[0]:
+            # continuous batching: one slot takes more prompt tokens mid-stream
+            b, n = extend[1], extend[2]
+            more = synth.tokens(shape, 1, n, seed=seed + 100)
+            z = oracles[b].prefill(more, k, mode)["logits"][0, -1]
+            lg = m.prefill_slot(b, _tok(more[0]), k, mode).cpu().numpy()
+            check_logits(lg, z)
+            cur[b] = int(np.argmax(z))
+        lg, g = m.decode_ragged(_tok(cur), k, mode)
+        lg, g, hid = lg.cpu().numpy(), g.cpu().numpy(), m.hidden(B).cpu().numpy()
+        for b, o in enumerate(oracles):
+            r = o.decode(cur[b:b + 1], k, mode)
+            check_logits(lg[b:b + 1], r["logits"])
+            check_hidden(hid[b:b + 1], r["hidden"])
+            check_greedy(g[b:b + 1], r["logits"])
+        cur = np.array([int(np.argmax(o_lg)) for o_lg in lg], np.int32)
+    assert m.lengths(B) == [o.length for o in oracles]
+    assert m.device_status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
+@pytest.mark.parametrize("k", [1, 2])
+def test_ragged_tiny(dev, mode, k):
+    shape = synth.TINY_LOOPFULL                      # window 16: the rings wrap
+    _run(dev, shape, synth.make_weights(shape), [5, 23, 12], mode, k, steps=4, max_ctx=64,
+         extend=(2, 0, 7), seed=10 * k + mode)
+
+
+@pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
+def test_ragged_4b_width_windowed(dev, mode):
+    """4B-class width with a 128-position window so that the window rings
+    (128 slots) wrap for the longer sequences and not for the shorter."""
+    shape = synth.DORY4B_SLIM.replace(window=128)
+    _run(dev, shape, synth.make_weights(shape), [70, 200, 131], mode, 2, steps=3, max_ctx=384,
+         extend=(1, 2, 9), seed=30 + mode)
+
+
+def test_ragged_equal_lengths_match_uniform_bitwise(dev):
+    import torch
+    shape = synth.DORY4B_SLIM
+    w = synth.make_weights(shape)
+    B, T, k = 3, 70, 2
+    prompt = synth.tokens(shape, B, T, seed=5)
+    a = dev.Model(shape, w, max_batch=B, max_ctx=128, max_chunk=T, k_max=k)
+    b = dev.Model(shape, w, max_batch=B, max_ctx=128, max_chunk=T, k_max=k)
+    a.prefill(_tok(prompt), k)
+    b.prefill(_tok(prompt), k)
+    tok = _tok(np.array([3, 1000, 77], np.int32))
+    for _ in range(3):
+        la, ga = a.decode(tok, k)
+        lb, gb = b.decode_ragged(tok, k)
+        assert torch.equal(la, lb) and torch.equal(ga, gb)
+        tok = ga
+    assert b.lengths(B) == [T + 3] * B
+    a.close()
+    b.close()
+
+
+def test_ragged_refusals(dev):
+    shape = synth.TINY
+    m = dev.Model(shape, synth.make_weights(shape), max_batch=2, max_ctx=16, max_chunk=8)
+    L = dev.lib()
+    m.prefill_slot(1, _tok(synth.tokens(shape, 1, 4)[0]), 1)
+    assert m.lengths(2) == [0, 4]
+    with pytest.raises(dev.DoryError):                 # uniform calls in the ragged state
+        m.decode(_tok(np.array([1, 2], np.int32)), 1)
+    with pytest.raises(dev.DoryError):
+        m.prefill(_tok(synth.tokens(shape, 2, 3)), 1)
+    with pytest.raises(dev.DoryError):                 # slot out of range
+        m.prefill_slot(2, _tok(np.array([1], np.int32)), 1)
+    with pytest.raises(dev.DoryError) as e:            # too long for the ring capacity
+        m.prefill_slot(1, _tok(synth.tokens(shape, 1, 13)[0]), 1)
+    assert e.value.code == dev.DORY_ECAPACITY
+    with pytest.raises(dev.DoryError):
+        m.set_lengths([3, 17])
+    assert m.lengths(2) == [0, 4]
+    m.set_length(2, 0)                                  # back to one shared length
+    m.prefill(_tok(synth.tokens(shape, 2, 3)), 1)
+    assert m.lengths(2) == [3, 3]
+    m.close()
