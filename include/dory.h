@@ -356,6 +356,16 @@ DORY_API int dory_prefill_slot(dory_t* m, int slot, const int32_t* tokens, int T
 DORY_API int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, int k,
                                      int cache_mode, float* logits, int32_t* next, void* stream);
 
+/* The same step with one loop count per sequence: ks (host int[B], each
+ * >= 1), last-loop cache only (else DORY_EKMISMATCH).  Sequence b runs the
+ * recurrent block ks[b] times, stores its key and value of each recurrent
+ * layer at its own last loop and enters the output block with s_(ks[b]),
+ * exactly as a step at k = ks[b] alone.  The recurrent block runs max(ks)
+ * times for the whole batch (rows past their count compute values that are
+ * discarded). */
+DORY_API int dory_decode_step_multi(dory_t* m, const int32_t* tokens, int B, const int* ks,
+                                    int cache_mode, float* logits, int32_t* next, void* stream);
+
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
 

@@ -110,6 +110,7 @@ _SIGS = {
     "dory_get_lengths": (_I, [_P, _I, ctypes.POINTER(_I)]),
     "dory_prefill_slot": (_I, [_P, _I, _P, _I, _I, _I, _P, _I, _P]),
     "dory_decode_step_ragged": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "dory_decode_step_multi": (_I, [_P, _P, _I, ctypes.POINTER(_I), _I, _P, _P, _P]),
     "dory_quant_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                               ctypes.POINTER(ctypes.c_size_t)]),
     "dory_quantize_matrix": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P]),
@@ -383,6 +384,23 @@ class Model:
             next_tokens = torch.empty((B,), dtype=torch.int32, device=self.device)
         _check("dory_decode_step_ragged", lib().dory_decode_step_ragged(
             self.handle, _ptr(tokens), B, k, mode, _ptr(logits), _ptr(next_tokens),
+            _stream_ptr(stream)))
+        return logits, next_tokens
+
+    def decode_multi(self, tokens, ks, cache_mode=None, logits=None, next_tokens=None,
+                     stream=None):
+        """One decode step of slots 0 .. B-1 at their own lengths and their
+        own loop counts ks (last-loop cache).  Returns (logits, next)."""
+        import torch
+        B = tokens.shape[0]
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        if logits is None:
+            logits = torch.empty((B, self.shape.vocab), dtype=torch.float32, device=self.device)
+        if next_tokens is None:
+            next_tokens = torch.empty((B,), dtype=torch.int32, device=self.device)
+        arr = (ctypes.c_int * B)(*[int(x) for x in ks])
+        _check("dory_decode_step_multi", lib().dory_decode_step_multi(
+            self.handle, _ptr(tokens), B, arr, mode, _ptr(logits), _ptr(next_tokens),
             _stream_ptr(stream)))
         return logits, next_tokens
 

@@ -586,6 +586,8 @@ struct DecAttnArgs {
   int P0, S, n_q, n_kv, window;   // P0: the position of every sequence's new token, or
                                   // (ragged batches) the largest one
   const int* p0s;                 // ragged batches: [B] each sequence's position (device), or null
+  const int* kstore;              // per-sequence loop counts: [B]; sequence b also stores
+  int loop;                       //   its key and value when kstore[b] == loop
   float scale_log2;
   int chunk, n_splits;
   int tpg;                        // TMA kernel: 64-key tiles per (sequence, kv head) group
@@ -745,7 +747,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
             float* dst = hh == G ? sKc : sVc;
             dst[i] = __bfloat162float(b1);
             dst[i + HALF] = __bfloat162float(b2);
-            if (a.store && split == 0) {
+            if ((a.store || (a.kstore && a.kstore[b] == a.loop)) && split == 0) {
               __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
               const long long off = (((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH;
               cache[off + i] = b1;
@@ -762,7 +764,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const DecAttnArgs a) {
             const __nv_bfloat16* src = hh == G ? a.k_cur : a.v_cur;
             const __nv_bfloat16 v = src[((long long)b * a.n_kv + kvh) * DH + i];
             (hh == G ? sKc : sVc)[i] = __bfloat162float(v);
-            if (a.store && split == 0) {
+            if ((a.store || (a.kstore && a.kstore[b] == a.loop)) && split == 0) {
               __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
               cache[(((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH + i] = v;
             }

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
             float* dst = hh == G ? sKc : sVc;
             dst[i] = __bfloat162float(b1);
             dst[i + HALF] = __bfloat162float(b2);
-            if (a.store && split == 0) {
+            if ((a.store || (a.kstore && a.kstore[b] == a.loop)) && split == 0) {
               __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
               const long long off = (((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH;
               cache[off + i] = b1;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kDecTmaThreads, 1)
             const __nv_bfloat16* src = hh == G ? a.k_cur : a.v_cur;
             const __nv_bfloat16 v = src[((long long)b * a.n_kv + kvh) * DH + i];
             (hh == G ? sKc : sVc)[i] = __bfloat162float(v);
-            if (a.store && split == 0) {
+            if ((a.store || (a.kstore && a.kstore[b] == a.loop)) && split == 0) {
               __nv_bfloat16* cache = hh == G ? a.k_cache : a.v_cache;
               cache[(((long long)b * a.n_kv + kvh) * a.S + (P0 % a.S)) * DH + i] = v;
             }

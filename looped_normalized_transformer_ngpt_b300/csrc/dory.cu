@@ -48,7 +48,7 @@ constexpr int kSwapMaxParts = 16;   // K splits of the swapped GEMM
 struct WsLayout {
   size_t status, h32, h32b, x32, hb, y32, q, k, v, g, att, m, rope_swa, rope_full, ropet_swa,
       ropet_full, gy, dec_o,
-      dec_ml, dec_cnt, parts, seq_pos, total;
+      dec_ml, dec_cnt, parts, seq_pos, seq_k, save32, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -90,6 +90,8 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.dec_ml = take((size_t)max_batch * c.n_q * kDecMaxSplits * 2 * 4);
   L.dec_cnt = take((size_t)max_batch * c.n_kv * 4);   // split tickets, zero between launches
   L.seq_pos = take((size_t)max_batch * 4);            // ragged decode: positions
+  L.seq_k = take((size_t)max_batch * 4);              //   and loop counts
+  L.save32 = take((size_t)max_batch * c.d * 4);       //   and finished rows' states
   // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
   if (max_batch > kGemvMaxM) {
     const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
@@ -822,6 +824,9 @@ struct dory_model {
   bool ragged = false;
   int slot = 0;
   bool ragged_step = false;
+  bool multi_k = false;      // the ragged step also has per-sequence loop counts
+  std::vector<int> step_k;   // those counts (host copy)
+  int step_loop = 0;         // recurrent loop being run (per-sequence KV stores)
   int batch = 0;       // batch of the current sequences (0 = none yet)
   int last_rows = 0;   // rows of the last processed chunk (B * C)
   int hsel_last = 0;   // hidden-state buffer holding the last step's final rows
@@ -1022,6 +1027,10 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
   if (m->ragged_step) {
     da.p0s = wsp<int>(m, m->L.seq_pos);
     da.tpg = ragged_tpg(m, B, da.window);
+    if (m->multi_k && m->step_loop > 0) {     // a recurrent layer: per-sequence stores
+      da.kstore = wsp<int>(m, m->L.seq_k);
+      da.loop = m->step_loop;
+    }
   }
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
@@ -1156,6 +1165,10 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
   if (m->ragged_step) {
     da.p0s = wsp<int>(m, m->L.seq_pos);
     da.tpg = ragged_tpg(m, B, da.window);
+    if (m->multi_k && m->step_loop > 0) {     // a recurrent layer: per-sequence stores
+      da.kstore = wsp<int>(m, m->L.seq_k);
+      da.loop = m->step_loop;
+    }
   }
   pb(m, DORY_K_ATTENTION, st);
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
@@ -1426,15 +1439,19 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
 
 // Loop-boundary kernel on the current hidden buffer; an owed nGPT step is
 // applied first inside the same kernel.
-int boundary(dory_model* m, int M, int mode, StepState& s, cudaStream_t st) {
+// With per-sequence loop counts, `loop` is the loop just finished: rows
+// whose count it is keep their final state (see boundary_kernel).
+int boundary(dory_model* m, int M, int mode, StepState& s, cudaStream_t st, int loop = 0) {
   const float* y = s.pend ? wsp<float>(m, m->L.y32) : nullptr;
   const float* al = s.pend;
   s.pend = nullptr;
+  const bool mk = m->multi_k && (mode == BND_ENTER_NEXT || mode == BND_EXIT);
   pb(m, DORY_K_BOUNDARY, st);
   return pe(m, st,
             launch_k(boundary_kernel, dim3(M), dim3(kRowThreads), 0, st, hbuf(m, s.hsel),
                      wsp<__nv_bfloat16>(m, m->L.hb), wsp<float>(m, m->L.x32), m->cfg.d, mode, y, 1,
-                     (long long)0, al) == cudaSuccess
+                     (long long)0, al, mk ? (const int*)wsp<int>(m, m->L.seq_k) : nullptr, loop,
+                     wsp<float>(m, m->L.save32)) == cudaSuccess
                 ? DORY_OK
                 : DORY_ECUDA);
 }
@@ -1473,7 +1490,10 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   if (m->ragged_step) {
     // each sequence's position: RoPE rows and the positions for the attention
     SeqPos sp{};
-    for (int b = 0; b < B; ++b) sp.p[b] = m->seq_len[b];
+    for (int b = 0; b < B; ++b) {
+      sp.p[b] = m->seq_len[b];
+      sp.k[b] = m->multi_k ? m->step_k[b] : 0;
+    }
     const int n = 2 * B * (c.head_dim / 2);
     pb(m, DORY_K_ROPE, st);
     DORY_TRY(pe(m, st,
@@ -1481,7 +1501,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
                          c.rope ? wsp<float2>(m, m->L.rope_swa) : nullptr,
                          c.rope ? wsp<float2>(m, m->L.rope_full) : nullptr, sp, B, c.head_dim,
                          (double)c.rope_base_swa, (double)c.rope_base_full,
-                         wsp<int>(m, m->L.seq_pos)) == cudaSuccess
+                         wsp<int>(m, m->L.seq_pos),
+                         m->multi_k ? wsp<int>(m, m->L.seq_k) : nullptr) == cudaSuccess
                     ? DORY_OK
                     : DORY_ECUDA));
   } else if (c.rope) {
@@ -1513,14 +1534,19 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   };
   for (int l = 0; l < c.n_in; ++l) DORY_TRY(layer(l, 0, true));
   if (c.n_rec > 0) {
+    // per-sequence loop counts (last-loop cache): k is the largest; a
+    // sequence stores its keys and values at its own last loop and keeps its
+    // final state from there to the output block
     const bool per_loop = m->cache_mode == DORY_CACHE_PER_LOOP;
     for (int i = 1; i <= k; ++i) {
-      DORY_TRY(boundary(m, M, i == 1 ? BND_SAVE_ENTER : BND_ENTER_NEXT, s, st));
+      DORY_TRY(boundary(m, M, i == 1 ? BND_SAVE_ENTER : BND_ENTER_NEXT, s, st, i - 1));
       const int slice = per_loop ? i - 1 : 0;
-      const bool store = per_loop || i == k;
+      const bool store = per_loop || (i == k && !m->multi_k);
+      m->step_loop = i;
       for (int l = c.n_in; l < c.n_in + c.n_rec; ++l) DORY_TRY(layer(l, slice, store));
     }
-    DORY_TRY(boundary(m, M, BND_EXIT, s, st));
+    m->step_loop = 0;
+    DORY_TRY(boundary(m, M, BND_EXIT, s, st, k));
   }
   for (int l = c.n_in + c.n_rec; l < n_layers(c); ++l) DORY_TRY(layer(l, 0, true));
   DORY_TRY(flush_pending(m, s, M, st));
@@ -1600,6 +1626,55 @@ int check_call(dory_model* m, int B, int n_new, int k, int cache_mode) {
 
 int dory_prefill_body(dory_t* m, const int32_t* tokens, int B, int T, int k, float* logits,
                       int all_logits, void* stream);
+
+// One decode step of batch slots 0 .. B-1 at their own lengths, with one
+// loop count k for all or (ks, host array, last-loop cache) one per
+// sequence, k then being the largest.
+int ragged_decode(dory_model* m, const int32_t* tokens, int B, int k, const int* ks,
+                  int cache_mode, float* logits, int32_t* next, void* stream) {
+  if (!m || !tokens) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (B <= 0) return DORY_EINVAL;
+  if (B > kRaggedMax) return DORY_EUNSUPPORTED;
+  if (next && !logits) return DORY_EINVAL;
+  if (B > m->max_batch) return DORY_ECAPACITY;
+  if (!m->ragged) {
+    for (int b = 0; b < m->max_batch; ++b) m->seq_len[b] = b < m->batch ? m->len : 0;
+    m->ragged = true;
+  }
+  int pmax = 0;
+  for (int b = 0; b < B; ++b) {
+    if (m->seq_len[b] + 1 > m->max_ctx) return DORY_ECAPACITY;
+    if (m->seq_len[b] > pmax) pmax = m->seq_len[b];
+  }
+  const int saved_len = m->len, saved_batch = m->batch;
+  m->len = pmax;                        // the step's largest position (schedules)
+  m->batch = 0;
+  int rc = check_call(m, B, 1, k, cache_mode);
+  if (rc == DORY_OK) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    m->launches = 0;
+    m->ragged_step = true;
+    m->multi_k = ks != nullptr;
+    if (ks) m->step_k.assign(ks, ks + B);
+    rc = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st, next);
+    m->ragged_step = false;
+    m->multi_k = false;
+    if (rc == DORY_OK && next && !m->next_done) {
+      pb(m, DORY_K_ARGMAX, st);
+      rc = pe(m, st,
+              launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits,
+                       m->cfg.vocab, next) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA);
+    }
+    if (rc == DORY_OK)
+      for (int b = 0; b < B; ++b) m->seq_len[b] += 1;
+  }
+  m->len = saved_len;
+  m->batch = saved_batch > B ? saved_batch : B;
+  return rc;
+}
 
 }  // namespace
 
@@ -2190,45 +2265,19 @@ int dory_prefill_slot(dory_t* m, int slot, const int32_t* tokens, int T, int k, 
 
 int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                             float* logits, int32_t* next, void* stream) {
-  if (!m || !tokens) return DORY_EINVAL;
-  if (!m->bound) return DORY_EUNBOUND;
-  if (B <= 0) return DORY_EINVAL;
-  if (B > kRaggedMax) return DORY_EUNSUPPORTED;
-  if (next && !logits) return DORY_EINVAL;
-  if (B > m->max_batch) return DORY_ECAPACITY;
-  if (!m->ragged) {
-    for (int b = 0; b < m->max_batch; ++b) m->seq_len[b] = b < m->batch ? m->len : 0;
-    m->ragged = true;
+  return ragged_decode(m, tokens, B, k, nullptr, cache_mode, logits, next, stream);
+}
+
+int dory_decode_step_multi(dory_t* m, const int32_t* tokens, int B, const int* ks,
+                           int cache_mode, float* logits, int32_t* next, void* stream) {
+  if (!ks) return DORY_EINVAL;
+  if (m && m->bound && cache_mode != DORY_CACHE_LAST_LOOP) return DORY_EKMISMATCH;
+  int kmax = 0;
+  for (int b = 0; b < B && B <= kRaggedMax; ++b) {
+    if (ks[b] < 1) return DORY_EINVAL;
+    if (ks[b] > kmax) kmax = ks[b];
   }
-  int pmax = 0;
-  for (int b = 0; b < B; ++b) {
-    if (m->seq_len[b] + 1 > m->max_ctx) return DORY_ECAPACITY;
-    if (m->seq_len[b] > pmax) pmax = m->seq_len[b];
-  }
-  const int saved_len = m->len, saved_batch = m->batch;
-  m->len = pmax;                        // the step's largest position (schedules)
-  m->batch = 0;
-  int rc = check_call(m, B, 1, k, cache_mode);
-  if (rc == DORY_OK) {
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    m->launches = 0;
-    m->ragged_step = true;
-    rc = run_step(m, tokens, 1, B, 1, k, logits, 1, 0, logits ? 1 : 0, st, next);
-    m->ragged_step = false;
-    if (rc == DORY_OK && next && !m->next_done) {
-      pb(m, DORY_K_ARGMAX, st);
-      rc = pe(m, st,
-              launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, (const float*)logits,
-                       m->cfg.vocab, next) == cudaSuccess
-                  ? DORY_OK
-                  : DORY_ECUDA);
-    }
-    if (rc == DORY_OK)
-      for (int b = 0; b < B; ++b) m->seq_len[b] += 1;
-  }
-  m->len = saved_len;
-  m->batch = saved_batch > B ? saved_batch : B;
-  return rc;
+  return ragged_decode(m, tokens, B, kmax, ks, cache_mode, logits, next, stream);
 }
 
 int dory_destroy(dory_t* m) {

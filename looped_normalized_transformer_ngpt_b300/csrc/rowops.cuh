@@ -200,11 +200,17 @@ enum BoundaryMode : int {
 // With y != null the row is first moved by the pending nGPT step of the last
 // sublayer, h <- N(h + alpha * (N(y) - h)), y being that sublayer's
 // projection output (n_parts partial sums part_stride apart).
+// Per-sequence loop counts (kb != null, one row per sequence): at the
+// boundary after loop `loop` a row whose count is `loop` saves its final
+// state s into save (BND_ENTER_NEXT), and at the exit after the last loop a
+// row whose count is below `loop` takes its saved state back (BND_EXIT), so
+// the output block sees every row's s_(k_b).
 __global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_bfloat16* hb,
                                                                float* x32, int d, int mode,
                                                                const float* y, int n_parts,
                                                                long long part_stride,
-                                                               const float* alpha) {
+                                                               const float* alpha, const int* kb,
+                                                               int loop, float* save) {
   __shared__ float red[4];
   pdl_wait();
   pdl_trigger();
@@ -290,6 +296,19 @@ __global__ void __launch_bounds__(kRowThreads) boundary_kernel(float* h32, __nv_
     for (int j = 0; j < kRowMaxChunks; ++j)
 #pragma unroll
       for (int i = 0; i < 8; ++i) hv[j][i] *= inv;
+    if (kb) {
+      const int krow = kb[row];
+      const bool keep = mode == BND_ENTER_NEXT && krow == loop;
+      const bool take = mode == BND_EXIT && krow != loop;
+#pragma unroll
+      for (int j = 0; j < kRowMaxChunks; ++j) {
+        const int ch = threadIdx.x + j * kRowThreads;
+        if (ch < nch) {
+          if (keep) store8(save + row * d + ch * 8, hv[j]);
+          if (take) load8(save + row * d + ch * 8, hv[j]);
+        }
+      }
+    }
   }
   if (mode != BND_EXIT) {
     float ss = 0.f;
@@ -375,20 +394,25 @@ __global__ void rope_table_kernel(float2* tab0, float2* tab1, float2* tabt0, flo
 // carried in the launch parameters).
 constexpr int kRaggedMax = 128;
 struct SeqPos {
-  int p[kRaggedMax];
+  int p[kRaggedMax];       // positions
+  int k[kRaggedMax];       // loop counts (per-sequence loop counts only)
 };
 
 // RoPE (cos, sin) rows of B sequences at their own positions (tab0: base0,
 // tab1: base1, [B][dh / 2]; null tables when RoPE is off) and the positions
 // themselves into pos_out [B] for the decode attention.
 __global__ void rope_rows_kernel(float2* tab0, float2* tab1, const __grid_constant__ SeqPos sp,
-                                 int B, int dh, double base0, double base1, int* pos_out) {
+                                 int B, int dh, double base0, double base1, int* pos_out,
+                                 int* k_out) {
   pdl_wait();
   pdl_trigger();
   const int half = dh / 2;
   const long long n = (long long)B * half;
   if (blockIdx.x == 0)
-    for (int b = threadIdx.x; b < B; b += blockDim.x) pos_out[b] = sp.p[b];
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      pos_out[b] = sp.p[b];
+      if (k_out) k_out[b] = sp.k[b];
+    }
   if (!tab0) return;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < 2 * n;
        idx += (long long)gridDim.x * blockDim.x) {

@@ -26,17 +26,19 @@ def dev(cuda_ok):
     return dory
 
 
-def _run(dev, shape, w, lens, mode, k, steps, max_ctx, extend=None, seed=0):
+def _run(dev, shape, w, lens, mode, k, steps, max_ctx, extend=None, seed=0, ks=None):
+    """ks: one loop count per sequence (last-loop cache), else k for all."""
     B = len(lens)
+    ks = list(ks) if ks is not None else [k] * B
     dt = np.float64 if shape.d <= 256 else np.float32
-    m = dev.Model(shape, w, max_batch=B + 1, max_ctx=max_ctx, max_chunk=max(lens), k_max=k,
-                  cache_mode=mode)
+    m = dev.Model(shape, w, max_batch=B + 1, max_ctx=max_ctx, max_chunk=max(lens),
+                  k_max=max(ks), cache_mode=mode)
     oracles, nxt = [], []
     for b, T in enumerate(lens):
         prompt = synth.tokens(shape, 1, T, seed=seed + b)
         o = oracle.Oracle(shape, w, dtype=dt)
-        z = o.prefill(prompt, k, mode)["logits"][0, -1]
-        lg = m.prefill_slot(b, _tok(prompt[0]), k, mode).cpu().numpy()
+        z = o.prefill(prompt, ks[b], mode)["logits"][0, -1]
+        lg = m.prefill_slot(b, _tok(prompt[0]), ks[b], mode).cpu().numpy()
         check_logits(lg, z)
         oracles.append(o)
         nxt.append(int(np.argmax(z)))
@@ -47,14 +49,17 @@ def _run(dev, shape, w, lens, mode, k, steps, max_ctx, extend=None, seed=0):
             # continuous batching: one slot takes more prompt tokens mid-stream
             b, n = extend[1], extend[2]
             more = synth.tokens(shape, 1, n, seed=seed + 100)
-            z = oracles[b].prefill(more, k, mode)["logits"][0, -1]
-            lg = m.prefill_slot(b, _tok(more[0]), k, mode).cpu().numpy()
+            z = oracles[b].prefill(more, ks[b], mode)["logits"][0, -1]
+            lg = m.prefill_slot(b, _tok(more[0]), ks[b], mode).cpu().numpy()
             check_logits(lg, z)
             cur[b] = int(np.argmax(z))
-        lg, g = m.decode_ragged(_tok(cur), k, mode)
+        if len(set(ks)) == 1:
+            lg, g = m.decode_ragged(_tok(cur), k, mode)
+        else:
+            lg, g = m.decode_multi(_tok(cur), ks, mode)
         lg, g, hid = lg.cpu().numpy(), g.cpu().numpy(), m.hidden(B).cpu().numpy()
         for b, o in enumerate(oracles):
-            r = o.decode(cur[b:b + 1], k, mode)
+            r = o.decode(cur[b:b + 1], ks[b], mode)
             check_logits(lg[b:b + 1], r["logits"])
             check_hidden(hid[b:b + 1], r["hidden"])
             check_greedy(g[b:b + 1], r["logits"])
@@ -79,6 +84,39 @@ def test_ragged_4b_width_windowed(dev, mode):
     shape = synth.DORY4B_SLIM.replace(window=128)
     _run(dev, shape, synth.make_weights(shape), [70, 200, 131], mode, 2, steps=3, max_ctx=384,
          extend=(1, 2, 9), seed=30 + mode)
+
+
+def test_per_sequence_loop_counts_tiny(dev):
+    """Each sequence at its own loop count in one decode step (last-loop
+    cache): as the same sequence decoded alone at that count."""
+    shape = synth.TINY_LOOPFULL
+    _run(dev, shape, synth.make_weights(shape), [5, 23, 12, 9], oracle.LAST_LOOP, 0, steps=4,
+         max_ctx=64, extend=(2, 1, 6), seed=77, ks=[1, 3, 2, 4])
+
+
+def test_per_sequence_loop_counts_4b_width(dev):
+    shape = synth.DORY4B_SLIM.replace(window=128)
+    _run(dev, shape, synth.make_weights(shape), [70, 200, 131], oracle.LAST_LOOP, 0, steps=3,
+         max_ctx=384, seed=88, ks=[2, 4, 1])
+
+
+def test_equal_loop_counts_match_ragged_bitwise(dev):
+    import torch
+    shape = synth.DORY4B_SLIM
+    w = synth.make_weights(shape)
+    B, k = 3, 2
+    ms = [dev.Model(shape, w, max_batch=B, max_ctx=192, max_chunk=64, k_max=k) for _ in range(2)]
+    for m in ms:
+        for b, T in enumerate([20, 64, 41]):
+            m.prefill_slot(b, _tok(synth.tokens(shape, 1, T, seed=b)[0]), k)
+    tok = _tok(np.array([3, 1000, 77], np.int32))
+    for _ in range(2):
+        la, ga = ms[0].decode_ragged(tok, k)
+        lb, gb = ms[1].decode_multi(tok, [k] * B)
+        assert torch.equal(la, lb) and torch.equal(ga, gb)
+        tok = ga
+    for m in ms:
+        m.close()
 
 
 def test_ragged_equal_lengths_match_uniform_bitwise(dev):
@@ -119,6 +157,8 @@ def test_ragged_refusals(dev):
     assert e.value.code == dev.DORY_ECAPACITY
     with pytest.raises(dev.DoryError):
         m.set_lengths([3, 17])
+    with pytest.raises(dev.DoryError):                 # a loop count below 1
+        m.decode_multi(_tok(np.array([1, 2], np.int32)), [1, 0])
     assert m.lengths(2) == [0, 4]
     m.set_length(2, 0)                                  # back to one shared length
     m.prefill(_tok(synth.tokens(shape, 2, 3)), 1)
