@@ -366,6 +366,20 @@ DORY_API int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, in
 DORY_API int dory_decode_step_multi(dory_t* m, const int32_t* tokens, int B, const int* ks,
                                     int cache_mode, float* logits, int32_t* next, void* stream);
 
+/* A mixed step: one forward pass over Bd decode rows (batch slots 0 ..
+ * Bd-1, one token each at its own length) and a chunk of C tokens of the
+ * sequence in batch slot `slot` (slot >= Bd, continuing from its own
+ * length), so that the decode tokens and the chunk share every weight read
+ * (chunked prefill piggybacking on decode).  tokens: device int32 [Bd + C],
+ * the decode tokens then the chunk.  logits (may be NULL): device fp32
+ * [Bd + 1][V], the decode rows then the chunk's last position; next (may be
+ * NULL, needs logits and Bd >= 1): greedy tokens of the decode rows [Bd].
+ * One loop count k; the cache mode's rules as for dory_prefill.  Lengths
+ * grow by 1 (decode slots) and C (the chunk's slot).  Every row computes
+ * what it computes alone.  Requires C <= max_chunk. */
+DORY_API int dory_step_mixed(dory_t* m, const int32_t* tokens, int Bd, int slot, int C, int k,
+                             int cache_mode, float* logits, int32_t* next, void* stream);
+
 /* Current length of the sequences (host state; no CUDA call). */
 DORY_API int dory_length(const dory_t* m, int* out);
 

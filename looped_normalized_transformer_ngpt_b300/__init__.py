@@ -111,6 +111,7 @@ _SIGS = {
     "dory_prefill_slot": (_I, [_P, _I, _P, _I, _I, _I, _P, _I, _P]),
     "dory_decode_step_ragged": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "dory_decode_step_multi": (_I, [_P, _P, _I, ctypes.POINTER(_I), _I, _P, _P, _P]),
+    "dory_step_mixed": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "dory_quant_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                               ctypes.POINTER(ctypes.c_size_t)]),
     "dory_quantize_matrix": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P]),
@@ -403,6 +404,22 @@ class Model:
             self.handle, _ptr(tokens), B, arr, mode, _ptr(logits), _ptr(next_tokens),
             _stream_ptr(stream)))
         return logits, next_tokens
+
+    def step_mixed(self, dec_tokens, slot, chunk, k, cache_mode=None, stream=None):
+        """One forward pass over decode tokens of slots 0 .. Bd-1 (int32
+        device [Bd]) and a chunk (int32 device [C]) of the sequence in slot
+        `slot`.  Returns (logits [Bd + 1, V]: decode rows then the chunk's
+        last position, greedy next tokens [Bd] or None)."""
+        import torch
+        Bd, C = dec_tokens.shape[0], chunk.shape[0]
+        mode = self.cache_mode if cache_mode is None else cache_mode
+        toks = torch.cat([dec_tokens, chunk]).to(torch.int32).contiguous()
+        logits = torch.empty((Bd + 1, self.shape.vocab), dtype=torch.float32, device=self.device)
+        nxt = torch.empty((max(Bd, 1),), dtype=torch.int32, device=self.device)
+        _check("dory_step_mixed", lib().dory_step_mixed(
+            self.handle, _ptr(toks), Bd, slot, C, k, mode, _ptr(logits),
+            _ptr(nxt) if Bd > 0 else None, _stream_ptr(stream)))
+        return logits, (nxt[:Bd] if Bd > 0 else None)
 
     def copy_prefix(self, src, dst, length, stream=None):
         """Copy the cached positions 0 .. length-1 of sequence src into the

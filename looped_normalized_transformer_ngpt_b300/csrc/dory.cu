@@ -75,12 +75,13 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.g = take(M * hq * 2);
   L.att = take(M * hq * 2);
   L.m = take(M * (size_t)c.ffn * 2);
-  // RoPE rows: the call's positions, or (ragged decode) each sequence's
-  const size_t rope_rows = max_chunk > max_batch ? max_chunk : max_batch;
+  // RoPE rows: the call's positions, (ragged decode) each sequence's, or (a
+  // mixed step) decode rows followed by a chunk
+  const size_t rope_rows = (size_t)max_chunk + max_batch;
   L.rope_swa = take(rope_rows * (c.head_dim / 2) * 8);
   L.rope_full = take(rope_rows * (c.head_dim / 2) * 8);
-  L.ropet_swa = take((size_t)max_chunk * (c.head_dim / 2) * 8);    // transposed copies
-  L.ropet_full = take((size_t)max_chunk * (c.head_dim / 2) * 8);
+  L.ropet_swa = take(rope_rows * (c.head_dim / 2) * 8);    // transposed copies
+  L.ropet_full = take(rope_rows * (c.head_dim / 2) * 8);
   // few-row projections (decode): fp32 output of the QKV+gate / up+gate GEMV
   const size_t nq = (size_t)(2 * c.n_q + 2 * c.n_kv) * c.head_dim;
   const size_t wide = nq > 2 * (size_t)c.ffn ? nq : 2 * (size_t)c.ffn;
@@ -825,6 +826,10 @@ struct dory_model {
   int slot = 0;
   bool ragged_step = false;
   bool multi_k = false;      // the ragged step also has per-sequence loop counts
+  // a mixed step: mix_bd decode rows (slots 0 .. mix_bd-1) followed by a
+  // chunk of one sequence in slot mix_slot at position mix_p
+  bool mixed_step = false;
+  int mix_bd = 0, mix_slot = 0, mix_p = 0;
   std::vector<int> step_k;   // those counts (host copy)
   int step_loop = 0;         // recurrent loop being run (per-sequence KV stores)
   int batch = 0;       // batch of the current sequences (0 = none yet)
@@ -1263,8 +1268,82 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
   __nv_bfloat16* kc = kv_block(m, l, slice, 0);
   __nv_bfloat16* vc = kv_block(m, l, slice, 1);
   __nv_bfloat16* att = wsp<__nv_bfloat16>(m, m->L.att);
-  pb(m, DORY_K_ATTENTION, st);
-  if (C == 1) {
+  if (m->mixed_step) {
+    // a mixed step: the first mix_bd rows decode one token each in slots
+    // 0 .. mix_bd-1 at their own positions (split-key kernel, KV write
+    // fused); the remaining rows are one chunk of the sequence in slot
+    // mix_slot (multi-token kernel on that slot's blocks, then its KV write)
+    const int Bd = m->mix_bd, Cc = M - Bd;
+    const size_t hk = (size_t)c.n_kv * c.head_dim;
+    if (Bd > 0) {
+      DecAttnArgs da{};
+      da.q = ga.q;
+      da.k_cur = ga.k;
+      da.v_cur = ga.v;
+      da.gate = ga.g;
+      da.k_cache = kc;
+      da.v_cache = vc;
+      da.store = store ? 1 : 0;
+      int pmax = 0;
+      for (int b = 0; b < Bd; ++b) pmax = m->seq_len[b] > pmax ? m->seq_len[b] : pmax;
+      da.P0 = pmax;
+      da.p0s = wsp<int>(m, m->L.seq_pos);
+      da.tpg = ragged_tpg(m, Bd, full ? 0 : c.window);
+      da.S = S;
+      da.n_q = c.n_q;
+      da.n_kv = c.n_kv;
+      da.window = full ? 0 : c.window;
+      da.scale_log2 = attn_scale_log2(c);
+      da.part_o = wsp<float>(m, m->L.dec_o);
+      da.part_ml = wsp<float>(m, m->L.dec_ml);
+      da.counter = wsp<int>(m, m->L.dec_cnt);
+      da.out = att;
+      da.cache_rows = cache_rows(m, S);
+      da.status = status;
+      pb(m, DORY_K_ATTENTION, st);
+      DORY_TRY(pe(m, st, dec_attn<false>(da, Bd, c.head_dim, st)));
+    }
+    const size_t so = (size_t)m->mix_slot * c.n_kv * S * c.head_dim;
+    AttnArgs aa{};
+    aa.q = ga.q + (size_t)Bd * hq;
+    aa.k_cur = ga.k + Bd * hk;
+    aa.v_cur = ga.v + Bd * hk;
+    aa.k_cache = kc + so;
+    aa.v_cache = vc + so;
+    aa.gate = ga.g + (size_t)Bd * hq;
+    aa.out = att + (size_t)Bd * hq;
+    aa.C = Cc;
+    aa.P0 = m->mix_p;
+    aa.S = S;
+    aa.n_q = c.n_q;
+    aa.n_kv = c.n_kv;
+    aa.window = full ? 0 : c.window;
+    aa.scale_log2 = attn_scale_log2(c);
+    aa.part_o = wsp<float>(m, m->L.dec_o);
+    aa.part_ml = wsp<float>(m, m->L.dec_ml);
+    aa.part_cap = (int)((long long)kDecMaxSplits * m->max_batch / Cc);
+    const long long rows_c = (long long)(m->max_batch - m->mix_slot) * c.n_kv * S;
+    pb(m, DORY_K_ATTENTION, st);
+    int arc = m->use_tc_attn ? launch_attn_tc(aa, 1, c.head_dim, rows_c, status, st)
+                             : DORY_EUNSUPPORTED;
+    if (arc == DORY_EUNSUPPORTED) {
+      if (c.head_dim == 32) arc = launch_attn<32>(aa, 1, st);
+      if (c.head_dim == 64) arc = launch_attn<64>(aa, 1, st);
+      if (c.head_dim == 128) arc = launch_attn<128>(aa, 1, st);
+    }
+    DORY_TRY(pe(m, st, arc));
+    if (store) {
+      const int t_first = Cc > S ? Cc - S : 0;
+      pb(m, DORY_K_KV_WRITE, st);
+      DORY_TRY(pe(m, st,
+                  launch_k(kv_write_kernel, dim3(Cc - t_first, 1), dim3(128), 0, st, aa.k_cur,
+                           aa.v_cur, kc + so, vc + so, Cc, m->mix_p, S, t_first, c.n_kv,
+                           c.head_dim) == cudaSuccess
+                      ? DORY_OK
+                      : DORY_ECUDA));
+    }
+  } else if (C == 1) {
+    pb(m, DORY_K_ATTENTION, st);
     // one token per sequence: split-key kernel, KV write fused
     DecAttnArgs da{};
     da.q = ga.q;
@@ -1288,6 +1367,7 @@ int run_layer(dory_model* m, int l, int slice, bool store, int B, int C, int P0,
     da.status = status;
     DORY_TRY(pe(m, st, dec_attn<false>(da, B, c.head_dim, st)));
   } else {
+    pb(m, DORY_K_ATTENTION, st);
     AttnArgs aa{};
     aa.q = ga.q;
     aa.k_cur = ga.k;
@@ -1467,8 +1547,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   const int M = B * C;
   const int P0 = m->len;
   int* status = wsp<int>(m, m->L.status);
-  const bool decode = C == 1 && M <= kGemvMaxM;
-  const bool batched = C == 1 && M > kGemvMaxM && M <= kSwapMaxM;
+  const bool decode = !m->mixed_step && C == 1 && M <= kGemvMaxM;
+  const bool batched = !m->mixed_step && C == 1 && M > kGemvMaxM && M <= kSwapMaxM;
 
   CUtensorMap tm_hb, tm_att, tm_m;
   const int hq = c.n_q * c.head_dim;
@@ -1487,7 +1567,21 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
       !encode_f32_out(&em.out, m->ws + m->L.y32, M, c.d, c.d))   // output / down projections
     return DORY_ECUDA;
 
-  if (m->ragged_step) {
+  if (m->mixed_step) {
+    SeqPos sp{};
+    for (int b = 0; b < m->mix_bd; ++b) sp.p[b] = m->seq_len[b];
+    const int n = 2 * M * (c.head_dim / 2);
+    pb(m, DORY_K_ROPE, st);
+    DORY_TRY(pe(m, st,
+                launch_k(rope_mixed_kernel, dim3((n + 255) / 256), dim3(256), 0, st,
+                         c.rope ? wsp<float2>(m, m->L.rope_swa) : nullptr,
+                         c.rope ? wsp<float2>(m, m->L.rope_full) : nullptr,
+                         wsp<float2>(m, m->L.ropet_swa), wsp<float2>(m, m->L.ropet_full), sp,
+                         m->mix_bd, m->mix_p, M - m->mix_bd, c.head_dim, (double)c.rope_base_swa,
+                         (double)c.rope_base_full, wsp<int>(m, m->L.seq_pos)) == cudaSuccess
+                    ? DORY_OK
+                    : DORY_ECUDA));
+  } else if (m->ragged_step) {
     // each sequence's position: RoPE rows and the positions for the attention
     SeqPos sp{};
     for (int b = 0; b < B; ++b) {
@@ -1626,6 +1720,43 @@ int check_call(dory_model* m, int B, int n_new, int k, int cache_mode) {
 
 int dory_prefill_body(dory_t* m, const int32_t* tokens, int B, int T, int k, float* logits,
                       int all_logits, void* stream);
+
+// Logits of n consecutive rows of the last step's final hidden states (bf16
+// copy), from row row0, into out [n][vocab] (s_z applied).
+int lm_head_rows(dory_model* m, int row0, int n, float* out, cudaStream_t st) {
+  const dory_config& c = m->cfg;
+  if (n <= kGemvMaxM) {
+    GemvArgs g{};
+    g.M = n;
+    g.X = wsp<__nv_bfloat16>(m, m->L.hb) + (size_t)row0 * c.d;
+    g.ldx = c.d;
+    g.W = static_cast<const __nv_bfloat16*>(m->embed_out);
+    g.N = c.vocab;
+    g.K = c.d;
+    g.Y = out;
+    g.ldy = c.vocab;
+    g.col_scale = m->s_z;
+    pb(m, DORY_K_LM_HEAD, st);
+    return pe(m, st, launch_gemv(g, st, wsp<int>(m, m->L.status)));
+  }
+  CUtensorMap tm_rows;
+  if (!encode_bf16(&tm_rows, m->ws + m->L.hb + (size_t)row0 * c.d * 2, n, c.d, c.d, 128))
+    return DORY_ECUDA;
+  GemmArgs gl{};
+  gl.w_pre = 1;
+  gl.M = n;
+  gl.N = c.vocab;
+  gl.K = c.d;
+  gl.status = wsp<int>(m, m->L.status);
+  gl.col_scale = m->s_z;
+  gl.ldo = c.vocab;
+  gl.out = out;
+  EpiMaps el;
+  const bool st_ok = encode_f32_out(&el.out, out, n, c.vocab, c.vocab);
+  pb(m, DORY_K_LM_HEAD, st);
+  return pe(m, st, launch_gemm<kGemmBN, EPI_F32>(tm_rows, m->tm_embed_out, gl, st,
+                                                 st_ok ? &el : nullptr));
+}
 
 // One decode step of batch slots 0 .. B-1 at their own lengths, with one
 // loop count k for all or (ks, host array, last-loop cache) one per
@@ -2266,6 +2397,55 @@ int dory_prefill_slot(dory_t* m, int slot, const int32_t* tokens, int T, int k, 
 int dory_decode_step_ragged(dory_t* m, const int32_t* tokens, int B, int k, int cache_mode,
                             float* logits, int32_t* next, void* stream) {
   return ragged_decode(m, tokens, B, k, nullptr, cache_mode, logits, next, stream);
+}
+
+int dory_step_mixed(dory_t* m, const int32_t* tokens, int Bd, int slot, int C, int k,
+                    int cache_mode, float* logits, int32_t* next, void* stream) {
+  if (!m || !tokens) return DORY_EINVAL;
+  if (!m->bound) return DORY_EUNBOUND;
+  if (Bd < 0 || C < 1 || slot < Bd || slot >= m->max_batch) return DORY_EINVAL;
+  if (Bd > kRaggedMax) return DORY_EUNSUPPORTED;
+  if (next && (!logits || Bd == 0)) return DORY_EINVAL;
+  if (C > m->max_chunk) return DORY_ECAPACITY;
+  if (!m->ragged) {
+    for (int b = 0; b < m->max_batch; ++b) m->seq_len[b] = b < m->batch ? m->len : 0;
+    m->ragged = true;
+  }
+  for (int b = 0; b < Bd; ++b)
+    if (m->seq_len[b] + 1 > m->max_ctx) return DORY_ECAPACITY;
+  const int saved_len = m->len, saved_batch = m->batch;
+  m->len = m->seq_len[slot];
+  m->batch = 0;
+  int rc = check_call(m, 1, C, k, cache_mode);
+  if (rc == DORY_OK) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int M = Bd + C;
+    m->launches = 0;
+    m->mixed_step = true;
+    m->mix_bd = Bd;
+    m->mix_slot = slot;
+    m->mix_p = m->seq_len[slot];
+    rc = run_step(m, tokens, M, 1, M, k, nullptr, 1, 0, 0, st);
+    m->mixed_step = false;
+    if (rc == DORY_OK && logits && Bd > 0) rc = lm_head_rows(m, 0, Bd, logits, st);
+    if (rc == DORY_OK && logits)
+      rc = lm_head_rows(m, M - 1, 1, logits + (size_t)Bd * m->cfg.vocab, st);
+    if (rc == DORY_OK && next) {
+      pb(m, DORY_K_ARGMAX, st);
+      rc = pe(m, st,
+              launch_k(argmax_kernel, dim3(Bd), dim3(1024), 0, st, (const float*)logits,
+                       m->cfg.vocab, next) == cudaSuccess
+                  ? DORY_OK
+                  : DORY_ECUDA);
+    }
+    if (rc == DORY_OK) {
+      for (int b = 0; b < Bd; ++b) m->seq_len[b] += 1;
+      m->seq_len[slot] += C;
+    }
+  }
+  m->len = saved_len;
+  m->batch = saved_batch > slot + 1 ? saved_batch : slot + 1;
+  return rc;
 }
 
 int dory_decode_step_multi(dory_t* m, const int32_t* tokens, int B, const int* ks,

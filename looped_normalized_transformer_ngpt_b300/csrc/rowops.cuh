@@ -429,6 +429,38 @@ __global__ void rope_rows_kernel(float2* tab0, float2* tab1, const __grid_consta
   }
 }
 
+// Mixed steps: RoPE rows for Bd decode rows at sp.p[r] followed by C rows of
+// one chunk at positions p_chunk + t, in both layouts of rope_table_kernel
+// (the call's rows counted as M = Bd + C), and the decode rows' positions
+// into pos_out.
+__global__ void rope_mixed_kernel(float2* tab0, float2* tab1, float2* tabt0, float2* tabt1,
+                                  const __grid_constant__ SeqPos sp, int Bd, int p_chunk, int C,
+                                  int dh, double base0, double base1, int* pos_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int half = dh / 2, M = Bd + C;
+  const long long n = (long long)M * half;
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b < Bd; b += blockDim.x) pos_out[b] = sp.p[b];
+  if (!tab0) return;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < 2 * n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int which = idx >= n;
+    const long long e = idx - which * n;
+    const int r = (int)(e / half), i = (int)(e % half);
+    const int pos = r < Bd ? sp.p[r] : p_chunk + (r - Bd);
+    const double inv_freq = pow(which ? base1 : base0, -2.0 * i / dh);
+    double ang = (double)pos * inv_freq;
+    const double two_pi = 6.283185307179586476925286766559;
+    ang -= floor(ang / two_pi) * two_pi;
+    double s, c;
+    sincos(ang, &s, &c);
+    const float2 cs = make_float2((float)c, (float)s);
+    (which ? tab1 : tab0)[e] = cs;
+    (which ? tabt1 : tabt0)[((long long)(i >> 1) * M + r) * 2 + (i & 1)] = cs;
+  }
+}
+
 // Greedy token per row: argmax of logits[row, 0..V), lowest index on ties.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* logits, int V, int32_t* next) {
   __shared__ float bv[32];

@@ -164,3 +164,66 @@ def test_ragged_refusals(dev):
     m.prefill(_tok(synth.tokens(shape, 2, 3)), 1)
     assert m.lengths(2) == [3, 3]
     m.close()
+
+
+def _run_mixed(dev, shape, w, lens, chunks, mode, k, max_ctx, seed):
+    """Slots 0 .. B-1 hold prompts of `lens`; slot B receives a new prompt
+    whose first chunk is prefilled alone and whose later chunks ride along
+    with one decode token of every other slot (dory_step_mixed).  Every row
+    against its own sequence's oracle; then one ragged decode of all slots."""
+    B = len(lens)
+    dt = np.float64 if shape.d <= 256 else np.float32
+    m = dev.Model(shape, w, max_batch=B + 1, max_ctx=max_ctx,
+                  max_chunk=max(max(lens), max(chunks)), k_max=k, cache_mode=mode)
+    oracles, cur = [], []
+    for b, T in enumerate(lens):
+        prompt = synth.tokens(shape, 1, T, seed=seed + b)
+        o = oracle.Oracle(shape, w, dtype=dt)
+        z = o.prefill(prompt, k, mode)["logits"][0, -1]
+        check_logits(m.prefill_slot(b, _tok(prompt[0]), k, mode).cpu().numpy(), z)
+        oracles.append(o)
+        cur.append(int(np.argmax(z)))
+    oc = oracle.Oracle(shape, w, dtype=dt)
+    new = synth.tokens(shape, 1, sum(chunks), seed=seed + 50)[0]
+    t0 = chunks[0]
+    zc = oc.prefill(new[None, :t0], k, mode)["logits"][0, -1]
+    check_logits(m.prefill_slot(B, _tok(new[:t0]), k, mode).cpu().numpy(), zc)
+    for C in chunks[1:]:
+        lg, g = m.step_mixed(_tok(np.array(cur, np.int32)), B, _tok(new[t0:t0 + C]), k, mode)
+        lg, g = lg.cpu().numpy(), g.cpu().numpy()
+        for b, o in enumerate(oracles):
+            r = o.decode(np.array([cur[b]], np.int32), k, mode)
+            check_logits(lg[b:b + 1], r["logits"])
+            check_greedy(g[b:b + 1], r["logits"])
+        r = oc.prefill(new[None, t0:t0 + C], k, mode)
+        check_logits(lg[B:B + 1], r["logits"][:, -1])
+        cur = [int(x) for x in np.argmax(lg[:B], axis=-1)]
+        t0 += C
+    # a step with no decode rows, then every slot decodes together
+    lg, g = m.step_mixed(_tok(np.zeros(0, np.int32)), B, _tok(new[:3]), k, mode)
+    r = oc.prefill(new[None, :3], k, mode)
+    check_logits(lg.cpu().numpy()[0:1], r["logits"][:, -1])
+    assert g is None
+    allc = np.array(cur + [int(np.argmax(r["logits"][0, -1]))], np.int32)
+    lg, _ = m.decode_ragged(_tok(allc), k, mode)
+    for b, o in enumerate(oracles + [oc]):
+        check_logits(lg.cpu().numpy()[b:b + 1], o.decode(allc[b:b + 1], k, mode)["logits"])
+    assert m.lengths(B + 1) == [o.length for o in oracles + [oc]]
+    assert m.device_status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
+def test_mixed_steps_tiny(dev, mode):
+    shape = synth.TINY_LOOPFULL                      # window 16: the rings wrap
+    _run_mixed(dev, shape, synth.make_weights(shape), [5, 23, 12], [7, 4, 19, 1], mode, 2,
+               max_ctx=96, seed=5)
+
+
+@pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
+def test_mixed_steps_4b_width(dev, mode):
+    """Chunks of 5 (8 rows: the GEMV path) and 40 / 64 (43 and 67 rows: the
+    tensor-core GEMMs) after decode rows of three slots, window 128."""
+    shape = synth.DORY4B_SLIM.replace(window=128)
+    _run_mixed(dev, shape, synth.make_weights(shape), [70, 150, 131], [100, 5, 40, 64], mode, 2,
+               max_ctx=384, seed=9)
