@@ -141,11 +141,29 @@ def embeddings(shape: Shape, shape_id: int | None = None) -> dict:
     }
 
 
+_CACHE = {}
+
+
 def make_weights(shape: Shape, shape_id: int | None = None, workers: int = 1) -> dict:
     """All weights of a model: {'embed_in', 'embed_out', 's_z', 'layers': [...]}.
 
     workers > 1 draws the tensors on that many threads (each tensor has its
-    own seed, so the values do not depend on the thread count)."""
+    own seed, so the values do not depend on the thread count).  Shallow
+    models of 1024 or more wide (the test-sized cuts of the wide shapes,
+    seconds to draw) are drawn once per process: each call returns new dicts
+    around the same arrays, which callers must not modify in place."""
+    key = (repr(shape), shape_id)
+    if shape.d >= 1024 and shape.n_layers <= 8:
+        if key not in _CACHE:
+            _CACHE[key] = _draw(shape, shape_id, workers)
+        base = _CACHE[key]
+        w = {k: v for k, v in base.items() if k != "layers"}
+        w["layers"] = [dict(lw) for lw in base["layers"]]
+        return w
+    return _draw(shape, shape_id, workers)
+
+
+def _draw(shape: Shape, shape_id: int | None, workers: int) -> dict:
     if workers <= 1:
         w = embeddings(shape, shape_id)
         w["layers"] = [layer_weights(shape, l, shape_id) for l in range(shape.n_layers)]
