@@ -968,6 +968,58 @@ def run_workload_4b(args):
                                 "so few drafts are accepted; drafting at k = 4 accepts every "
                                 "draft and bounds what the step can gain; eager calls, "
                                 "host-timed"})
+        elif args.workload == "serve4b":
+            # serving steps: B decode sequences at ragged lengths (synthetic
+            # cache) and one new prompt fed in chunks, either as one mixed
+            # step per chunk (decode rows + chunk share the weight reads) or
+            # as a ragged decode step followed by a slot prefill
+            import numpy as np
+            Bd, CH, NCH, K = 32, 256, 8, (args.decode_k or [2])[0]
+            rng = np.random.default_rng(0)
+            lens = [int(x) for x in rng.integers(2048, 16384, Bd)]
+            weights = synth.make_weights_torch(sh)
+            weights["layers"] = list(weights["layers"])
+            res = {}
+            for mode_name in ("mixed", "separate"):
+                m = dory.Model(sh, weights, max_batch=Bd + 1, max_ctx=16384 + 64,
+                               max_chunk=CH, k_max=K)
+                fill_cache_synthetic(m, sh)
+                m.set_lengths(lens + [0])
+                dec = torch.tensor(synth.tokens(sh, Bd, 1, seed=4)[:, 0], device="cuda",
+                                   dtype=torch.int32)
+                prompt = torch.tensor(synth.tokens(sh, 1, CH * (NCH + 2), seed=6)[0],
+                                      device="cuda", dtype=torch.int32)
+
+                def one(i):
+                    chunk = prompt[i * CH:(i + 1) * CH]
+                    if mode_name == "mixed":
+                        m.step_mixed(dec, Bd, chunk, K)
+                    else:
+                        m.decode_ragged(dec, K)
+                        m.prefill_slot(Bd, chunk, K)
+                for i in range(2):                            # untimed
+                    one(i)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for i in range(2, NCH + 2):
+                    one(i)
+                e1.record()
+                e1.synchronize()
+                ms = e0.elapsed_time(e1) / NCH
+                assert m.device_status() == 0
+                res[mode_name] = {"ms_per_step": round(ms, 3),
+                                  "tokens_per_step": Bd + CH,
+                                  "tokens_s": round((Bd + CH) / (ms / 1e3), 1)}
+                m.close()
+                del m
+                torch.cuda.empty_cache()
+            out.update({"decode_sequences": Bd, "lengths": "uniform in [2048, 16384)",
+                        "chunk": CH, "k": K, "per_mode": res,
+                        "speedup_mixed": round(res["separate"]["ms_per_step"] /
+                                               res["mixed"]["ms_per_step"], 3),
+                        "note": "eager calls on the default stream, CUDA-event timed; the decode "
+                                "cache contents are synthetic"})
         elif args.workload == "quant4b":
             # weight-only quantised decode: the same decode steps with bf16,
             # MXFP8 and NVFP4 projection weights (last-loop cache, synthetic
@@ -1339,7 +1391,7 @@ def main(argv=None):
                     help="4B-class profile target: skip the prefill")
     ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
                                            "longctx4b", "longprefill4b", "divergence4b",
-                                           "spec4b", "quant4b"],
+                                           "spec4b", "quant4b", "serve4b"],
                     default="headline4b",
                     help="headline4b: the default benchmark line (4B-class prefill 1x8192 + "
                          "decode 64x32768); small: the small looped nGPT line; the others time "
