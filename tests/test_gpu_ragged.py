@@ -227,3 +227,30 @@ def test_mixed_steps_4b_width(dev, mode):
     shape = synth.DORY4B_SLIM.replace(window=128)
     _run_mixed(dev, shape, synth.make_weights(shape), [70, 150, 131], [100, 5, 40, 64], mode, 2,
                max_ctx=384, seed=9)
+
+
+@pytest.mark.parametrize("mode", [oracle.LAST_LOOP, oracle.PER_LOOP], ids=["last", "perloop"])
+def test_ragged_batched_path_tiny(dev, mode):
+    """20 sequences (more rows than the few-row projections take: the
+    swapped tensor-core GEMMs), ragged lengths, one slot extended
+    mid-stream."""
+    shape = synth.TINY_LOOPFULL
+    lens = [3 + 2 * b for b in range(20)]
+    _run(dev, shape, synth.make_weights(shape), lens, mode, 2, steps=3, max_ctx=64,
+         extend=(1, 7, 5), seed=200 + mode)
+
+
+def test_per_sequence_loop_counts_batched_path_tiny(dev):
+    shape = synth.TINY_LOOPFULL
+    lens = [4 + 3 * b for b in range(18)]
+    _run(dev, shape, synth.make_weights(shape), lens, oracle.LAST_LOOP, 0, steps=3, max_ctx=80,
+         seed=300, ks=[1 + b % 4 for b in range(18)])
+
+
+def test_ragged_batched_path_4b_width(dev):
+    """18 sequences at the 4B-class width through the swapped GEMMs and the
+    TMA decode attention at ragged positions (window 128: some rings wrap)."""
+    shape = synth.DORY4B_SLIM.replace(window=128)
+    lens = [10 + 11 * b for b in range(18)]
+    _run(dev, shape, synth.make_weights(shape), lens, oracle.LAST_LOOP, 2, steps=2, max_ctx=256,
+         seed=400)
