@@ -1024,7 +1024,7 @@ def run_workload_4b(args):
             # weight-only quantised decode: the same decode steps with bf16,
             # MXFP8 and NVFP4 projection weights (last-loop cache, synthetic
             # contents), B sequences at ctx positions, k = 1 and 4
-            cases = [(1, 8192), (4, 8192), (16, 8192), (1, 262144)]
+            cases = [(1, 8192), (4, 8192), (16, 8192), (32, 8192), (64, 4096), (1, 262144)]
             D = 4
             weights = synth.make_weights_torch(sh)
             weights["layers"] = list(weights["layers"])     # used by three models
@@ -1073,8 +1073,11 @@ def run_workload_4b(args):
                          for c, v in res[f].items() if isinstance(v, dict)}
                      for f in ("mxfp8", "nvfp4")}
             out.update({"per_format": res, "speedup_vs_bf16": speed,
-                        "note": "few-row projections stream the packed codes; embeddings and the "
-                                "LM head stay bf16; CUDA graphs of 4 decode steps"})
+                        "note": "projections of 1-4 rows (bulk-copy GEMV) and of 17-128 rows "
+                                "(swapped tensor-core GEMM expanding the codes in shared memory) "
+                                "stream the packed codes, 5-16 rows read the dequantised bf16 "
+                                "copy; embeddings and the LM head stay bf16; CUDA graphs of 4 "
+                                "decode steps"})
         elif args.workload == "prefill4b":
             T = 8192
             m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,

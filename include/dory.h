@@ -306,13 +306,16 @@ typedef struct {
     dory_qmatrix qkvg, o, upgate, down;   /* same rows and K as the bf16 matrices */
 } dory_qlayer;
 
-/* From now on, every layer projection computed with at most 4 rows (the
- * decode steps of up to 4 sequences, prefill chunks of up to 4 rows)
- * streams these quantised weights instead of the bf16 ones; projections of
- * more rows keep reading the bf16 matrices (with 5 or more rows, decoding
- * the codes once per row makes the projection compute-bound), which should
- * then hold the dequantised values (dory_quantize_matrix's deq) so that
- * every path computes with the same weights.  The LM head and the embeddings are never
+/* From now on the decode projections stream these quantised weights
+ * instead of the bf16 ones: with at most 4 rows (decode of up to 4
+ * sequences, prefill chunks of up to 4 rows) through the few-row GEMVs, and
+ * for decode steps of 17 to 128 sequences through the swapped tensor-core
+ * GEMM, which expands each tile's codes to bf16 in shared memory.  The
+ * other projections (5 to 16 rows, where decoding the codes per row made
+ * the GEMV compute-bound, and prefill) keep reading the bf16 matrices,
+ * which should then hold the dequantised values (dory_quantize_matrix's
+ * deq): the expanded tiles equal those values exactly, so every path
+ * computes with the same weights.  The LM head and the embeddings are never
  * quantised.  layers: HOST array of n_layers entries (copied); fmt
  * DORY_QUANT_NONE switches back to the bf16 weights (layers may be NULL).
  * DORY_EINVAL for null pointers, misaligned codes (16 bytes) or NVFP4

@@ -190,6 +190,22 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// uint8 matrix [rows][cols] (row stride ld bytes), loaded as unswizzled
+// boxes {box_cols, box_rows} (packed quantised weights).
+bool encode_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+               uint32_t box_cols, uint32_t box_rows) {
+  if (!get_encoder()) return false;
+  if (((uintptr_t)base & 15) || ld % 16 || box_cols % 16) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 tensor [d2][d1][d0] (d0 contiguous, strides s1 / s2 elements), loaded
 // as boxes {64, box1, box2} with the 128-byte swizzle.
 bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -250,7 +266,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
   const int cols = EPI == EPI_SWIGLU ? args.N / 2 : args.N;
   const int bn_out = EPI == EPI_SWIGLU ? BN / 2 : BN;
   args.tiles_n = (cols + bn_out - 1) / bn_out;
-  if (EPI != EPI_PARTS) args.k_splits = 1;
+  if (!Cf::PARTS) args.k_splits = 1;
   if (args.k_splits < 1) return DORY_EINVAL;
   const int tiles = args.tiles_m * args.tiles_n * args.k_splits;
   if (tiles == 0) return DORY_OK;
@@ -265,7 +281,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs args, cud
   }
   // fp32 / SwiGLU: staged stores when the caller described the output
   args.staged = maps ? 1 : 0;
-  return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM, st, ta, tb,
+  return launch_k(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(Cf::THREADS), Cf::SMEM, st, ta, tb,
                   args, em) ==
                  cudaSuccess
              ? DORY_OK
@@ -1090,7 +1106,8 @@ int run_layer_decode(dory_model* m, int l, int slice, bool store, int B, int P0,
 // Swapped split-K projection for a decode batch: parts[s][row][n] (fp32) =
 // X[row, K range s] . W[n, K range s]^T; returns the number of splits.
 int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int rows,
-              int K, float* parts, int& n_parts, cudaStream_t st) {
+              int K, float* parts, int& n_parts, cudaStream_t st,
+              const dory_qmatrix* q = nullptr) {
   GemmArgs g{};
   g.w_pre = 1;   // weight operand: loads may start before the wait
   g.M = n_out;
@@ -1120,7 +1137,27 @@ int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n
   }
   g.k_splits = sp;
   n_parts = sp;
+  if (q && m->qfmt && K % 64 == 0) {
+    // weight-only quantised weights: the packed codes stream in and are
+    // expanded to bf16 in shared memory (the dequantised matrix's values)
+    const bool fp4 = m->qfmt == DORY_QUANT_NVFP4;
+    const uint64_t rb = fp4 ? K / 2 : K;
+    CUtensorMap tq;
+    if (!encode_u8(&tq, q->codes, n_out, rb, rb, fp4 ? 32 : 64, 128)) return DORY_ECUDA;
+    g.qfmt = m->qfmt;
+    g.qscales = static_cast<const uint8_t*>(q->scales);
+    g.qrow = q->row_scale;
+    return launch_gemm<kSwapBN, EPI_QPARTS>(tq, tx, g, st);
+  }
   return launch_gemm<kSwapBN, EPI_PARTS>(tw, tx, g, st);
+}
+
+// The layer's quantised matrix (which: 0 QKV+gate, 1 output, 2 up+gate, 3
+// down), or null without quantised weights.
+const dory_qmatrix* qmat(const dory_model* m, int l, int which) {
+  if (!m->qfmt) return nullptr;
+  const dory_qlayer& q = m->qlayers[l];
+  return which == 0 ? &q.qkvg : which == 1 ? &q.o : which == 2 ? &q.upgate : &q.down;
 }
 
 // One layer for one new token per sequence with more sequences than the GEMV
@@ -1143,7 +1180,7 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
   int np = 1;
 
   pb(m, DORY_K_QKVG_GEMM, st);
-  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_qkvg[l], tx_hb, nqkvg, B, c.d, parts, np, st)));
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_qkvg[l], tx_hb, nqkvg, B, c.d, parts, np, st, qmat(m, l, 0))));
 
   DecAttnArgs da{};
   da.y = parts;
@@ -1179,11 +1216,12 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
   DORY_TRY(pe(m, st, dec_attn<true>(da, B, c.head_dim, st)));
 
   pb(m, DORY_K_O_GEMM, st);
-  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_o[l], tx_att, c.d, B, hq, parts, np, st)));
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_o[l], tx_att, c.d, B, hq, parts, np, st, qmat(m, l, 1))));
   DORY_TRY(ngpt_update(m, B, h, w.alpha_attn, st, parts, np, (long long)B * c.d));
 
   pb(m, DORY_K_UPGATE_GEMM, st);
-  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_upgate[l], tx_hb, 2 * c.ffn, B, c.d, parts, np, st)));
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_upgate[l], tx_hb, 2 * c.ffn, B, c.d, parts, np, st,
+                                qmat(m, l, 2))));
   pb(m, DORY_K_UPGATE_GEMM, st);
   DORY_TRY(pe(m, st,
               launch_k(swiglu_parts_kernel, dim3((c.ffn + 8 * kRowThreads - 1) / (8 * kRowThreads), B),
@@ -1193,7 +1231,7 @@ int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0
                   : DORY_ECUDA));
 
   pb(m, DORY_K_DOWN_GEMM, st);
-  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_down[l], tx_m, c.d, B, c.ffn, parts, np, st)));
+  DORY_TRY(pe(m, st, swap_gemm(m, m->tm_down[l], tx_m, c.d, B, c.ffn, parts, np, st, qmat(m, l, 3))));
   return ngpt_update(m, B, h, w.alpha_mlp, st, parts, np, (long long)B * c.d);
 }
 

@@ -43,10 +43,12 @@
 //               the consumers add the partials.
 #pragma once
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace dory {
 
-enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2, EPI_PARTS = 3, EPI_NGPT = 4 };
+enum EpiKind { EPI_F32 = 0, EPI_QKVG = 1, EPI_SWIGLU = 2, EPI_PARTS = 3, EPI_NGPT = 4,
+               EPI_QPARTS = 5 };
 
 struct GemmArgs {
   int M, N, K;          // N: output columns of the GEMM (for SWIGLU: 2 * ffn)
@@ -82,6 +84,12 @@ struct GemmArgs {
   // tiles_n (N / 256 <= 8)
   const float* h32;
   const float* alpha;
+  // EPI_QPARTS (EPI_PARTS with weight-only quantised weights): tmA maps the
+  // packed codes (uint8 [M][K or K / 2]); qfmt 1 MXFP8, 2 NVFP4; block
+  // scales [M][K / 32 or K / 16]; qrow: NVFP4 row scales [M]
+  int qfmt;
+  const uint8_t* qscales;
+  const float* qrow;
   // 1: the weight operand (A for EPI_PARTS, else B) never changes during the
   // forward pass, so the producer issues the weight loads of the first ring
   // stages before waiting on the previous kernel (programmatic launch); the
@@ -96,7 +104,9 @@ struct GemmCfg {
   // QKV+gate 2 halves x 128 x 128 bf16 (64 KB), fp32 2 halves x 2 buffers x
   // {32 x 128} fp32 (64 KB), SwiGLU 2 halves x {64 x 128} bf16 (32 KB).
   // The first two cost a stage of the operand ring.
-  static constexpr bool STAGED = BN == 256 && EPI != 3;
+  static constexpr bool PARTS = EPI == 3 || EPI == 5;
+  static constexpr bool QA = EPI == 5;          // A: packed codes expanded in shared memory
+  static constexpr bool STAGED = BN == 256 && !PARTS;
   static constexpr bool NGPT = EPI == 4;
   static constexpr uint32_t OUT_BYTES = !STAGED ? 0 : (EPI == 2 ? 2 * 16384 : 4 * 16384);
   static constexpr int STAGES = STAGED ? (EPI == 2 ? 4 : 3) : (BN == 256 ? 4 : 6);
@@ -104,13 +114,18 @@ struct GemmCfg {
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t BAR_BYTES = QA ? 512 : 256;
+  // EPI_QPARTS: a raw stage per ring stage holds the tile's codes (128 rows x
+  // 64 bytes for MXFP8, 32 for NVFP4); a converter warpgroup (threads
+  // 320..447) expands them into the ring's bf16 A stage
+  static constexpr uint32_t RAW_STAGE = QA ? BM * BK : 0;
+  static constexpr int THREADS = QA ? 448 : 320;
   static constexpr uint32_t SQK_BYTES = EPI == 1 ? 512 : 0;   // s_qk of a 128-wide head
   // EPI_NGPT: alpha slice [256], half partial sums for y and u [2][128] each,
   // the cluster's per-row sums for y and u [8][128] each, two mbarriers
   static constexpr uint32_t NGPT_BYTES = NGPT ? (256 + 2 * 256 + 2 * 8 * 128) * 4 + 16 : 0;
-  static constexpr size_t SMEM =
-      STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES + NGPT_BYTES + 1024;
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES +
+                                 NGPT_BYTES + STAGES * RAW_STAGE + 1024;
 };
 
 // Destination maps of the staged epilogues, all with the 128-byte swizzle:
@@ -643,7 +658,7 @@ __device__ __forceinline__ bool epi_ngpt(const GemmArgs& a, const EpiMaps& maps,
 constexpr int kGemmThreads = 320;   // producer, MMA, 8 epilogue warps
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args, const __grid_constant__ EpiMaps maps) {
   using C = GemmCfg<BN, EPI>;
@@ -673,9 +688,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* raw_full = drain_bar + 2;                 // EPI_QPARTS: [STAGES]
+  uint64_t* conv_bar = raw_full + STAGES;             // EPI_QPARTS: [STAGES]
+  uint8_t* raw_base = smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES + C::BAR_BYTES +
+                      C::SQK_BYTES + C::NGPT_BYTES;
+  const int raw_row = C::QA ? (args.qfmt == 2 ? BK / 2 : BK) : 0;   // code bytes per row
+  const uint32_t raw_bytes = (uint32_t)(BM * raw_row);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int splits = EPI == EPI_PARTS ? args.k_splits : 1;
+  const int splits = C::PARTS ? args.k_splits : 1;
   const int num_tiles = args.tiles_m * args.tiles_n * splits;
   const int KB = (args.K + BK - 1) / BK;
   // K blocks [kb_lo, kb_hi) of work unit `tile` (split = tile / (tiles_m tiles_n))
@@ -695,6 +716,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty_bar[b], 256);
     }
     mbar_init(drain_bar, 1);
+    if (C::QA) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(&raw_full[s], 1);
+        mbar_init(&conv_bar[s], 4);                 // one arrival per converter warp
+      }
+    }
     if (C::NGPT) {
       mbar_init(ns.bar_y, 1);
       mbar_init(ns.bar_u, 1);
@@ -743,6 +770,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = kb_lo; kb < kb_hi && n_pre < STAGES; ++kb, ++n_pre) {
         uint8_t* a_dst = smem + n_pre * C::STAGE_BYTES;
         uint8_t* b_dst = a_dst + C::A_BYTES;
+        if (C::QA) {                                // the codes; the activations follow
+          mbar_arrive_expect_tx(&raw_full[n_pre], raw_bytes);
+          tma_load_2d(raw_base + n_pre * C::RAW_STAGE, &tmA, &raw_full[n_pre], kb * raw_row, m0);
+          continue;
+        }
         mbar_arrive_expect_tx(&full_bar[n_pre], C::STAGE_BYTES);
         if (EPI == EPI_PARTS) {
           tma_load_2d(a_dst, &tmA, &full_bar[n_pre], kb * BK, m0);
@@ -775,7 +807,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* a_dst = smem + stage * C::STAGE_BYTES;
           uint8_t* b_dst = a_dst + C::A_BYTES;
-          if (g < n_pre) {                          // weights already on their way
+          if (C::QA) {
+            // activations into the ring; codes into the raw stage (free: the
+            // MMA that released this stage read the tile converted from it)
+            mbar_arrive_expect_tx(&full_bar[stage], C::B_BYTES);
+            tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
+            tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
+            if (g >= n_pre) {
+              mbar_arrive_expect_tx(&raw_full[stage], raw_bytes);
+              tma_load_2d(raw_base + stage * C::RAW_STAGE, &tmA, &raw_full[stage], kb * raw_row,
+                          m0);
+            }
+          } else if (g < n_pre) {                   // weights already on their way
             if (EPI == EPI_PARTS) {
               tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
               tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
@@ -815,7 +858,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int kb_lo, kb_hi;
         kb_range(tile, kb_lo, kb_hi);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait_bounded(&full_bar[stage], phase, args.status, DEV_GEMM_MMA_FULL)) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, args.status, DEV_GEMM_MMA_FULL) ||
+              (C::QA &&
+               !mbar_wait_bounded(&conv_bar[stage], phase, args.status, DEV_GEMM_MMA_FULL))) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -843,6 +888,89 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_wait_bounded(drain_bar, 0, args.status, DEV_GEMM_DRAIN);
     }
     __syncwarp();
+  } else if (C::QA && warp >= 10) {
+    // ------------------------------------------------ code expansion (warps 10..13)
+    // thread r expands row r of each tile's k block into the bf16 A stage
+    // (128-byte swizzle, as TMA would have written it) with the block scale
+    // (and the NVFP4 row scale): the values of the dequantised bf16 matrix
+    const int r = threadIdx.x - 320;
+    const bool fp4 = args.qfmt == 2;
+    const int spr = fp4 ? args.K / 16 : args.K / 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok && !*abort_flag; tile += gridDim.x) {
+      int m0, nb0, nb1, kb_lo, kb_hi;
+      coords(tile, m0, nb0, nb1);
+      kb_range(tile, kb_lo, kb_hi);
+      const int row = m0 + r;
+      const bool rv = row < args.M;
+      const float rs = (fp4 && rv && args.qrow) ? args.qrow[row] : 1.0f;
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        const bool w_ok =
+            !*abort_flag &&
+            mbar_wait_bounded(&empty_bar[stage], phase ^ 1, args.status, DEV_GEMM_CONV) &&
+            mbar_wait_bounded(&raw_full[stage], phase, args.status, DEV_GEMM_CONV);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* a_st = smem + stage * C::STAGE_BYTES;
+        const uint4* raw = reinterpret_cast<const uint4*>(raw_base + stage * C::RAW_STAGE +
+                                                          r * raw_row);
+        uint32_t pk[32];
+        if (!rv) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = 0u;
+        } else if (!fp4) {
+          const uint8_t* sc = args.qscales + (long long)row * spr + kb * 2;
+          const float s0 = e8m0_to_f32(sc[0]), s1 = e8m0_to_f32(sc[1]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = raw[q];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            const float s = q < 2 ? s0 : s1;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              float f[4];
+              e4m3x4_to_f32(w4[t], f);
+              pk[q * 8 + 2 * t] = pack_bf16x2(f[0] * s, f[1] * s);
+              pk[q * 8 + 2 * t + 1] = pack_bf16x2(f[2] * s, f[3] * s);
+            }
+          }
+        } else {
+          const uint32_t s4 =
+              *reinterpret_cast<const uint32_t*>(args.qscales + (long long)row * spr + kb * 4);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint4 v = raw[q];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {                  // 8 codes of block 2q + t / 2
+              const float s = e4m3_to_f32((s4 >> (8 * (2 * q + t / 2))) & 0xFFu);
+              float f[8];
+              e2m1x8_to_f32(w4[t], f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                pk[q * 16 + 4 * t + i] =
+                    pack_bf16x2(__fmul_rn(f[2 * i] * s, rs), __fmul_rn(f[2 * i + 1] * s, rs));
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *sw128_chunk(a_st, r, j) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                                                pk[4 * j + 3]);
+        fence_proxy_async_smem();                   // visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_bar[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------ epilogue warps 2..9
     const int quarter = warp & 3;
@@ -916,7 +1044,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           epi_swiglu<BN>(args, tacc, row, tn, c_lo, c_hi);
       }
-      if (EPI == EPI_PARTS)
+      if (C::PARTS)
         epi_parts<BN>(args, tacc, row, tn * BN, tile / (args.tiles_m * args.tiles_n), c_lo, c_hi);
       if (C::NGPT) {
         if (!epi_ngpt(args, maps, ns, tacc, rloc, m0, tn * BN, c_lo, my_stage, chalf, leader, nst,

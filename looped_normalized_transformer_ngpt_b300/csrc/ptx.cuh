@@ -17,6 +17,7 @@ enum : int {
   DEV_GEMM_EPI = 0x14,
   DEV_GEMM_DRAIN = 0x15,
   DEV_GEMM_NGPT = 0x16,
+  DEV_GEMM_CONV = 0x17,
   DEV_ATTN_PRODUCER = 0x41,
   DEV_ATTN_MMA = 0x42,
   DEV_ATTN_SOFTMAX = 0x43,

@@ -14,8 +14,10 @@ maximum scaling, NVFP4 with the squared-error scale search).
   shape, the bulk-copy form at the 4B width, with 1 and with 2-4 rows) and a
   chunk of 15 rows (the dequantised bf16 copy), both cache modes on the tiny
   shape with a full layer in the loop, and at the 4B-class width (3 layers),
-  where every projection of the 4B-class model has its full size.
-  Tolerances as in test_gpu_parity."""
+  where every projection of the 4B-class model has its full size; decode of
+  20 sequences through the swapped tensor-core GEMM that expands the codes
+  in shared memory, against the oracle and bit for bit against the same
+  GEMM on the dequantised bf16 matrices.  Tolerances as in test_gpu_parity."""
 import numpy as np
 import pytest
 
@@ -181,3 +183,36 @@ def test_quantized_switch_back(dev):
     nxt = np.array([3], np.int32)
     check_logits(m.decode(_tok(nxt), 1)[0].cpu().numpy(), o.decode(nxt, 1, oracle.LAST_LOOP)["logits"])
     m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_quantized_batched_decode_equals_dequantised_copy(dev, weights_3l, fmt):
+    """20 sequences decode through the swapped tensor-core GEMM, which
+    expands the packed codes to bf16 in shared memory: bit for bit the
+    results of the same GEMM reading the dequantised bf16 matrices."""
+    import torch
+    B, T, k = 20, 9, 2
+    prompt = synth.tokens(SHAPE_3L, B, T, seed=51)
+    a = dev.Model(SHAPE_3L, weights_3l, max_batch=B, max_ctx=64, max_chunk=T, k_max=k)
+    b = dev.Model(SHAPE_3L, weights_3l, max_batch=B, max_ctx=64, max_chunk=T, k_max=k)
+    a.quantize(fmt)
+    b.quantize(fmt)
+    b.quantize(dev.QUANT_NONE)                       # the same values, as bf16 matrices
+    la, lb = a.prefill(_tok(prompt), k), b.prefill(_tok(prompt), k)
+    assert torch.equal(la, lb)
+    tok = torch.argmax(la, dim=-1).to(torch.int32)
+    for _ in range(3):
+        la, ga = a.decode(tok, k)
+        lb, gb = b.decode(tok, k)
+        assert torch.equal(la, lb) and torch.equal(ga, gb)
+        tok = ga
+    assert a.device_status() == 0
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_quantized_batched_decode_4b_width(dev, weights_3l, fmt):
+    qw, _ = quant.quantize_weights(weights_3l, fmt)
+    _run_model(dev, SHAPE_3L, weights_3l, fmt, oracle.LAST_LOOP, k=2, B=20, T=9, D=2, seed=61,
+               qw=qw)
