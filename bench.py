@@ -1056,14 +1056,27 @@ def run_workload_4b(args):
                         ms = _graph_time(fn, st, warm=1, reps=3) / D
                         by = decode_step_bytes(sh, B, k, P0 + D // 2)
                         na = len(layer_apps(sh, k))
+                        # one sequence streams the codes (GEMV); 2-128 read
+                        # the bf16 copy unless the swapped GEMM expands the
+                        # codes (timed as well below)
+                        swap_rows = 1 < B <= 128
+                        wq = wb if fmt and B == 1 else 2 * sum(layer_params(sh).values())
                         w = by["weights"] - 2 * sum(layer_params(sh).values()) * na \
-                            + wb * na // sh.n_layers
+                            + wq * na // sh.n_layers
                         gbs = (w + by["kv"]) / (ms / 1e3) / 1e9
                         r[f"B{B}_ctx{ctx}_k{k}"] = {
                             "decode_tok_s": round(B / (ms / 1e3), 1), "ms_per_step": round(ms, 3),
                             "bytes_per_step_GB": round((w + by["kv"]) / 1e9, 2),
                             "achieved_GBs": round(gbs, 1),
                             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+                        if fmt and swap_rows:
+                            m.set_quantized_swap(True)
+                            ms_s = _graph_time(fn, st, warm=1, reps=3) / D
+                            m.set_quantized_swap(False)
+                            w_s = w - (2 * sum(layer_params(sh).values()) - wb) * na // sh.n_layers
+                            r[f"B{B}_ctx{ctx}_k{k}"]["codes_in_swapped_gemm"] = {
+                                "ms_per_step": round(ms_s, 3),
+                                "bytes_per_step_GB": round((w_s + by["kv"]) / 1e9, 2)}
                     assert m.device_status() == 0
                 res[fmt_name] = r
                 m.close()
@@ -1073,11 +1086,12 @@ def run_workload_4b(args):
                          for c, v in res[f].items() if isinstance(v, dict)}
                      for f in ("mxfp8", "nvfp4")}
             out.update({"per_format": res, "speedup_vs_bf16": speed,
-                        "note": "projections of 1-4 rows (bulk-copy GEMV) and of 17-128 rows "
-                                "(swapped tensor-core GEMM expanding the codes in shared memory) "
-                                "stream the packed codes, 5-16 rows read the dequantised bf16 "
-                                "copy; embeddings and the LM head stay bf16; CUDA graphs of 4 "
-                                "decode steps"})
+                        "note": "decode of one sequence streams the packed codes (bulk-copy "
+                                "GEMV), 2-128 sequences read the dequantised bf16 copy through "
+                                "the swapped tensor-core GEMM by default; "
+                                "codes_in_swapped_gemm: the opt-in path that expands the codes "
+                                "in that GEMM's shared memory; embeddings and the LM head stay "
+                                "bf16; CUDA graphs of 4 decode steps"})
         elif args.workload == "prefill4b":
             T = 8192
             m = dory.Model(sh, synth.make_weights_torch(sh), max_batch=1, max_ctx=T, max_chunk=T,

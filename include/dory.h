@@ -152,9 +152,12 @@ DORY_API int dory_prefill(dory_t* m, const int32_t* tokens, int B, int T, int k,
  * runs the forward at loop count k.  tokens: device int32 [B].  logits:
  * device fp32 [B, vocab] or NULL; next: device int32 [B] greedy tokens or
  * NULL (requires logits).
- * Decode steps of up to 16 sequences run five kernels per layer application
- * (weight-streaming projections, one attention kernel); larger batches run
- * the tensor-core projections with K split over the SMs.  With
+ * Decode steps of up to 128 sequences run the tensor-core projections with
+ * the weights as the 128-row operand and K split over the SMs (on B300 this
+ * streams the weights faster than a GEMV, from one sequence up); a single
+ * sequence with quantised weights runs five kernels per layer application
+ * instead (GEMVs streaming the packed codes, one attention kernel); larger
+ * batches run the prefill GEMMs.  With
  * head_dim 128 and ring sizes that are multiples of 64 (max_ctx and window,
  * as given to dory_bind / dory_create) the attention streams the cached K/V
  * with TMA through a 4-stage ring; otherwise a cp.async kernel does (same
@@ -307,20 +310,31 @@ typedef struct {
 } dory_qlayer;
 
 /* From now on the decode projections stream these quantised weights
- * instead of the bf16 ones: with at most 4 rows (decode of up to 4
- * sequences, prefill chunks of up to 4 rows) through the few-row GEMVs, and
- * for decode steps of 17 to 128 sequences through the swapped tensor-core
- * GEMM, which expands each tile's codes to bf16 in shared memory.  The
- * other projections (5 to 16 rows, where decoding the codes per row made
- * the GEMV compute-bound, and prefill) keep reading the bf16 matrices,
- * which should then hold the dequantised values (dory_quantize_matrix's
- * deq): the expanded tiles equal those values exactly, so every path
- * computes with the same weights.  The LM head and the embeddings are never
+ * instead of the bf16 ones: through the few-row GEMVs for decode steps of
+ * one sequence and prefill chunks of up to 4 rows, and, when
+ * dory_set_quantized_swap enables it, for decode steps of 2 to 128
+ * sequences through the swapped tensor-core GEMM, which expands each
+ * tile's codes to bf16 in shared memory.  The other projections (decode of
+ * 2 to 128 sequences by default, prefill chunks of 5 or more rows, where
+ * decoding the codes per row made the GEMV compute-bound) keep reading the
+ * bf16 matrices, which should then hold the dequantised values
+ * (dory_quantize_matrix's deq): the expanded tiles equal those values
+ * exactly, so every path computes with the same weights.  The LM head and the embeddings are never
  * quantised.  layers: HOST array of n_layers entries (copied); fmt
  * DORY_QUANT_NONE switches back to the bf16 weights (layers may be NULL).
  * DORY_EINVAL for null pointers, misaligned codes (16 bytes) or NVFP4
  * scales (2 bytes), or d, n_q*head_dim or ffn not multiples of 32. */
 DORY_API int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* layers);
+
+/* stream_codes 1: decode steps of 2 to 128 sequences run their quantised
+ * projections through the swapped GEMM that expands the codes in shared
+ * memory; 0 (the default): they read the dequantised bf16 matrices.  Both
+ * give bit-identical results.  The default is the faster one on B300 for
+ * the 4B-class decode shapes: those GEMMs are short and latency-bound, so
+ * halving or quartering their weight bytes does not shorten them, and the
+ * expansion adds its own latency.  Host state only; applies to later
+ * steps.  DORY_EINVAL for a null handle or a value other than 0 / 1. */
+DORY_API int dory_set_quantized_swap(dory_t* m, int stream_codes);
 
 /* ------------------------------------------------------------------------
  * Ragged batches: sequences of different lengths in one decode step (the

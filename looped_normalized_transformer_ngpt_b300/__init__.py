@@ -116,6 +116,7 @@ _SIGS = {
                               ctypes.POINTER(ctypes.c_size_t)]),
     "dory_quantize_matrix": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dory_set_quantized_weights": (_I, [_P, _I, ctypes.POINTER(DoryQLayer)]),
+    "dory_set_quantized_swap": (_I, [_P, _I]),
     "dory_profile_begin": (_I, [_P, _I]),
     "dory_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "dory_debug_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -345,6 +346,13 @@ class Model:
             table[l] = DoryQLayer(mats["qkvg"], mats["o"], mats["upg"], mats["down"])
         _check("dory_set_quantized_weights", L.dory_set_quantized_weights(self.handle, fmt, table))
         self._q = keep
+
+    def set_quantized_swap(self, stream_codes):
+        """Whether decode steps of 2-128 sequences expand the quantised
+        codes inside the swapped GEMM (True) or read the dequantised bf16
+        matrices (False, the default); the results are bit-identical."""
+        _check("dory_set_quantized_swap",
+               lib().dory_set_quantized_swap(self.handle, 1 if stream_codes else 0))
 
     def set_lengths(self, lengths):
         """Per-sequence lengths of batch slots 0 .. len(lengths) - 1."""

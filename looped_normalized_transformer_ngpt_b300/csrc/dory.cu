@@ -93,8 +93,8 @@ WsLayout ws_layout(const dory_config& c, int max_batch, int max_chunk) {
   L.seq_pos = take((size_t)max_batch * 4);            // ragged decode: positions
   L.seq_k = take((size_t)max_batch * 4);              //   and loop counts
   L.save32 = take((size_t)max_batch * c.d * 4);       //   and finished rows' states
-  // batched decode (kGemvMaxM < rows <= kSwapMaxM): split-K partial sums
-  if (max_batch > kGemvMaxM) {
+  // batched decode (up to kSwapMaxM rows): split-K partial sums
+  {
     const size_t rows = max_batch < kSwapMaxM ? max_batch : kSwapMaxM;
     const size_t w2 = wide > (size_t)c.d ? wide : (size_t)c.d;
     L.parts = take((size_t)kSwapMaxParts * rows * w2 * 4);
@@ -193,7 +193,8 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 // uint8 matrix [rows][cols] (row stride ld bytes), loaded as unswizzled
 // boxes {box_cols, box_rows} (packed quantised weights).
 bool encode_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
-               uint32_t box_cols, uint32_t box_rows) {
+               uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   if (!get_encoder()) return false;
   if (((uintptr_t)base & 15) || ld % 16 || box_cols % 16) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -201,8 +202,7 @@ bool encode_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -821,6 +821,7 @@ struct dory_model {
   std::vector<dory_layer_weights> layers;
   int qfmt = 0;                          // DORY_QUANT_* of the few-row projections
   std::vector<dory_qlayer> qlayers;
+  int q_swap = 0;                        // 17-128 rows: expand the codes in the swapped GEMM
   const void* embed_in = nullptr;
   const void* embed_out = nullptr;
   const float* s_z = nullptr;
@@ -975,7 +976,8 @@ float attn_scale_log2(const dory_config& c) {
   return scale * 1.4426950408889634f;
 }
 
-// One layer for one new token per sequence (decode, B <= kGemvMaxM rows):
+// One layer for one new token per sequence through the few-row GEMVs (a
+// single sequence with quantised weights, see gemv_decode):
 // five kernels.  QKV + gate GEMV (owed nGPT step fused) -> attention (RoPE /
 // q-k norm in its prologue, split merge, gate and KV write fused) -> output
 // GEMV -> up + gate GEMV with SwiGLU (attention nGPT step fused) -> down GEMV
@@ -1137,31 +1139,46 @@ int swap_gemm(dory_model* m, const CUtensorMap& tw, const CUtensorMap& tx, int n
   }
   g.k_splits = sp;
   n_parts = sp;
-  if (q && m->qfmt && K % 64 == 0) {
-    // weight-only quantised weights: the packed codes stream in and are
-    // expanded to bf16 in shared memory (the dequantised matrix's values)
-    const bool fp4 = m->qfmt == DORY_QUANT_NVFP4;
+  const bool fp4 = m->qfmt == DORY_QUANT_NVFP4;
+  const int spr = fp4 ? K / 16 : K / 32;             // block-scale bytes per row
+  if (q && m->qfmt && K % 64 == 0 && spr % 16 == 0) {
+    // weight-only quantised weights: the packed codes and block scales
+    // stream in and are expanded to bf16 in shared memory (the dequantised
+    // matrix's values)
     const uint64_t rb = fp4 ? K / 2 : K;
     CUtensorMap tq;
-    if (!encode_u8(&tq, q->codes, n_out, rb, rb, fp4 ? 32 : 64, 128)) return DORY_ECUDA;
+    EpiMaps em;
+    std::memset(&em, 0, sizeof(em));
+    // code rows with the swizzle of their width (bank-conflict-free reads)
+    if (!encode_u8(&tq, q->codes, n_out, rb, rb, fp4 ? 32 : 64, 128,
+                   fp4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_u8(&em.q, q->scales, n_out, spr, spr, 16, 128))
+      return DORY_ECUDA;
     g.qfmt = m->qfmt;
     g.qscales = static_cast<const uint8_t*>(q->scales);
     g.qrow = q->row_scale;
-    return launch_gemm<kSwapBN, EPI_QPARTS>(tq, tx, g, st);
+    return launch_gemm<kSwapBN, EPI_QPARTS>(tq, tx, g, st, &em);
   }
   return launch_gemm<kSwapBN, EPI_PARTS>(tw, tx, g, st);
 }
 
 // The layer's quantised matrix (which: 0 QKV+gate, 1 output, 2 up+gate, 3
 // down), or null without quantised weights.
+// One-token steps run through the few-row GEMVs only for a single sequence
+// with quantised weights (the GEMV streams its packed codes); every other
+// one-token step takes the swapped tensor-core GEMM, which on B300 reads the
+// weights faster than the GEMV from one sequence up (measured: the 4B-class
+// decode step at 1, 2, 4 and 16 sequences, 9 to 75% shorter).
+bool gemv_decode(const dory_model* m, int M) { return m->qfmt != 0 && M == 1; }
+
 const dory_qmatrix* qmat(const dory_model* m, int l, int which) {
-  if (!m->qfmt) return nullptr;
+  if (!m->qfmt || !m->q_swap) return nullptr;
   const dory_qlayer& q = m->qlayers[l];
   return which == 0 ? &q.qkvg : which == 1 ? &q.o : which == 2 ? &q.upgate : &q.down;
 }
 
-// One layer for one new token per sequence with more sequences than the GEMV
-// handles (kGemvMaxM < B <= kSwapMaxM): weights are the 128-row operand of
+// One layer for one new token per sequence (B <= kSwapMaxM, unless
+// gemv_decode): weights are the 128-row operand of
 // the tensor-core GEMM, the batch the 64-row one, K split over the SMs; the
 // attention, nGPT-step and SwiGLU kernels add the partial sums.
 int run_layer_batched(dory_model* m, int l, int slice, bool store, int B, int P0,
@@ -1585,8 +1602,8 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
   const int M = B * C;
   const int P0 = m->len;
   int* status = wsp<int>(m, m->L.status);
-  const bool decode = !m->mixed_step && C == 1 && M <= kGemvMaxM;
-  const bool batched = !m->mixed_step && C == 1 && M > kGemvMaxM && M <= kSwapMaxM;
+  const bool decode = !m->mixed_step && C == 1 && gemv_decode(m, M);
+  const bool batched = !m->mixed_step && C == 1 && !decode && M <= kSwapMaxM;
 
   CUtensorMap tm_hb, tm_att, tm_m;
   const int hq = c.n_q * c.head_dim;
@@ -1694,7 +1711,7 @@ int run_step(dory_model* m, const int32_t* tokens, int ld_tok, int B, int C, int
     gl.status = status;
     gl.col_scale = m->s_z;
     gl.ldo = c.vocab;
-    if (n_logit_rows == 1 && B <= kGemvMaxM) {
+    if (n_logit_rows == 1 && decode) {
       GemvArgs g{};
       g.M = B;
       g.X = wsp<__nv_bfloat16>(m, m->L.hb) + (size_t)(C - 1) * c.d;
@@ -2352,6 +2369,12 @@ int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* layers) {
   }
   m->qlayers.assign(layers, layers + n_layers(c));
   m->qfmt = fmt;
+  return DORY_OK;
+}
+
+int dory_set_quantized_swap(dory_t* m, int stream_codes) {
+  if (!m || (stream_codes != 0 && stream_codes != 1)) return DORY_EINVAL;
+  m->q_swap = stream_codes;
   return DORY_OK;
 }
 

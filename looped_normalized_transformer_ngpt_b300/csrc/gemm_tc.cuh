@@ -85,8 +85,9 @@ struct GemmArgs {
   const float* h32;
   const float* alpha;
   // EPI_QPARTS (EPI_PARTS with weight-only quantised weights): tmA maps the
-  // packed codes (uint8 [M][K or K / 2]); qfmt 1 MXFP8, 2 NVFP4; block
-  // scales [M][K / 32 or K / 16]; qrow: NVFP4 row scales [M]
+  // packed codes (uint8 [M][K or K / 2]) and EpiMaps::q the block scales
+  // (uint8 [M][K / 32 or K / 16], {16, 128} boxes); qfmt 1 MXFP8, 2 NVFP4;
+  // qrow: NVFP4 row scales [M]
   int qfmt;
   const uint8_t* qscales;
   const float* qrow;
@@ -109,23 +110,35 @@ struct GemmCfg {
   static constexpr bool STAGED = BN == 256 && !PARTS;
   static constexpr bool NGPT = EPI == 4;
   static constexpr uint32_t OUT_BYTES = !STAGED ? 0 : (EPI == 2 ? 2 * 16384 : 4 * 16384);
-  static constexpr int STAGES = STAGED ? (EPI == 2 ? 4 : 3) : (BN == 256 ? 4 : 6);
+  static constexpr int STAGES = STAGED ? (EPI == 2 ? 4 : 3) : (BN == 256 || QA ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = QA ? 512 : 256;
-  // EPI_QPARTS: a raw stage per ring stage holds the tile's codes (128 rows x
-  // 64 bytes for MXFP8, 32 for NVFP4); a converter warpgroup (threads
-  // 320..447) expands them into the ring's bf16 A stage
-  static constexpr uint32_t RAW_STAGE = QA ? BM * BK : 0;
-  static constexpr int THREADS = QA ? 448 : 320;
+  // EPI_QPARTS: a ring of raw stages, deeper than the operand ring, each
+  // holding a tile's codes for one k block (128 rows x 64 bytes for MXFP8,
+  // 32 for NVFP4, with the 64- / 32-byte swizzle) and a 16-byte group of
+  // each row's block scales (the k block's scales among them); warp 14
+  // loads them, a converter warpgroup (warps 10..13) expands them into the
+  // operand ring's bf16 A stages
+  static constexpr int RAW_STAGES = QA ? 10 : 0;
+  static constexpr uint32_t RAW_SCALES = BM * 16;
+  static constexpr uint32_t RAW_STAGE = QA ? BM * BK + RAW_SCALES : 0;
+  static constexpr int THREADS = QA ? 480 : 320;
   static constexpr uint32_t SQK_BYTES = EPI == 1 ? 512 : 0;   // s_qk of a 128-wide head
   // EPI_NGPT: alpha slice [256], half partial sums for y and u [2][128] each,
   // the cluster's per-row sums for y and u [8][128] each, two mbarriers
   static constexpr uint32_t NGPT_BYTES = NGPT ? (256 + 2 * 256 + 2 * 8 * 128) * 4 + 16 : 0;
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES +
-                                 NGPT_BYTES + STAGES * RAW_STAGE + 1024;
+  static constexpr uint32_t BASE_BYTES =
+      STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + SQK_BYTES + NGPT_BYTES;
+  static constexpr uint32_t RAW_OFF = (BASE_BYTES + 1023) / 1024 * 1024;   // swizzle-aligned
+  static constexpr size_t SMEM = (QA ? RAW_OFF + RAW_STAGES * RAW_STAGE : BASE_BYTES) + 1024;
+  // full, empty [STAGES]; tfull, tempty [2]; drain; TMEM slot + abort flag;
+  // EPI_QPARTS: raw_full, raw_empty [RAW_STAGES], conv [STAGES]
+  static_assert((2 * STAGES + 6 + 2 * RAW_STAGES + (QA ? STAGES : 0)) * 8 <= BAR_BYTES,
+                "barrier area");
+  static_assert(RAW_STAGE % 1024 == 0, "raw stages keep the swizzle alignment");
 };
 
 // Destination maps of the staged epilogues, all with the 128-byte swizzle:
@@ -688,12 +701,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint64_t* raw_full = drain_bar + 2;                 // EPI_QPARTS: [STAGES]
-  uint64_t* conv_bar = raw_full + STAGES;             // EPI_QPARTS: [STAGES]
-  uint8_t* raw_base = smem + STAGES * C::STAGE_BYTES + C::OUT_BYTES + C::BAR_BYTES +
-                      C::SQK_BYTES + C::NGPT_BYTES;
+  uint64_t* raw_full = drain_bar + 2;                 // EPI_QPARTS: [RAW_STAGES]
+  uint64_t* raw_empty = raw_full + C::RAW_STAGES;     // EPI_QPARTS: [RAW_STAGES]
+  uint64_t* conv_bar = raw_empty + C::RAW_STAGES;     // EPI_QPARTS: [STAGES]
+  uint8_t* raw_base = smem + C::RAW_OFF;
   const int raw_row = C::QA ? (args.qfmt == 2 ? BK / 2 : BK) : 0;   // code bytes per row
   const uint32_t raw_bytes = (uint32_t)(BM * raw_row);
+  const int sc_kb = args.qfmt == 2 ? 4 : 2;           // scale bytes per row and k block
+  // codes and the 16-byte scale group of k block kb into raw stage s
+  auto raw_load = [&](int s, int kb, int m0) {
+    uint8_t* dst = raw_base + s * C::RAW_STAGE;
+    mbar_arrive_expect_tx(&raw_full[s], raw_bytes + C::RAW_SCALES);
+    tma_load_2d(dst, &tmA, &raw_full[s], kb * raw_row, m0);
+    tma_load_2d(dst + raw_bytes, &maps.q, &raw_full[s], (kb * sc_kb) & ~15, m0);
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = C::PARTS ? args.k_splits : 1;
@@ -717,10 +738,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     if (C::QA) {
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < C::RAW_STAGES; ++s) {
         mbar_init(&raw_full[s], 1);
-        mbar_init(&conv_bar[s], 4);                 // one arrival per converter warp
+        mbar_init(&raw_empty[s], 4);                // one arrival per converter warp
       }
+      for (int s = 0; s < STAGES; ++s) mbar_init(&conv_bar[s], 4);
     }
     if (C::NGPT) {
       mbar_init(ns.bar_y, 1);
@@ -734,6 +756,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
     }
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (C::QA) tma_prefetch_desc(&maps.q);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -762,7 +785,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
   // weights of the first ring stages, before the wait on the previous kernel
   // (each stage's barrier expects the whole stage; the activations complete it)
   int n_pre = 0;
-  if (args.w_pre && warp == 0 && lane == 0) {
+  if (args.w_pre && !C::QA && warp == 0 && lane == 0) {
     for (int tile = blockIdx.x; tile < num_tiles && n_pre < STAGES; tile += gridDim.x) {
       int m0, nb0, nb1, kb_lo, kb_hi;
       coords(tile, m0, nb0, nb1);
@@ -770,11 +793,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
       for (int kb = kb_lo; kb < kb_hi && n_pre < STAGES; ++kb, ++n_pre) {
         uint8_t* a_dst = smem + n_pre * C::STAGE_BYTES;
         uint8_t* b_dst = a_dst + C::A_BYTES;
-        if (C::QA) {                                // the codes; the activations follow
-          mbar_arrive_expect_tx(&raw_full[n_pre], raw_bytes);
-          tma_load_2d(raw_base + n_pre * C::RAW_STAGE, &tmA, &raw_full[n_pre], kb * raw_row, m0);
-          continue;
-        }
         mbar_arrive_expect_tx(&full_bar[n_pre], C::STAGE_BYTES);
         if (EPI == EPI_PARTS) {
           tma_load_2d(a_dst, &tmA, &full_bar[n_pre], kb * BK, m0);
@@ -786,9 +804,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
     }
   }
   // set-up above overlaps the previous kernel; global memory it may have
-  // written only from here
-  pdl_wait();
-  pdl_trigger();
+  // written only from here (the code loads and their expansion read weights
+  // only and start at once)
+  if (!(C::QA && warp >= 10)) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -807,17 +828,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
           }
           uint8_t* a_dst = smem + stage * C::STAGE_BYTES;
           uint8_t* b_dst = a_dst + C::A_BYTES;
-          if (C::QA) {
-            // activations into the ring; codes into the raw stage (free: the
-            // MMA that released this stage read the tile converted from it)
+          if (C::QA) {                              // activations; warp 14 loads the codes
             mbar_arrive_expect_tx(&full_bar[stage], C::B_BYTES);
             tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
             tma_load_2d(b_dst + C::B_BYTES / 2, &tmB, &full_bar[stage], kb * BK, nb1);
-            if (g >= n_pre) {
-              mbar_arrive_expect_tx(&raw_full[stage], raw_bytes);
-              tma_load_2d(raw_base + stage * C::RAW_STAGE, &tmA, &raw_full[stage], kb * raw_row,
-                          m0);
-            }
           } else if (g < n_pre) {                   // weights already on their way
             if (EPI == EPI_PARTS) {
               tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, nb0);
@@ -888,6 +902,32 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
       mbar_wait_bounded(drain_bar, 0, args.status, DEV_GEMM_DRAIN);
     }
     __syncwarp();
+  } else if (C::QA && warp == 14) {
+    // ------------------------------------------------ code loads (warp 14)
+    if (lane == 0) {
+      int rs = 0;
+      uint32_t rph = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        int m0, nb0, nb1, kb_lo, kb_hi;
+        coords(tile, m0, nb0, nb1);
+        kb_range(tile, kb_lo, kb_hi);
+        bool ok = true;
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait_bounded(&raw_empty[rs], rph ^ 1, args.status, DEV_GEMM_PRODUCER)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          raw_load(rs, kb, m0);
+          if (++rs == C::RAW_STAGES) {
+            rs = 0;
+            rph ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
   } else if (C::QA && warp >= 10) {
     // ------------------------------------------------ code expansion (warps 10..13)
     // thread r expands row r of each tile's k block into the bf16 A stage
@@ -895,9 +935,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
     // (and the NVFP4 row scale): the values of the dequantised bf16 matrix
     const int r = threadIdx.x - 320;
     const bool fp4 = args.qfmt == 2;
-    const int spr = fp4 ? args.K / 16 : args.K / 32;
-    int stage = 0;
-    uint32_t phase = 0;
+    // the raw rows carry the 64-byte (MXFP8) / 32-byte (NVFP4) swizzle:
+    // 16-byte chunk q of row r sits at chunk q ^ sw of the row
+    const int sw = fp4 ? (r >> 2) & 1 : (r >> 1) & 3;
+    int stage = 0, rst = 0;
+    uint32_t phase = 0, rph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok && !*abort_flag; tile += gridDim.x) {
       int m0, nb0, nb1, kb_lo, kb_hi;
@@ -910,25 +952,29 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
         const bool w_ok =
             !*abort_flag &&
             mbar_wait_bounded(&empty_bar[stage], phase ^ 1, args.status, DEV_GEMM_CONV) &&
-            mbar_wait_bounded(&raw_full[stage], phase, args.status, DEV_GEMM_CONV);
+            mbar_wait_bounded(&raw_full[rst], rph, args.status, DEV_GEMM_CONV);
         if (!__all_sync(0xffffffffu, w_ok)) {
           *abort_flag = 1;
           ok = false;
           break;
         }
         uint8_t* a_st = smem + stage * C::STAGE_BYTES;
-        const uint4* raw = reinterpret_cast<const uint4*>(raw_base + stage * C::RAW_STAGE +
+        const uint4* raw = reinterpret_cast<const uint4*>(raw_base + rst * C::RAW_STAGE +
                                                           r * raw_row);
+        // this k block's scales: bytes (kb sc_kb) mod 16 .. of the row's group
+        const uint32_t sword = *reinterpret_cast<const uint32_t*>(
+            raw_base + rst * C::RAW_STAGE + raw_bytes + r * 16 + ((kb * sc_kb) & 12));
         uint32_t pk[32];
         if (!rv) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = 0u;
         } else if (!fp4) {
-          const uint8_t* sc = args.qscales + (long long)row * spr + kb * 2;
-          const float s0 = e8m0_to_f32(sc[0]), s1 = e8m0_to_f32(sc[1]);
+          const uint32_t sh = 8 * ((kb * 2) & 3);
+          const float s0 = e8m0_to_f32((sword >> sh) & 0xFFu),
+                      s1 = e8m0_to_f32((sword >> (sh + 8)) & 0xFFu);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 v = raw[q];
+            const uint4 v = raw[q ^ sw];
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
             const float s = q < 2 ? s0 : s1;
 #pragma unroll
@@ -940,11 +986,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
             }
           }
         } else {
-          const uint32_t s4 =
-              *reinterpret_cast<const uint32_t*>(args.qscales + (long long)row * spr + kb * 4);
+          const uint32_t s4 = sword;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            const uint4 v = raw[q];
+            const uint4 v = raw[q ^ sw];
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {                  // 8 codes of block 2q + t / 2
@@ -964,10 +1009,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::THREADS, 1)
                                                 pk[4 * j + 3]);
         fence_proxy_async_smem();                   // visible to the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive(&conv_bar[stage]);
+        if (lane == 0) {
+          mbar_arrive(&conv_bar[stage]);
+          mbar_arrive(&raw_empty[rst]);              // this warp's reads of the raw stage are done
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++rst == C::RAW_STAGES) {
+          rst = 0;
+          rph ^= 1;
         }
       }
     }

@@ -158,6 +158,10 @@ def test_path_switches_validate_arguments(L):
         assert L.dory_set_fused_ngpt(h, 1) == dory.DORY_OK
         assert L.dory_set_tc_attention(h, 3) == dory.DORY_EINVAL
         assert L.dory_set_tc_attention(h, 0) == dory.DORY_OK
+        assert L.dory_set_quantized_swap(None, 1) == dory.DORY_EINVAL
+        assert L.dory_set_quantized_swap(h, 2) == dory.DORY_EINVAL
+        assert L.dory_set_quantized_swap(h, 1) == dory.DORY_OK
+        assert L.dory_set_quantized_swap(h, 0) == dory.DORY_OK
     finally:
         assert L.dory_destroy(h) == dory.DORY_OK
 

@@ -109,8 +109,8 @@ def test_4b_width_chunked_prefill_then_decode(dev, weights, mode):
 
 @pytest.mark.parametrize("B", [5, 16])
 def test_4b_width_few_row_decode(dev, weights, model_last, B):
-    """Decode batches of 5..16 sequences take the few-row projections (bulk-copy
-    weight streaming, activation rows held for up to 16 sequences): the
+    """Decode batches of 5 and 16 sequences: the swapped tensor-core GEMM with
+    a part-filled activation operand (rows past B read as zeros): the
     4B-width model at k = 2, two decode steps after a short prefill, against
     the oracle."""
     k, T, D = 2, 24, 2

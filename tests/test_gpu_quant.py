@@ -110,13 +110,14 @@ def test_quantize_refusals(dev):
                                   None, None, None) == dev.DORY_EINVAL
 
 
-def _run_model(dev, shape, w, fmt, mode, k, B, T, D, seed, chunk=0, qw=None):
+def _run_model(dev, shape, w, fmt, mode, k, B, T, D, seed, chunk=0, qw=None, swap=False):
     if qw is None:
         qw, _ = quant.quantize_weights(w, fmt)
     o = oracle.Oracle(shape, qw, dtype=np.float64 if shape.d <= 256 else np.float32)
     m = dev.Model(shape, w, max_batch=B, max_ctx=T + D + 24, max_chunk=max(T, 16), k_max=k,
                   cache_mode=mode)
     m.quantize(fmt)
+    m.set_quantized_swap(swap)
     prompt = synth.tokens(shape, B, T, seed=seed)
     r = o.prefill(prompt, k, mode, all_logits=True)
     lg = m.prefill(_tok(prompt), k, mode).cpu().numpy()
@@ -196,6 +197,7 @@ def test_quantized_batched_decode_equals_dequantised_copy(dev, weights_3l, fmt):
     a = dev.Model(SHAPE_3L, weights_3l, max_batch=B, max_ctx=64, max_chunk=T, k_max=k)
     b = dev.Model(SHAPE_3L, weights_3l, max_batch=B, max_ctx=64, max_chunk=T, k_max=k)
     a.quantize(fmt)
+    a.set_quantized_swap(True)
     b.quantize(fmt)
     b.quantize(dev.QUANT_NONE)                       # the same values, as bf16 matrices
     la, lb = a.prefill(_tok(prompt), k), b.prefill(_tok(prompt), k)
@@ -215,4 +217,4 @@ def test_quantized_batched_decode_equals_dequantised_copy(dev, weights_3l, fmt):
 def test_quantized_batched_decode_4b_width(dev, weights_3l, fmt):
     qw, _ = quant.quantize_weights(weights_3l, fmt)
     _run_model(dev, SHAPE_3L, weights_3l, fmt, oracle.LAST_LOOP, k=2, B=20, T=9, D=2, seed=61,
-               qw=qw)
+               qw=qw, swap=True)
