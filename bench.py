@@ -1060,7 +1060,7 @@ def run_workload_4b(args):
                         # the bf16 copy unless the swapped GEMM expands the
                         # codes (timed as well below)
                         swap_rows = 1 < B <= 128
-                        wq = wb if fmt and B == 1 else 2 * sum(layer_params(sh).values())
+                        wq = wb if fmt and B == 1 else quant_weight_bytes(sh, 0)
                         w = by["weights"] - 2 * sum(layer_params(sh).values()) * na \
                             + wq * na // sh.n_layers
                         gbs = (w + by["kv"]) / (ms / 1e3) / 1e9
@@ -1073,7 +1073,7 @@ def run_workload_4b(args):
                             m.set_quantized_swap(True)
                             ms_s = _graph_time(fn, st, warm=1, reps=3) / D
                             m.set_quantized_swap(False)
-                            w_s = w - (2 * sum(layer_params(sh).values()) - wb) * na // sh.n_layers
+                            w_s = w - (quant_weight_bytes(sh, 0) - wb) * na // sh.n_layers
                             r[f"B{B}_ctx{ctx}_k{k}"]["codes_in_swapped_gemm"] = {
                                 "ms_per_step": round(ms_s, 3),
                                 "bytes_per_step_GB": round((w_s + by["kv"]) / 1e9, 2)}
