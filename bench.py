@@ -1341,6 +1341,7 @@ def run_profile_target_4b(args):
     md = dory.Model(sh, w, max_batch=B, max_ctx=ctx64(ctx + 1), max_chunk=1, k_max=4)
     if args.quant:
         md.quantize(args.quant)
+        md.set_quantized_swap(True)       # batches of 2-128: codes expanded in the GEMM
     fill_cache_synthetic(md, sh)
     md.set_length(B, ctx)
     first = torch.tensor(synth.tokens(sh, B, 1, seed=5000)[:, 0], device="cuda")
@@ -1403,7 +1404,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=HEAD_B,
                     help="decode sequences of the 4B-class profile target")
     ap.add_argument("--quant", type=int, default=0, choices=[0, 1, 2],
-                    help="profile target: quantise the decode model (1 MXFP8, 2 NVFP4)")
+                    help="profile target: quantise the decode model (1 MXFP8, 2 NVFP4); "
+                         "batches of 2-128 expand the codes inside the swapped GEMM")
     ap.add_argument("--decode-only", action="store_true",
                     help="4B-class profile target: skip the prefill")
     ap.add_argument("--workload", choices=["headline4b", "small", "prefill4b", "decode4b",
