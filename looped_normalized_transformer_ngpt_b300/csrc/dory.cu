@@ -821,7 +821,7 @@ struct dory_model {
   std::vector<dory_layer_weights> layers;
   int qfmt = 0;                          // DORY_QUANT_* of the few-row projections
   std::vector<dory_qlayer> qlayers;
-  int q_swap = 0;                        // 17-128 rows: expand the codes in the swapped GEMM
+  int q_swap = 0;                        // 2-128 rows: expand the codes in the swapped GEMM
   const void* embed_in = nullptr;
   const void* embed_out = nullptr;
   const float* s_z = nullptr;
