@@ -109,11 +109,16 @@ __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __
   const long long row = blockIdx.x;
   const int nch = d / 8;
   float yv[kRowMaxChunks][8];
+  // h and alpha are loaded with y (one memory round trip before the first
+  // reduction instead of two around it)
+  float hv[kRowMaxChunks][8], av[kRowMaxChunks][8];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kRowMaxChunks; ++j) {
     const int ch = threadIdx.x + j * kRowThreads;
     if (ch < nch) {
+      load8(h32 + row * d + ch * 8, hv[j]);
+      load8(alpha + ch * 8, av[j]);
       load8(y + row * d + ch * 8, yv[j]);
       for (int p = 1; p < n_parts; ++p) {
         float t[8];
@@ -131,12 +136,9 @@ __global__ void __launch_bounds__(kRowThreads) ngpt_update_kernel(float* h32, __
   for (int j = 0; j < kRowMaxChunks; ++j) {
     const int ch = threadIdx.x + j * kRowThreads;
     if (ch < nch) {
-      float hv[8], av[8];
-      load8(h32 + row * d + ch * 8, hv);
-      load8(alpha + ch * 8, av);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float u = hv[i] + av[i] * (yv[j][i] * inv_y - hv[i]);
+        const float u = hv[j][i] + av[j][i] * (yv[j][i] * inv_y - hv[j][i]);
         yv[j][i] = u;
         su += u * u;
       }
