@@ -1,4 +1,5 @@
-// gemv.cuh - projections for few rows (decode: M = batch <= 16).
+// gemv.cuh - projections for few rows (M <= 16: prefill chunks, the
+// verifier's rows, the quantised one-sequence decode).
 //
 // With M <= 16 rows the projections stream weights (2 M FLOP per 2-byte
 // weight): the bound is HBM bandwidth and load latency, not the tensor cores.

@@ -1,4 +1,4 @@
-// gemv_tma.cuh - projections for few rows (decode, M <= 16) with the weights
+// gemv_tma.cuh - projections for few rows (M <= 16) with the weights
 // streamed into shared memory by bulk copies.
 //
 // Same operation as gemv_kernel (gemv.cuh), including the SwiGLU pair and
