@@ -328,7 +328,10 @@ DORY_API int dory_set_quantized_weights(dory_t* m, int fmt, const dory_qlayer* l
 
 /* stream_codes 1: decode steps of 2 to 128 sequences run their quantised
  * projections through the swapped GEMM that expands the codes in shared
- * memory; 0 (the default): they read the dequantised bf16 matrices.  Both
+ * memory (projections whose K is a multiple of 512 for MXFP8 or 256 for
+ * NVFP4, so that a row's block scales come in 16-byte groups; the others
+ * keep the bf16 matrices); 0 (the default): they read the dequantised bf16
+ * matrices.  Both
  * give bit-identical results.  The default is the faster one on B300 for
  * the 4B-class decode shapes: those GEMMs are short and latency-bound, so
  * halving or quartering their weight bytes does not shorten them, and the
